@@ -1,0 +1,374 @@
+// C ABI of the DBSCAN library: argument validation, workspace layout and the
+// order of the kernel stages.
+//
+// Stage order ("Design and optimization of DBSCAN Algorithm based on CUDA",
+// §I lists the three GPU steps: all-pair distances, core points + primitive
+// clusters, merging):
+//   prep     ranges, centring, norms, thresholds, tiled staging      O(N d)
+//   count    fused distance + neighbour count over the upper
+//            triangle of tiles (§IV-B1, §IV-B2)                      O(N^2 d)
+//   compact  core flags, stable compaction of cores and candidates   O(N)
+//   union    core-core sweep hooking a lock-free union-find          O(Nc^2 d)
+//   flatten  labels of core points                                   O(Nc)
+//   border   candidates x cores, smallest neighbouring label         O(Nb Nc d)
+//   finalize candidates without a core neighbour become noise        O(Nb)
+// Nothing of size N x N is ever stored.
+#include "dbscan_internal.cuh"
+
+#include <math.h>
+#include <mutex>
+#include <set>
+#include <vector>
+
+namespace dbscan {
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+Layout make_layout(int64_t n, int32_t d) {
+    Layout L{};
+    L.n = n;
+    L.d = d;
+    L.ntiles = (n + BT - 1) / BT;
+    L.tile_floats = (size_t)(d + 1) * BT;
+    const size_t staged = (size_t)L.ntiles * L.tile_floats * sizeof(float);
+    const size_t per_pt = (size_t)L.ntiles * BT * sizeof(float);
+    L.nscan_blocks = (n + SCAN_BLOCK - 1) / SCAN_BLOCK;
+    size_t off = 0;
+    L.off_ctrl = off;        off += align256(sizeof(Ctrl));
+    L.off_stats = off;       off += align256((size_t)3 * DBSCAN_MAX_D * sizeof(int));
+    L.off_staged_all = off;  off += align256(staged);
+    L.off_staged_core = off; off += align256(staged);
+    L.off_staged_cand = off; off += align256(staged);
+    L.off_T_all = off;       off += align256(per_pt);
+    L.off_T_core = off;      off += align256(per_pt);
+    L.off_T_cand = off;      off += align256(per_pt);
+    L.off_cnt = off;         off += align256(per_pt);
+    L.off_cidx = off;        off += align256(per_pt);
+    L.off_candidx = off;     off += align256(per_pt);
+    L.off_parent = off;      off += align256(per_pt);
+    L.off_clabel = off;      off += align256(per_pt);
+    L.off_bsum = off;        off += align256((size_t)2 * (L.nscan_blocks + 1) * sizeof(int));
+    L.total = off;
+    return L;
+}
+
+Work carve(void *base, const Layout &L) {
+    char *b = static_cast<char *>(base);
+    Work w{};
+    w.ctrl = reinterpret_cast<Ctrl *>(b + L.off_ctrl);
+    w.stat_min = reinterpret_cast<int *>(b + L.off_stats);
+    w.stat_max = w.stat_min + DBSCAN_MAX_D;
+    w.centre = reinterpret_cast<float *>(w.stat_max + DBSCAN_MAX_D);
+    w.staged_all = reinterpret_cast<float *>(b + L.off_staged_all);
+    w.staged_core = reinterpret_cast<float *>(b + L.off_staged_core);
+    w.staged_cand = reinterpret_cast<float *>(b + L.off_staged_cand);
+    w.T_all = reinterpret_cast<float *>(b + L.off_T_all);
+    w.T_core = reinterpret_cast<float *>(b + L.off_T_core);
+    w.T_cand = reinterpret_cast<float *>(b + L.off_T_cand);
+    w.cnt = reinterpret_cast<int *>(b + L.off_cnt);
+    w.cidx = reinterpret_cast<int *>(b + L.off_cidx);
+    w.candidx = reinterpret_cast<int *>(b + L.off_candidx);
+    w.parent = reinterpret_cast<int *>(b + L.off_parent);
+    w.clabel = reinterpret_cast<int *>(b + L.off_clabel);
+    w.bsum = reinterpret_cast<int *>(b + L.off_bsum);
+    return w;
+}
+
+// Host-side checks that need no GPU.
+static int check_shape(int64_t n, int32_t d, int32_t dtype) {
+    if (n < 0 || d < 1) return DBSCAN_ERR_INVALID_ARG;
+    if (dtype != DBSCAN_F32 && dtype != DBSCAN_BF16) return DBSCAN_ERR_INVALID_ARG;
+    if (n > 0x7fffffffLL) return DBSCAN_ERR_UNSUPPORTED;
+    if (d > DBSCAN_MAX_D) return DBSCAN_ERR_UNSUPPORTED;
+    if (dtype == DBSCAN_BF16 && (d % 16) != 0) return DBSCAN_ERR_UNSUPPORTED;
+    return DBSCAN_OK;
+}
+
+static int check_scalars(float eps, int32_t min_pts) {
+    if (!(eps >= 0.f) || isinf(eps)) return DBSCAN_ERR_INVALID_ARG;
+    if (min_pts < 1) return DBSCAN_ERR_INVALID_ARG;
+    return DBSCAN_OK;
+}
+
+// A kernel given a host pointer would fault; reject anything the device
+// cannot address as device or managed memory.
+static int check_device_ptr(const void *p) {
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return DBSCAN_ERR_INVALID_ARG;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return DBSCAN_ERR_INVALID_ARG;
+    return DBSCAN_OK;
+}
+
+// Keep freed stream-ordered allocations in the device's pool between calls
+// (once per device, for this process only).
+static void keep_pool(void) {
+    static std::mutex mu;
+    static std::set<int> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count(dev)) return;
+    cudaMemPool_t pool;
+    if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+        uint64_t thr = 8ull << 30;
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+    }
+    done.insert(dev);
+}
+
+// ---- stage timing ------------------------------------------------------------
+// Kernels launched by each stage: prep 4, count 1, compact 4, union 1,
+// flatten 1, border 1, finalize 1.
+static const int kStageLaunches[DBSCAN_NUM_STAGES] = {4, 1, 4, 1, 1, 1, 1};
+
+struct ProfCall {
+    cudaEvent_t ev[DBSCAN_NUM_STAGES + 1];
+    int stages;   // number of stages the call ran
+};
+struct ProfState {
+    bool on = false;
+    bool failed = false;
+    std::vector<ProfCall> calls;
+};
+static thread_local ProfState g_prof;
+
+struct StageMarks {
+    ProfCall call{};
+    bool on = false;
+    int next = 0;
+    explicit StageMarks(cudaStream_t s) {
+        if (!g_prof.on) return;
+        for (int i = 0; i <= DBSCAN_NUM_STAGES; ++i) {
+            if (cudaEventCreate(&call.ev[i]) != cudaSuccess) {
+                for (int j = 0; j < i; ++j) cudaEventDestroy(call.ev[j]);
+                g_prof.failed = true;
+                return;
+            }
+        }
+        on = true;
+        mark(s);
+    }
+    void mark(cudaStream_t s) {
+        if (on && next <= DBSCAN_NUM_STAGES) cudaEventRecord(call.ev[next++], s);
+    }
+    void done() {
+        if (!on) return;
+        call.stages = next - 1;
+        for (int i = next; i <= DBSCAN_NUM_STAGES; ++i) cudaEventDestroy(call.ev[i]);
+        g_prof.calls.push_back(call);
+        on = false;
+    }
+    ~StageMarks() { done(); }
+};
+
+// Launch every stage; cnt_out != NULL stops after the count and copies it out.
+static int run(const void *points, int dtype, int64_t n, int d, float eps, int min_pts,
+               int32_t *labels, uint8_t *is_core, int32_t *cnt_out, void *ws, const Layout &L,
+               cudaStream_t s) {
+    Work w = carve(ws, L);
+    StageMarks marks(s);
+    if (cudaMemsetAsync(w.ctrl, 0, sizeof(Ctrl), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+    if (cudaMemsetAsync(w.cnt, 0, (size_t)n * sizeof(int), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+    if (launch_prep(points, dtype, n, d, eps, w, L, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+    marks.mark(s);
+    if (launch_count(w, L, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+    marks.mark(s);
+    if (cnt_out) {
+        if (cudaMemcpyAsync(cnt_out, w.cnt, (size_t)n * sizeof(int), cudaMemcpyDeviceToDevice, s) !=
+            cudaSuccess)
+            return DBSCAN_ERR_CUDA;
+        return DBSCAN_OK;
+    }
+    if (launch_compact(w, L, min_pts, labels, is_core, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+    marks.mark(s);
+    if (launch_union(w, L, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+    marks.mark(s);
+    if (launch_flatten(w, L, labels, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+    marks.mark(s);
+    if (launch_border(w, L, labels, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+    marks.mark(s);
+    if (launch_finalize(w, L, labels, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+    marks.mark(s);
+    return DBSCAN_OK;
+}
+
+static int read_status(const void *ws, cudaStream_t s) {
+    int err = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+    if (cudaMemcpy(&err, &static_cast<const Ctrl *>(ws)->err, sizeof(int), cudaMemcpyDeviceToHost) !=
+        cudaSuccess)
+        return DBSCAN_ERR_CUDA;
+    return err;
+}
+
+// Shared body of dbscan_fit_ex and dbscan_neighbor_counts.
+static int fit_common(const void *points, int32_t dtype, int64_t n, int32_t d, float eps,
+                      int32_t min_pts, int32_t *labels, uint8_t *is_core, int32_t *cnt_out,
+                      void *workspace, size_t workspace_bytes, void *stream) {
+    int st = check_shape(n, d, dtype);
+    if (st != DBSCAN_OK) return st;
+    if ((st = check_scalars(eps, min_pts)) != DBSCAN_OK) return st;
+    if (n == 0) return DBSCAN_OK;
+    if (!points) return DBSCAN_ERR_INVALID_ARG;
+    if (!cnt_out && (!labels || !is_core)) return DBSCAN_ERR_INVALID_ARG;
+    const Layout L = make_layout(n, d);
+    if (workspace) {
+        if (workspace_bytes < L.total) return DBSCAN_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255) return DBSCAN_ERR_INVALID_ARG;
+    }
+    if (check_device_ptr(points) != DBSCAN_OK) return DBSCAN_ERR_INVALID_ARG;
+    if (cnt_out) {
+        if (check_device_ptr(cnt_out) != DBSCAN_OK) return DBSCAN_ERR_INVALID_ARG;
+    } else {
+        if (check_device_ptr(labels) != DBSCAN_OK || check_device_ptr(is_core) != DBSCAN_OK)
+            return DBSCAN_ERR_INVALID_ARG;
+    }
+    if (workspace && check_device_ptr(workspace) != DBSCAN_OK) return DBSCAN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (workspace)
+        return run(points, dtype, n, d, eps, min_pts, labels, is_core, cnt_out, workspace, L, s);
+
+    keep_pool();
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, L.total, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DBSCAN_ERR_ALLOC;
+    }
+    st = run(points, dtype, n, d, eps, min_pts, labels, is_core, cnt_out, ws, L, s);
+    int dev_st = read_status(ws, s);
+    cudaFreeAsync(ws, s);
+    if (cudaStreamSynchronize(s) != cudaSuccess && st == DBSCAN_OK) st = DBSCAN_ERR_CUDA;
+    return st != DBSCAN_OK ? st : dev_st;
+}
+
+}  // namespace dbscan
+
+using namespace dbscan;
+
+extern "C" {
+
+size_t dbscan_workspace_size(int64_t n, int32_t d, int32_t dtype) {
+    if (check_shape(n, d, dtype) != DBSCAN_OK) return 0;
+    if (n == 0) return 256;
+    return make_layout(n, d).total;
+}
+
+const char *dbscan_strerror(int status) {
+    switch (status) {
+    case DBSCAN_OK: return "DBSCAN_OK";
+    case DBSCAN_ERR_INVALID_ARG: return "DBSCAN_ERR_INVALID_ARG: invalid argument";
+    case DBSCAN_ERR_UNSUPPORTED: return "DBSCAN_ERR_UNSUPPORTED: unsupported shape or type";
+    case DBSCAN_ERR_ALLOC: return "DBSCAN_ERR_ALLOC: workspace allocation failed";
+    case DBSCAN_ERR_CUDA: return "DBSCAN_ERR_CUDA: CUDA runtime error";
+    case DBSCAN_ERR_INTERNAL: return "DBSCAN_ERR_INTERNAL: device iteration cap reached";
+    default: return "DBSCAN: unknown status";
+    }
+}
+
+int dbscan_fit_ex(const void *points, int32_t dtype, int64_t n, int32_t d, float eps,
+                  int32_t min_pts, int32_t *labels_out, uint8_t *is_core_out, void *workspace,
+                  size_t workspace_bytes, void *stream) {
+    return fit_common(points, dtype, n, d, eps, min_pts, labels_out, is_core_out, nullptr,
+                      workspace, workspace_bytes, stream);
+}
+
+int dbscan_fit(const float *points, int64_t n, int32_t d, float eps, int32_t min_pts,
+               int32_t *labels_out, uint8_t *is_core_out) {
+    return fit_common(points, DBSCAN_F32, n, d, eps, min_pts, labels_out, is_core_out, nullptr,
+                      nullptr, 0, nullptr);
+}
+
+int dbscan_neighbor_counts(const void *points, int32_t dtype, int64_t n, int32_t d, float eps,
+                           int32_t *cnt_out, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+    return fit_common(points, dtype, n, d, eps, 1, nullptr, nullptr, cnt_out, workspace,
+                      workspace_bytes, stream);
+}
+
+int dbscan_profile_begin(void) {
+    for (auto &c : g_prof.calls)
+        for (int i = 0; i <= c.stages; ++i) cudaEventDestroy(c.ev[i]);
+    g_prof.calls.clear();
+    g_prof.failed = false;
+    g_prof.on = true;
+    return DBSCAN_OK;
+}
+
+int dbscan_profile_end(float *stage_ms, int32_t max_stages, int64_t *calls,
+                       int64_t *kernel_launches) {
+    float acc[DBSCAN_NUM_STAGES] = {0};
+    int64_t launches = 0;
+    int st = g_prof.failed ? DBSCAN_ERR_CUDA : DBSCAN_OK;
+    for (auto &c : g_prof.calls) {
+        for (int i = 0; i < c.stages; ++i) {
+            float ms = 0.f;
+            if (cudaEventSynchronize(c.ev[i + 1]) != cudaSuccess ||
+                cudaEventElapsedTime(&ms, c.ev[i], c.ev[i + 1]) != cudaSuccess)
+                st = DBSCAN_ERR_CUDA;
+            acc[i] += ms;
+            launches += kStageLaunches[i];
+        }
+        for (int i = 0; i <= c.stages; ++i) cudaEventDestroy(c.ev[i]);
+    }
+    if (calls) *calls = (int64_t)g_prof.calls.size();
+    if (kernel_launches) *kernel_launches = launches;
+    if (stage_ms)
+        for (int i = 0; i < max_stages && i < DBSCAN_NUM_STAGES; ++i) stage_ms[i] = acc[i];
+    g_prof.calls.clear();
+    g_prof.on = false;
+    return st;
+}
+
+int dbscan_workspace_status(const void *workspace, void *stream) {
+    if (!workspace) return DBSCAN_ERR_INVALID_ARG;
+    return read_status(workspace, static_cast<cudaStream_t>(stream));
+}
+
+int dbscan_fit_host(const void *points_host, int32_t dtype, int64_t n, int32_t d, float eps,
+                    int32_t min_pts, int32_t *labels_host, uint8_t *is_core_host, void *stream) {
+    int st = check_shape(n, d, dtype);
+    if (st != DBSCAN_OK) return st;
+    if ((st = check_scalars(eps, min_pts)) != DBSCAN_OK) return st;
+    if (n == 0) return DBSCAN_OK;
+    if (!points_host || !labels_host || !is_core_host) return DBSCAN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Layout L = make_layout(n, d);
+    const size_t esz = dtype == DBSCAN_BF16 ? 2 : 4;
+    const size_t pbytes = align256((size_t)n * d * esz);
+    const size_t lbytes = align256((size_t)n * sizeof(int32_t));
+    const size_t cbytes = align256((size_t)n);
+    keep_pool();
+    char *buf = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&buf), pbytes + lbytes + cbytes + L.total, s) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return DBSCAN_ERR_ALLOC;
+    }
+    void *dp = buf;
+    int32_t *dl = reinterpret_cast<int32_t *>(buf + pbytes);
+    uint8_t *dc = reinterpret_cast<uint8_t *>(buf + pbytes + lbytes);
+    void *ws = buf + pbytes + lbytes + cbytes;
+    st = DBSCAN_OK;
+    if (cudaMemcpyAsync(dp, points_host, (size_t)n * d * esz, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+        st = DBSCAN_ERR_CUDA;
+    if (st == DBSCAN_OK)
+        st = run(dp, dtype, n, d, eps, min_pts, dl, dc, nullptr, ws, L, s);
+    if (st == DBSCAN_OK &&
+        (cudaMemcpyAsync(labels_host, dl, (size_t)n * sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+             cudaSuccess ||
+         cudaMemcpyAsync(is_core_host, dc, (size_t)n, cudaMemcpyDeviceToHost, s) != cudaSuccess))
+        st = DBSCAN_ERR_CUDA;
+    int dev_st = read_status(ws, s);
+    cudaFreeAsync(buf, s);
+    if (cudaStreamSynchronize(s) != cudaSuccess && st == DBSCAN_OK) st = DBSCAN_ERR_CUDA;
+    return st != DBSCAN_OK ? st : dev_st;
+}
+
+}  // extern "C"

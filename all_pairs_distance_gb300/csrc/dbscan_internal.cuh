@@ -1,0 +1,105 @@
+// Internal definitions shared by the CUDA translation units of the DBSCAN
+// library: workspace layout, the device control block, launch wrappers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/dbscan.h"
+
+namespace dbscan {
+
+// Points are staged in tiles of BT points.  A tile holds, for each of the d
+// dimensions, the BT centred coordinates (structure of arrays), followed by
+// the BT squared norms: (d + 1) * BT floats, 512-byte aligned rows.
+constexpr int BT = 128;
+constexpr int SCAN_BLOCK = 1024;   // elements per block of the compaction scan
+
+// Sentinels for the padding slots of the last tile: a padding column has a
+// huge norm and never tests as a neighbour; a padding row has a hugely
+// negative threshold and never tests as a neighbour either.
+constexpr float PAD_NORM = 1.0e30f;
+constexpr float PAD_THRESH = -1.0e30f;
+
+// Device control block at offset 0 of every workspace.
+struct Ctrl {
+    int err;            // first device-side error (a dbscan_status), 0 = none
+    int n_core;         // number of core points
+    int n_cand;         // number of border candidates (non-core, count >= 2)
+    int nonint;         // set when a coordinate is not an integer
+    int nonfinite;      // set when a coordinate is NaN or infinite
+    int exact;          // 1 when the exactness bound holds (set by setup)
+    float thrx;         // row threshold constant, see prep.cu
+    int n_all;          // number of points
+    unsigned unit_ctr[4];   // work-unit counters of the three sweeps
+    float range_sq;     // sum_k (max_k - min_k)^2
+    int pad1[51];
+};
+static_assert(sizeof(Ctrl) == 256, "Ctrl must be 256 bytes");
+
+// Workspace carve-up (host side).  All offsets are 256-byte aligned.
+struct Layout {
+    int64_t n;
+    int32_t d;
+    int64_t ntiles;       // ceil(n / BT)
+    size_t tile_floats;   // (d + 1) * BT
+    size_t off_ctrl, off_stats, off_staged_all, off_staged_core, off_staged_cand;
+    size_t off_T_all, off_T_core, off_T_cand;
+    size_t off_cnt, off_cidx, off_candidx, off_parent, off_clabel, off_bsum;
+    int64_t nscan_blocks;
+    size_t total;
+};
+
+Layout make_layout(int64_t n, int32_t d);
+
+// Device pointers into one workspace.
+struct Work {
+    Ctrl *ctrl;
+    int *stat_min;        // [DBSCAN_MAX_D] ordered-int keys of per-dimension minima
+    int *stat_max;        // [DBSCAN_MAX_D] ordered-int keys of per-dimension maxima
+    float *centre;        // [DBSCAN_MAX_D] per-dimension centre
+    float *staged_all, *staged_core, *staged_cand;
+    float *T_all, *T_core, *T_cand;
+    int *cnt;             // [n] neighbour counts
+    int *cidx;            // [n] original index of each core point, ascending
+    int *candidx;         // [n] original index of each border candidate, ascending
+    int *parent;          // [n] union-find parents over core positions
+    int *clabel;          // [n] final label of each core position
+    int *bsum;            // [2 * nscan_blocks] per-block counts of the compaction scan
+};
+
+Work carve(void *base, const Layout &L);
+
+// Sweep modes.
+enum SweepMode { SWEEP_COUNT = 0, SWEEP_UNION = 1, SWEEP_BORDER = 2 };
+
+// ---- host launch wrappers (each returns cudaGetLastError()) ---------------
+cudaError_t launch_prep(const void *points, int dtype, int64_t n, int d, float eps,
+                        const Work &w, const Layout &L, cudaStream_t s);
+cudaError_t launch_count(const Work &w, const Layout &L, cudaStream_t s);
+cudaError_t launch_compact(const Work &w, const Layout &L, int min_pts,
+                           int32_t *labels, uint8_t *is_core, cudaStream_t s);
+cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s);
+cudaError_t launch_flatten(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
+cudaError_t launch_border(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
+cudaError_t launch_finalize(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
+
+int persistent_ctas(const void *kernel, int threads, size_t smem);
+
+// ---- device helpers --------------------------------------------------------
+__device__ __forceinline__ void set_error(Ctrl *c, int code) {
+    atomicCAS(&c->err, 0, code);
+}
+
+// Monotone map float -> int so that integer min/max order equals float order.
+__device__ __forceinline__ int float_key(float f) {
+    int b = __float_as_int(f);
+    return b >= 0 ? b : (b ^ 0x7fffffff);
+}
+__device__ __forceinline__ float key_float(int k) {
+    return __int_as_float(k >= 0 ? k : (k ^ 0x7fffffff));
+}
+
+}  // namespace dbscan

@@ -1,0 +1,486 @@
+// The tiled all-pairs sweeps: neighbour counting (pass 1), core-core
+// union-find (pass 2) and border assignment (pass 3).
+//
+// "Design and optimization of DBSCAN Algorithm based on CUDA" stages tiles of
+// points in shared memory (§IV-A3), unrolls the inner loop (§IV-A4), fuses
+// the distance evaluation with the neighbour count so no distance matrix is
+// stored (§IV-B1), and hoists the per-point terms of the squared distance out
+// of the loop (§IV-B2).  The sweeps here keep those ideas and change the rest
+// for sm_103a:
+//
+// * Work is a persistent grid pulling units (one 128-row block x a run of
+//   128-column tiles) from an atomic counter.  Counting and union sweep only
+//   the upper triangle of tiles (a pair is evaluated once and, in pass 1,
+//   credited to both points); the border sweep is a rectangle (candidates x
+//   cores).
+// * Column tiles stream through a 3-stage cp.async ring in shared memory; the
+//   tile layout (structure of arrays, 128 points per row) makes every load a
+//   conflict-free 16-byte vector.
+// * A thread owns 8 rows x 8 columns per tile.  Per pair the fast path does d
+//   fused multiply-adds (two pairs per packed f32x2 instruction for d <= 4)
+//   into v_ij = nrm_j - 2 c_i . c_j, and a three-input min per two pairs; a
+//   row whose minimum over its 8 columns is not below its threshold T_i has
+//   no neighbour there.  Only rows with a neighbour take the slow path, which
+//   re-tests the 8 pairs one by one and acts on each neighbour pair (count,
+//   union, or border label).  At the densities DBSCAN works at, almost all
+//   row-column blocks are empty, so the per-pair cost is the d FMAs plus half
+//   a min.
+#include "dbscan_internal.cuh"
+
+#include <mutex>
+#include <map>
+#include <utility>
+
+namespace dbscan {
+
+constexpr int THREADS = 256;
+constexpr int R = 8;           // rows per thread
+constexpr int C = 8;           // columns per thread per tile
+constexpr int UF_CAP = 1 << 22;  // iteration cap of union-find loops
+
+struct SweepArgs {
+    const float *rows;     // staged row points
+    const float *rowT;     // row thresholds
+    const int *n_rows;     // device-side row count
+    const float *cols;     // staged column points
+    const int *n_cols;     // device-side column count
+    int tri;               // 1: rows and cols are one set, sweep the upper triangle
+    unsigned *ctr;         // work-unit counter (zeroed before the launch)
+    Ctrl *ctrl;
+    int *cnt;              // pass 1: neighbour counts
+    int *parent;           // pass 2: union-find parents
+    const int *clabel;     // pass 3: label of each core position
+    const int *candidx;    // pass 3: original index of each candidate position
+    int32_t *labels;       // pass 3: labels (original order)
+};
+
+// Position of a thread's m-th row (or column) inside a 128-point tile.  Two
+// runs of four make each group of 8 threads read 128 contiguous bytes.
+__device__ __forceinline__ int slot_of(int g, int m) {
+    return (m < 4) ? (4 * g + m) : (64 + 4 * g + (m - 4));
+}
+
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// ---- union-find (parent[x] <= x always; roots are component minima) -------
+__device__ __noinline__ int uf_find(int *parent, int x, Ctrl *ctrl) {
+    for (int it = 0; it < UF_CAP; ++it) {
+        int p = __ldcg(parent + x);
+        if (p == x) return x;
+        int gp = __ldcg(parent + p);
+        if (gp != p) __stcg(parent + x, gp);   // path halving
+        x = gp;
+    }
+    set_error(ctrl, DBSCAN_ERR_INTERNAL);
+    return x;
+}
+
+__device__ __noinline__ void uf_unite(int *parent, int a, int b, Ctrl *ctrl) {
+    for (int it = 0; it < UF_CAP; ++it) {
+        a = uf_find(parent, a, ctrl);
+        b = uf_find(parent, b, ctrl);
+        if (a == b) return;
+        if (a < b) { int t = a; a = b; b = t; }
+        // hook the larger root under the smaller one
+        if (atomicCAS(parent + a, a, b) == a) return;
+    }
+    set_error(ctrl, DBSCAN_ERR_INTERNAL);
+}
+
+// ---- work units ------------------------------------------------------------
+struct Sched {
+    int nrt, nct, uc, kc;
+    unsigned units;
+};
+
+__device__ __forceinline__ Sched make_sched(int n_rows, int n_cols, int tri) {
+    Sched s;
+    s.nrt = (n_rows + BT - 1) / BT;
+    s.nct = (n_cols + BT - 1) / BT;
+    long long total = tri ? (long long)s.nrt * (s.nrt + 1) / 2 : (long long)s.nrt * s.nct;
+    long long target = 8LL * gridDim.x;
+    long long uc = (total + target - 1) / target;
+    if (uc < 1) uc = 1;
+    if (uc > s.nct) uc = s.nct;
+    s.uc = (int)uc;
+    s.kc = (s.nct + s.uc - 1) / s.uc;
+    s.units = (unsigned)((long long)s.nrt * s.kc);
+    return s;
+}
+
+// Unit u -> row tile rb and column tiles [t0, t1); false when empty.
+__device__ __forceinline__ bool decode_unit(unsigned u, const Sched &s, int tri, int &rb,
+                                            int &t0, int &t1) {
+    rb = (int)(u / s.kc);
+    int c = (int)(u % s.kc);
+    t0 = tri ? rb + c * s.uc : c * s.uc;
+    if (t0 >= s.nct) return false;
+    t1 = min(t0 + s.uc, s.nct);
+    return true;
+}
+
+// ---- per-neighbour-pair actions -------------------------------------------
+template <int MODE>
+__device__ __forceinline__ void on_neighbour(const SweepArgs &a, int p, int q, bool diag,
+                                             int &acc) {
+    if (MODE == SWEEP_COUNT) {
+        if (diag && q < p) return;        // counted from the other side
+        acc += 1;
+        if (q != p) atomicAdd(a.cnt + q, 1);
+    } else if (MODE == SWEEP_UNION) {
+        if (diag && q <= p) return;
+        uf_unite(a.parent, p, q, a.ctrl);
+    } else {
+        acc = min(acc, __ldcg(a.clabel + q));
+    }
+}
+
+template <int MODE>
+__device__ __forceinline__ int acc_init() {
+    return MODE == SWEEP_BORDER ? 0x7fffffff : 0;
+}
+
+template <int MODE>
+__device__ __forceinline__ void flush_rows(const SweepArgs &a, int rb, int tr, int n_rows,
+                                           const int (&acc)[R]) {
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        int p = rb * BT + slot_of(tr, m);
+        if (p >= n_rows) continue;
+        if (MODE == SWEEP_COUNT) {
+            if (acc[m]) atomicAdd(a.cnt + p, acc[m]);
+        } else if (MODE == SWEEP_BORDER) {
+            if (acc[m] != 0x7fffffff) atomicMin(a.labels + a.candidx[p], acc[m]);
+        }
+    }
+}
+
+// Issue the cp.async copies of one stage (tiles [tfirst, tfirst + ntiles)).
+__device__ __forceinline__ void issue_stage(float *dst, const float *cols, int tfirst,
+                                            int ntiles, int tile_floats) {
+    const float *src = cols + (size_t)tfirst * tile_floats;
+    const int chunks = ntiles * tile_floats / 4;
+    for (int c = threadIdx.x; c < chunks; c += THREADS) cp_async16(dst + 4 * c, src + 4 * c);
+}
+
+// ===========================================================================
+// d <= 4: rows in registers, packed f32x2 FMAs.
+// ===========================================================================
+template <int D, int MODE>
+__global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
+    constexpr int TILE = (D + 1) * BT;
+    constexpr int CT = 4;   // tiles per stage
+    constexpr int S = 3;    // stages
+    extern __shared__ __align__(16) float smem[];
+    __shared__ unsigned s_unit;
+
+    const int tid = threadIdx.x;
+    const int tr = tid >> 4, tc = tid & 15;
+    const int n_rows = *a.n_rows, n_cols = *a.n_cols;
+    if (n_rows <= 0 || n_cols <= 0) return;
+    const Sched sc = make_sched(n_rows, n_cols, a.tri);
+
+    for (;;) {
+        if (tid == 0) s_unit = atomicAdd(a.ctr, 1u);
+        __syncthreads();
+        const unsigned u = s_unit;
+        __syncthreads();
+        if (u >= sc.units) break;
+        int rb, t0, t1;
+        if (!decode_unit(u, sc, a.tri, rb, t0, t1)) continue;
+
+        // rows of this unit: packed (-2c, -2c) and thresholds
+        float2 ra[R][D];
+        float rT[R];
+        {
+            const float *rt = a.rows + (size_t)rb * TILE;
+#pragma unroll
+            for (int k = 0; k < D; ++k) {
+                float4 lo = *reinterpret_cast<const float4 *>(rt + k * BT + 4 * tr);
+                float4 hi = *reinterpret_cast<const float4 *>(rt + k * BT + 64 + 4 * tr);
+                float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+                for (int m = 0; m < R; ++m) ra[m][k] = make_float2(-2.f * v[m], -2.f * v[m]);
+            }
+            const float *tt = a.rowT + (size_t)rb * BT;
+            float4 lo = *reinterpret_cast<const float4 *>(tt + 4 * tr);
+            float4 hi = *reinterpret_cast<const float4 *>(tt + 64 + 4 * tr);
+            rT[0] = lo.x; rT[1] = lo.y; rT[2] = lo.z; rT[3] = lo.w;
+            rT[4] = hi.x; rT[5] = hi.y; rT[6] = hi.z; rT[7] = hi.w;
+        }
+        int acc[R];
+#pragma unroll
+        for (int m = 0; m < R; ++m) acc[m] = acc_init<MODE>();
+
+        const int nst = (t1 - t0 + CT - 1) / CT;
+#pragma unroll
+        for (int s = 0; s < S - 1; ++s) {
+            if (s < nst) issue_stage(smem + s * CT * TILE, a.cols, t0 + s * CT,
+                                     min(CT, t1 - (t0 + s * CT)), TILE);
+            cp_async_commit();
+        }
+        for (int g = 0; g < nst; ++g) {
+            cp_async_wait<S - 2>();
+            __syncthreads();
+            {
+                int gn = g + S - 1;
+                if (gn < nst) issue_stage(smem + (gn % S) * CT * TILE, a.cols, t0 + gn * CT,
+                                          min(CT, t1 - (t0 + gn * CT)), TILE);
+                cp_async_commit();
+            }
+            const float *sb = smem + (g % S) * CT * TILE;
+            const int ntile = min(CT, t1 - (t0 + g * CT));
+            for (int q = 0; q < ntile; ++q) {
+                const int tile = t0 + g * CT + q;
+                const float *st = sb + q * TILE;
+                float xc[D + 1][C];
+#pragma unroll
+                for (int k = 0; k <= D; ++k) {
+                    float4 lo = *reinterpret_cast<const float4 *>(st + k * BT + 4 * tc);
+                    float4 hi = *reinterpret_cast<const float4 *>(st + k * BT + 64 + 4 * tc);
+                    xc[k][0] = lo.x; xc[k][1] = lo.y; xc[k][2] = lo.z; xc[k][3] = lo.w;
+                    xc[k][4] = hi.x; xc[k][5] = hi.y; xc[k][6] = hi.z; xc[k][7] = hi.w;
+                }
+                unsigned hit = 0;
+#pragma unroll
+                for (int m = 0; m < R; ++m) {
+                    float2 v[C / 2];
+#pragma unroll
+                    for (int p2 = 0; p2 < C / 2; ++p2) {
+                        float2 t = make_float2(xc[D][2 * p2], xc[D][2 * p2 + 1]);
+#pragma unroll
+                        for (int k = 0; k < D; ++k)
+                            t = __ffma2_rn(ra[m][k], make_float2(xc[k][2 * p2], xc[k][2 * p2 + 1]), t);
+                        v[p2] = t;
+                    }
+                    float mn = min3f(min3f(v[0].x, v[0].y, v[1].x), min3f(v[1].y, v[2].x, v[2].y),
+                                     fminf(v[3].x, v[3].y));
+                    hit |= (mn < rT[m]) ? (1u << m) : 0u;
+                }
+                if (hit) {
+                    const bool diag = a.tri && tile == rb;
+#pragma unroll
+                    for (int m = 0; m < R; ++m) {
+                        if (!((hit >> m) & 1u)) continue;
+                        const int p = rb * BT + slot_of(tr, m);
+#pragma unroll
+                        for (int c = 0; c < C; ++c) {
+                            float v = xc[D][c];
+#pragma unroll
+                            for (int k = 0; k < D; ++k) v = fmaf(ra[m][k].x, xc[k][c], v);
+                            if (v < rT[m]) on_neighbour<MODE>(a, p, tile * BT + slot_of(tc, c), diag, acc[m]);
+                        }
+                    }
+                }
+            }
+        }
+        cp_async_wait<0>();
+        flush_rows<MODE>(a, rb, tr, n_rows, acc);
+    }
+}
+
+// ===========================================================================
+// d > 4: rows and columns from shared memory, 8x8 register accumulators.
+// ===========================================================================
+template <int MODE, int S>
+__global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
+    extern __shared__ __align__(16) float smem[];
+    __shared__ unsigned s_unit;
+    const int TILE = (D + 1) * BT;
+    float *rowbuf = smem;                  // D * BT floats: -2 c of the row tile
+    float *stages = smem + D * BT;         // S * TILE floats
+
+    const int tid = threadIdx.x;
+    const int tr = tid >> 4, tc = tid & 15;
+    const int n_rows = *a.n_rows, n_cols = *a.n_cols;
+    if (n_rows <= 0 || n_cols <= 0) return;
+    const Sched sc = make_sched(n_rows, n_cols, a.tri);
+
+    for (;;) {
+        if (tid == 0) s_unit = atomicAdd(a.ctr, 1u);
+        __syncthreads();
+        const unsigned u = s_unit;
+        __syncthreads();
+        if (u >= sc.units) break;
+        int rb, t0, t1;
+        if (!decode_unit(u, sc, a.tri, rb, t0, t1)) continue;
+
+        {
+            const float *rt = a.rows + (size_t)rb * TILE;
+            for (int e = tid; e < D * BT; e += THREADS) rowbuf[e] = -2.f * rt[e];
+        }
+        float rT[R];
+        {
+            const float *tt = a.rowT + (size_t)rb * BT;
+            float4 lo = *reinterpret_cast<const float4 *>(tt + 4 * tr);
+            float4 hi = *reinterpret_cast<const float4 *>(tt + 64 + 4 * tr);
+            rT[0] = lo.x; rT[1] = lo.y; rT[2] = lo.z; rT[3] = lo.w;
+            rT[4] = hi.x; rT[5] = hi.y; rT[6] = hi.z; rT[7] = hi.w;
+        }
+        int acc[R];
+#pragma unroll
+        for (int m = 0; m < R; ++m) acc[m] = acc_init<MODE>();
+
+        const int nst = t1 - t0;   // one tile per stage
+#pragma unroll
+        for (int s = 0; s < S - 1; ++s) {
+            if (s < nst) issue_stage(stages + s * TILE, a.cols, t0 + s, 1, TILE);
+            cp_async_commit();
+        }
+        for (int g = 0; g < nst; ++g) {
+            cp_async_wait<S - 2>();
+            __syncthreads();
+            {
+                int gn = g + S - 1;
+                if (gn < nst) issue_stage(stages + (gn % S) * TILE, a.cols, t0 + gn, 1, TILE);
+                cp_async_commit();
+            }
+            const int tile = t0 + g;
+            const float *st = stages + (g % S) * TILE;
+            float v[R][C];
+            {
+                float4 lo = *reinterpret_cast<const float4 *>(st + D * BT + 4 * tc);
+                float4 hi = *reinterpret_cast<const float4 *>(st + D * BT + 64 + 4 * tc);
+                float nn[C] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+                for (int m = 0; m < R; ++m)
+#pragma unroll
+                    for (int c = 0; c < C; ++c) v[m][c] = nn[c];
+            }
+#pragma unroll 2
+            for (int k = 0; k < D; ++k) {
+                float4 rlo = *reinterpret_cast<const float4 *>(rowbuf + k * BT + 4 * tr);
+                float4 rhi = *reinterpret_cast<const float4 *>(rowbuf + k * BT + 64 + 4 * tr);
+                float4 xlo = *reinterpret_cast<const float4 *>(st + k * BT + 4 * tc);
+                float4 xhi = *reinterpret_cast<const float4 *>(st + k * BT + 64 + 4 * tc);
+                float rr[R] = {rlo.x, rlo.y, rlo.z, rlo.w, rhi.x, rhi.y, rhi.z, rhi.w};
+                float xx[C] = {xlo.x, xlo.y, xlo.z, xlo.w, xhi.x, xhi.y, xhi.z, xhi.w};
+#pragma unroll
+                for (int m = 0; m < R; ++m)
+#pragma unroll
+                    for (int c = 0; c < C; ++c) v[m][c] = fmaf(rr[m], xx[c], v[m][c]);
+            }
+            unsigned hit = 0;
+#pragma unroll
+            for (int m = 0; m < R; ++m) {
+                float mn = min3f(min3f(v[m][0], v[m][1], v[m][2]), min3f(v[m][3], v[m][4], v[m][5]),
+                                 fminf(v[m][6], v[m][7]));
+                hit |= (mn < rT[m]) ? (1u << m) : 0u;
+            }
+            if (hit) {
+                const bool diag = a.tri && tile == rb;
+#pragma unroll
+                for (int m = 0; m < R; ++m) {
+                    if (!((hit >> m) & 1u)) continue;
+                    const int p = rb * BT + slot_of(tr, m);
+#pragma unroll
+                    for (int c = 0; c < C; ++c)
+                        if (v[m][c] < rT[m]) on_neighbour<MODE>(a, p, tile * BT + slot_of(tc, c), diag, acc[m]);
+                }
+            }
+        }
+        cp_async_wait<0>();
+        flush_rows<MODE>(a, rb, tr, n_rows, acc);
+    }
+}
+
+// ===========================================================================
+// host side
+// ===========================================================================
+int persistent_ctas(const void *kernel, int threads, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_pair(dev, kernel);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int sms = 0, per = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, threads, smem);
+    if (per < 1) per = 1;
+    if (sms < 1) sms = 1;
+    int v = sms * per;
+    cache[key] = v;
+    return v;
+}
+
+template <int D, int MODE>
+static cudaError_t run_small(const SweepArgs &args, cudaStream_t s) {
+    auto kernel = k_sweep_small<D, MODE>;
+    const size_t smem = (size_t)3 * 4 * (D + 1) * BT * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute((const void *)kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = persistent_ctas((const void *)kernel, THREADS, smem);
+    kernel<<<grid, THREADS, smem, s>>>(args);
+    return cudaGetLastError();
+}
+
+template <int MODE, int S>
+static cudaError_t run_gen(const SweepArgs &args, int d, cudaStream_t s) {
+    auto kernel = k_sweep_gen<MODE, S>;
+    const size_t smem = ((size_t)d * BT + (size_t)S * (d + 1) * BT) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute((const void *)kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = persistent_ctas((const void *)kernel, THREADS, smem);
+    kernel<<<grid, THREADS, smem, s>>>(args, d);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+static cudaError_t dispatch(const SweepArgs &args, int d, cudaStream_t s) {
+    switch (d) {
+    case 1: return run_small<1, MODE>(args, s);
+    case 2: return run_small<2, MODE>(args, s);
+    case 3: return run_small<3, MODE>(args, s);
+    case 4: return run_small<4, MODE>(args, s);
+    default:
+        return d <= 32 ? run_gen<MODE, 3>(args, d, s) : run_gen<MODE, 2>(args, d, s);
+    }
+}
+
+cudaError_t launch_count(const Work &w, const Layout &L, cudaStream_t s) {
+    SweepArgs a{};
+    a.rows = w.staged_all; a.rowT = w.T_all; a.n_rows = &w.ctrl->n_all;
+    a.cols = w.staged_all; a.n_cols = &w.ctrl->n_all;
+    a.tri = 1; a.ctr = &w.ctrl->unit_ctr[SWEEP_COUNT]; a.ctrl = w.ctrl; a.cnt = w.cnt;
+    return dispatch<SWEEP_COUNT>(a, L.d, s);
+}
+
+cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
+    SweepArgs a{};
+    a.rows = w.staged_core; a.rowT = w.T_core; a.n_rows = &w.ctrl->n_core;
+    a.cols = w.staged_core; a.n_cols = &w.ctrl->n_core;
+    a.tri = 1; a.ctr = &w.ctrl->unit_ctr[SWEEP_UNION]; a.ctrl = w.ctrl; a.parent = w.parent;
+    return dispatch<SWEEP_UNION>(a, L.d, s);
+}
+
+cudaError_t launch_border(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s) {
+    SweepArgs a{};
+    a.rows = w.staged_cand; a.rowT = w.T_cand; a.n_rows = &w.ctrl->n_cand;
+    a.cols = w.staged_core; a.n_cols = &w.ctrl->n_core;
+    a.tri = 0; a.ctr = &w.ctrl->unit_ctr[SWEEP_BORDER]; a.ctrl = w.ctrl;
+    a.clabel = w.clabel; a.candidx = w.candidx; a.labels = labels;
+    return dispatch<SWEEP_BORDER>(a, L.d, s);
+}
+
+}  // namespace dbscan

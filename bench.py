@@ -1,0 +1,334 @@
+#!/usr/bin/env python3
+"""DBSCAN benchmark: pair evaluations per second (N^2 / t) and end-to-end ms.
+
+Default workload: blobs_1m_d3 (N = 1,000,000 integer points in [0, 2047]^3,
+500 Gaussian blobs sigma = 12, 3 filaments, 20% uniform noise; eps = 10,
+minPts = 8), seeded and synthetic.  One step = one full DBSCAN (prep, count,
+compact, union, flatten, border, finalize) on device-resident points; the L2
+is flushed (a 256 MiB write) between timed steps, outside the timed events.
+
+Prints ONE JSON line on rank 0.  ``--impl reference`` times the CPU oracle
+instead (bounded samples of the same workload, on the host cores).
+Under torchrun (N > 1) each rank runs an independent replica of the workload
+(no data-path collective); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "DBSCAN pair evals/s (N²/t) and end-to-end ms at N=1M, d=3, one GB300"
+UNIT = "pair evals/s"
+FP32_LANES_PER_SM = 128          # FP32 FMA lanes per Blackwell SM
+SM_COUNT_FALLBACK = 152
+SM_MAX_MHZ_FALLBACK = 2070.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="blobs_1m_d3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (timing only)
+# ---------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if os.environ.get("BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class Clocks:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.idx = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f)
+    return None
+
+
+def count_flops(n: int, d: int) -> float:
+    """Algorithmic FLOP of the count sweep: each unordered pair once, d FMAs."""
+    return 2.0 * d * n * (n - 1) / 2.0
+
+
+def recorded_traffic(kernel_src: str, workload: str):
+    """Per-launch DRAM bytes of the count sweep from the committed ncu summary,
+    or None when the summary is missing or the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", f"count_sweep_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"sweep_source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    return float(m.group(1)) if h.group(1) == cur else None
+
+
+def cpu_baseline(P, eps, min_pts, target_s=12.0):
+    """The oracle as it stands on a leading sample of the workload, sized for
+    about target_s seconds of single-threaded work.  -> dict."""
+    import oracle
+    m0 = min(len(P), 6000)
+    t = time.perf_counter()
+    oracle.dbscan(P[:m0], eps, min_pts)
+    t0 = time.perf_counter() - t
+    per_pair = t0 / (m0 * m0)
+    m = int(min(len(P), max(m0, (target_s / per_pair) ** 0.5)))
+    t = time.perf_counter()
+    oracle.dbscan(P[:m], eps, min_pts)
+    dt = time.perf_counter() - t
+    return {"value": m * m / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {m} of {len(P)} points of the workload, full oracle DBSCAN "
+                      f"(count + BFS), single-threaded, {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args, dist: Dist):
+    if dist.rank != 0:
+        return 0
+    import oracle
+    from all_pairs_distance_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    P = synth.generate(args.workload)
+    m = 20_000 if w.d <= 4 else 6_000
+    S = P[:m]
+    for _ in range(args.warmup):
+        oracle.dbscan(S, w.eps, w.min_pts)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.dbscan(S, w.eps, w.min_pts)
+        times.append(time.perf_counter() - t)
+    step = sum(times) / len(times)
+    value = m * m / step
+    sample = (f"first {m} of {w.n} points of {w.name} per step, full oracle DBSCAN "
+              f"(count + BFS), single-threaded")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "n": w.n, "d": w.d, "eps": w.eps,
+                       "min_pts": w.min_pts, "sample_points": m},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gb300(args, dist: Dist):
+    import torch
+    from all_pairs_distance_gb300 import binding, synth
+    from all_pairs_distance_gb300 import build as lib_build
+
+    w = synth.WORKLOADS[args.workload]
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    binding.load()
+    P = synth.generate(args.workload)
+    dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    x = torch.from_numpy(P).to(dev).to(dtype)
+    n, d = x.shape
+    ws = binding.workspace_for(x)
+    labels = torch.empty(n, dtype=torch.int32, device=dev)
+    is_core = torch.empty(n, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.dbscan_fit_ex(x, w.eps, w.min_pts, labels=labels, is_core=is_core,
+                              workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = binding.dbscan_workspace_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {binding.dbscan_strerror(st)}")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(dist.local) if dist.rank == 0 else None
+    binding.dbscan_profile_begin()
+    for k in range(args.steps):
+        flush.zero_()
+        starts[k].record(stream)
+        step()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    stage_ms, calls, launches = binding.dbscan_profile_end()
+    clk = clocks.stop() if clocks else None
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    mean_ms = sum(step_ms) / len(step_ms)
+    mean_ms = dist.max(mean_ms)
+    value = dist.world * float(n) * float(n) / (mean_ms * 1e-3)
+    st = binding.dbscan_workspace_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {binding.dbscan_strerror(st)}")
+
+    # roofline of the dominant kernel (the count sweep)
+    count_ms = stage_ms["count"] / max(calls, 1)
+    peaks = measured_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sms = getattr(props, "multi_processor_count", SM_COUNT_FALLBACK)
+    max_mhz = (peaks or {}).get("sm_max_mhz", SM_MAX_MHZ_FALLBACK)
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12
+    achieved = count_flops(n, d) / (count_ms * 1e-3) / 1e12
+    traffic = recorded_traffic(os.path.join(ROOT, "all_pairs_distance_gb300", "csrc", "sweep.cu"),
+                               w.name)
+    roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp32_peak, "traffic": traffic,
+                "kernel": "count sweep (fp32 FFMA, upper triangle)",
+                "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
+                               f"{max_mhz:.0f} MHz (max SM clock"
+                               + (", MEASURED_PEAKS.json)" if peaks else ", recipe fallback)")}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "n": n, "d": d, "eps": w.eps, "min_pts": w.min_pts,
+                       "input_dtype": w.dtype, "l2": "flushed between steps (256 MiB write, untimed)",
+                       "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU"},
+            "stages_ms": {k: v / max(calls, 1) for k, v in stage_ms.items()},
+            "count_pair_evals_per_s": float(n) * n / (count_ms * 1e-3),
+            "roofline": roofline, "gpu_launches": launches, "clocks": clk}
+
+    if not args.no_e2e:
+        ph = torch.from_numpy(P).to(dtype).pin_memory()
+        lh = torch.empty(n, dtype=torch.int32).pin_memory()
+        ch = torch.empty(n, dtype=torch.uint8).pin_memory()
+        binding.dbscan_fit_host(ph, w.eps, w.min_pts, labels=lh, is_core=ch, stream=stream)
+        ts = []
+        for _ in range(max(1, min(args.steps, 5))):
+            flush.zero_()
+            torch.cuda.synchronize()
+            t = time.perf_counter()
+            binding.dbscan_fit_host(ph, w.eps, w.min_pts, labels=lh, is_core=ch, stream=stream)
+            ts.append(time.perf_counter() - t)
+        e2e_s = dist.max(sum(ts) / len(ts))
+        line["e2e"] = {"value": dist.world * float(n) * n / e2e_s, "unit": UNIT,
+                       "ms": e2e_s * 1e3, "h2d_bytes_per_step": int(ph.numel() * ph.element_size()),
+                       "d2h_bytes_per_step": int(n * 4 + n),
+                       "api": "dbscan_fit_host (pinned host buffers, copies inside the timed call)"}
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(P, w.eps, w.min_pts)
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, dist)
+        return run_gb300(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

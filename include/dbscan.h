@@ -1,0 +1,167 @@
+/*
+ * dbscan.h -- C ABI of the GB300 DBSCAN library (libdbscan_gb300.so).
+ *
+ * What it computes ("Design and optimization of DBSCAN Algorithm based on
+ * CUDA", Wang et al.):
+ *   - §II "Background": the eps-neighbourhood of a point is every point within
+ *     distance eps of it (the point itself included); a point is a core point
+ *     when at least MinPts points are in its eps-neighbourhood; clusters are
+ *     maximal sets connected by reachability, which only passes through core
+ *     points.
+ *   - §IV-A: distances are compared squared, against eps^2; §IV-B: a pair is a
+ *     neighbour pair when distance <= eps^2 (inclusive).
+ *   - §IV-B1/§IV-B2: neighbour counting is fused with the distance evaluation
+ *     (no distance matrix is stored) and uses the expanded form
+ *     T + P[n] - (X p_x + Y p_y + Z p_z) with per-point terms hoisted.
+ *   - §IV-C: clusters are merged; here by a lock-free union-find over core
+ *     pairs instead of the page's cluster matrix.
+ *
+ * Results (defined exactly):
+ *   eps2         = (float)eps * (float)eps            (single-precision product)
+ *   neighbour    : sum_k (x_ik - x_jk)^2 <= eps2, i == j included
+ *   is_core[i]   = |neighbours(i)| >= min_pts
+ *   labels[i]    = for a core point: the smallest core index of its cluster
+ *                  (clusters = connected components of core points under the
+ *                  neighbour relation);
+ *                  for a non-core point with at least one core neighbour
+ *                  (border point): the smallest label among the clusters of
+ *                  its core neighbours;
+ *                  otherwise (noise): -1.
+ * The page leaves open whether a point counts itself, whether "core" is
+ * ">= MinPts" or "> MinPts", and which cluster a border point shared by two
+ * clusters joins; the answers above are the readings this library takes.
+ *
+ * Exactness: when every coordinate is an integer and sum_k (max_k - min_k)^2
+ * over the data's per-dimension ranges is below 2^24, every quantity the
+ * kernels form is an integer below 2^24 and the results are exact (identical
+ * to a double-precision evaluation).  Otherwise pairs within float32 rounding
+ * of the eps boundary may be classified either way.
+ *
+ * Memory: every pointer argument is a DEVICE pointer unless the entry point's
+ * name ends in _host.  The caller owns all buffers; the library never frees
+ * or retains them.  points is row-major [n, d] and contiguous.
+ *
+ * Streams: a stream argument is a cudaStream_t passed as void* (NULL = the
+ * legacy default stream).
+ *
+ * Errors: every entry point returns a dbscan_status.  On error the outputs
+ * are undefined.  Errors found on the device (non-finite input, an internal
+ * iteration cap) are recorded in the workspace and returned by the
+ * synchronous entry points, or by dbscan_workspace_status().
+ */
+#ifndef DBSCAN_GB300_H
+#define DBSCAN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DBSCAN_OK = 0,
+    DBSCAN_ERR_INVALID_ARG = -1,  /* bad size, null pointer, eps, min_pts, workspace too small, non-finite input */
+    DBSCAN_ERR_UNSUPPORTED = -2,  /* n > 2^31 - 1, d > 256, bf16 with d not a multiple of 16 */
+    DBSCAN_ERR_ALLOC = -3,        /* the library could not allocate its own workspace */
+    DBSCAN_ERR_CUDA = -4,         /* a CUDA runtime call failed (launch, copy, sync) */
+    DBSCAN_ERR_INTERNAL = -5      /* a device-side iteration cap was hit */
+} dbscan_status;
+
+typedef enum {
+    DBSCAN_F32 = 0,   /* float32 points */
+    DBSCAN_BF16 = 1   /* bfloat16 points (d a multiple of 16) */
+} dbscan_dtype;
+
+/* Largest supported dimension. */
+#define DBSCAN_MAX_D 256
+
+/*
+ * Full DBSCAN on float32 device points; synchronous on the legacy default
+ * stream.  Allocates and frees its own workspace (stream-ordered).
+ *   points      [n, d] float32, device, read only
+ *   labels_out  [n] int32, device, written
+ *   is_core_out [n] uint8 (0/1), device, written
+ * n == 0 is a no-op returning DBSCAN_OK.
+ * Cites: §II definitions, §IV-A/§IV-B neighbour test, §IV-C merge step.
+ */
+int dbscan_fit(const float *points, int64_t n, int32_t d, float eps,
+               int32_t min_pts, int32_t *labels_out, uint8_t *is_core_out);
+
+/*
+ * Full DBSCAN, asynchronous on `stream` when a workspace is supplied.
+ *   points      [n, d] of `dtype` (dbscan_dtype), device
+ *   workspace   device buffer of at least dbscan_workspace_size(n, d, dtype)
+ *               bytes (256-byte aligned), owned by the caller, reused freely
+ *               between calls that do not overlap on the GPU; or NULL, in
+ *               which case the library allocates one stream-ordered, frees
+ *               it, and synchronises `stream` before returning so that
+ *               device-side errors can be reported.
+ * With a caller workspace nothing waits for the GPU: host-side argument
+ * errors and launch errors are returned, device-side errors are read later
+ * with dbscan_workspace_status().
+ * Cites: §II, §IV-A, §IV-B, §IV-B1, §IV-B2, §IV-C.
+ */
+int dbscan_fit_ex(const void *points, int32_t dtype, int64_t n, int32_t d,
+                  float eps, int32_t min_pts, int32_t *labels_out,
+                  uint8_t *is_core_out, void *workspace,
+                  size_t workspace_bytes, void *stream);
+
+/*
+ * Full DBSCAN on HOST buffers: copies points in, runs, copies the results
+ * out and synchronises `stream`.  Device memory is allocated stream-ordered
+ * for the call and freed before returning.  Host buffers may be pageable or
+ * pinned (pinned copies are faster).
+ *   points_host      [n, d] of `dtype`, host
+ *   labels_host      [n] int32, host
+ *   is_core_host     [n] uint8, host
+ */
+int dbscan_fit_host(const void *points_host, int32_t dtype, int64_t n,
+                    int32_t d, float eps, int32_t min_pts,
+                    int32_t *labels_host, uint8_t *is_core_host,
+                    void *stream);
+
+/*
+ * Neighbour counts only (the fused distance + count step, §IV-B1/§IV-B2):
+ *   cnt_out[i] = |{ j : sum_k (x_ik - x_jk)^2 <= eps2 }|  (i itself included)
+ * cnt_out is [n] int32, device.  Workspace rules as for dbscan_fit_ex
+ * (the same size suffices).
+ */
+int dbscan_neighbor_counts(const void *points, int32_t dtype, int64_t n,
+                           int32_t d, float eps, int32_t *cnt_out,
+                           void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/* Bytes of workspace dbscan_fit_ex needs for this problem shape; 0 when the
+ * shape is invalid or unsupported.  Pure host computation. */
+size_t dbscan_workspace_size(int64_t n, int32_t d, int32_t dtype);
+
+/* Synchronises `stream`, then returns the first device-side error recorded in
+ * `workspace` by the last call that used it (DBSCAN_OK if none). */
+int dbscan_workspace_status(const void *workspace, void *stream);
+
+/*
+ * Stage timing (measurement support, not part of the computation).
+ * Between dbscan_profile_begin() and dbscan_profile_end(), every call made
+ * on the same host thread records CUDA events on its own stream around its
+ * stages.  dbscan_profile_end() waits for those events and returns, summed
+ * over the calls, the milliseconds of each stage in the order
+ *   0 prep, 1 count, 2 compact, 3 union, 4 flatten, 5 border, 6 finalize
+ * (stage_ms has room for max_stages floats; a stage a call did not run adds
+ * 0), the number of calls and the number of kernels they launched.
+ * Pointers are host pointers and may be NULL.  Returns DBSCAN_OK, or
+ * DBSCAN_ERR_CUDA if an event could not be created or read.
+ */
+#define DBSCAN_NUM_STAGES 7
+int dbscan_profile_begin(void);
+int dbscan_profile_end(float *stage_ms, int32_t max_stages, int64_t *calls,
+                       int64_t *kernel_launches);
+
+/* Static, human-readable name of a status code. */
+const char *dbscan_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DBSCAN_GB300_H */

@@ -1,0 +1,96 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads,
+exports every function include/dbscan.h declares, and rejects bad arguments
+on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from all_pairs_distance_gb300 import build as lib_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dbscan.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = lib_build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dbscan_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("dbscan_fit", "dbscan_fit_ex", "dbscan_workspace_size", "dbscan_strerror"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in dbscan.h but not exported"
+
+
+def test_strerror(lib):
+    lib.dbscan_strerror.restype = ctypes.c_char_p
+    lib.dbscan_strerror.argtypes = [ctypes.c_int]
+    for code in range(-5, 1):
+        assert lib.dbscan_strerror(code).startswith(b"DBSCAN_")
+    assert b"unknown" in lib.dbscan_strerror(42)
+
+
+def test_workspace_size(lib):
+    f = lib.dbscan_workspace_size
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
+    assert f(-1, 3, 0) == 0            # negative n
+    assert f(10, 0, 0) == 0            # d < 1
+    assert f(10, 257, 0) == 0          # d above the maximum
+    assert f(10, 3, 1) == 0            # bf16 needs d % 16 == 0
+    assert f(10, 3, 7) == 0            # unknown dtype
+    assert f(1 << 31, 3, 0) == 0       # n beyond int32 labels
+    assert f(0, 3, 0) > 0
+    small, big = f(1000, 3, 0), f(1_000_000, 3, 0)
+    assert 0 < small < big
+    # O(N d) memory: no N x N term anywhere
+    assert big < 200 * 1_000_000 * 4
+    assert f(1_000_000, 3, 0) % 256 == 0
+    assert f(500_000, 64, 1) > f(500_000, 16, 1)
+
+
+def _fit_ex(lib):
+    f = lib.dbscan_fit_ex
+    f.restype = ctypes.c_int
+    P = ctypes.c_void_p
+    f.argtypes = [P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                  ctypes.c_int32, P, P, P, ctypes.c_size_t, P]
+    return f
+
+
+def test_host_side_argument_errors(lib):
+    f = _fit_ex(lib)
+    fake = ctypes.c_void_p(0x1000)   # never dereferenced: these calls fail validation first
+    INVALID, UNSUP = -1, -2
+    assert f(fake, 0, -5, 3, 1.0, 2, fake, fake, None, 0, None) == INVALID
+    assert f(fake, 0, 10, 0, 1.0, 2, fake, fake, None, 0, None) == INVALID
+    assert f(fake, 0, 10, 300, 1.0, 2, fake, fake, None, 0, None) == UNSUP
+    assert f(fake, 1, 10, 3, 1.0, 2, fake, fake, None, 0, None) == UNSUP
+    assert f(fake, 5, 10, 3, 1.0, 2, fake, fake, None, 0, None) == INVALID
+    assert f(fake, 0, 10, 3, -1.0, 2, fake, fake, None, 0, None) == INVALID
+    assert f(fake, 0, 10, 3, float("nan"), 2, fake, fake, None, 0, None) == INVALID
+    assert f(fake, 0, 10, 3, float("inf"), 2, fake, fake, None, 0, None) == INVALID
+    assert f(fake, 0, 10, 3, 1.0, 0, fake, fake, None, 0, None) == INVALID
+    assert f(None, 0, 10, 3, 1.0, 2, fake, fake, None, 0, None) == INVALID
+    assert f(fake, 0, 10, 3, 1.0, 2, None, fake, None, 0, None) == INVALID
+    assert f(fake, 0, 10, 3, 1.0, 2, fake, None, None, 0, None) == INVALID
+    assert f(fake, 0, (1 << 31), 3, 1.0, 2, fake, fake, None, 0, None) == UNSUP
+    # workspace too small, or not 256-byte aligned
+    assert f(fake, 0, 10, 3, 1.0, 2, fake, fake, ctypes.c_void_p(0x10000), 16, None) == INVALID
+    assert f(fake, 0, 10, 3, 1.0, 2, fake, fake, ctypes.c_void_p(0x10010), 1 << 30, None) == INVALID
+    # n == 0 is a no-op, whatever the pointers
+    assert f(None, 0, 0, 3, 1.0, 2, None, None, None, 0, None) == 0

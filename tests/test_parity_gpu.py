@@ -1,0 +1,192 @@
+"""Element-by-element parity of the CUDA path with the CPU oracle.
+
+Sizes are ones the oracle finishes in seconds while still spanning many
+128-point tiles and a ragged last tile; every kernel family (d <= 4 packed,
+d > 4 shared-memory, float32 and bfloat16 inputs) is exercised.  Counts,
+core flags and labels are integers and must match exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from all_pairs_distance_gb300 import binding, synth
+from conftest import GOLDEN_FILES, load_golden
+from gpu_util import assert_same, gpu_run
+
+pytestmark = pytest.mark.gpu
+
+
+def _blobs(n, d, hi, nb, sigma, noise, seed):
+    return synth.blob_set(n, d, hi, nb, sigma, noise, seed)
+
+
+CASES = {
+    # name: (points factory, eps, min_pts, dtype)
+    "c1_full_2k_d2": (lambda: synth.generate("blobs_2k_d2"), 30.0, 5, torch.float32),
+    "c2_like_20k_d2": (lambda: synth.scaled("blobs_100k_d2", 20_000), 20.0, 10, torch.float32),
+    "c4_like_20k_d3": (lambda: synth.scaled("blobs_1m_d3", 20_011), 10.0, 8, torch.float32),
+    "c3_like_6k_d16": (lambda: synth.scaled("blobs_200k_d16", 6_007), 120.0, 20, torch.float32),
+    "c5_like_4k_d64_bf16": (lambda: synth.scaled("blobs_500k_d64", 4_003), 100.0, 16, torch.bfloat16),
+    "c5_like_3k_d64_f32": (lambda: synth.scaled("blobs_500k_d64", 3_001, seed=9), 100.0, 16, torch.float32),
+    "d1_uniform": (lambda: synth.uniform_ints(5_000, 1, 20_000, 1), 3.0, 3, torch.float32),
+    "d1_blobs": (lambda: _blobs(4_100, 1, 4095, 6, 30.0, 400, 2), 2.0, 4, torch.float32),
+    "d4_blobs": (lambda: _blobs(9_000, 4, 1023, 20, 10.0, 900, 3), 12.0, 6, torch.float32),
+    "d5_blobs": (lambda: _blobs(7_000, 5, 1023, 15, 12.0, 700, 4), 20.0, 6, torch.float32),
+    "d8_blobs": (lambda: _blobs(6_000, 8, 255, 12, 6.0, 600, 5), 14.0, 5, torch.float32),
+    "d17_blobs": (lambda: _blobs(3_000, 17, 255, 8, 8.0, 300, 6), 40.0, 5, torch.float32),
+    "d33_blobs": (lambda: _blobs(2_500, 33, 127, 8, 4.0, 250, 7), 30.0, 5, torch.float32),
+    "d16_bf16": (lambda: _blobs(5_000, 16, 255, 10, 6.0, 500, 8), 30.0, 6, torch.bfloat16),
+    "d32_bf16": (lambda: _blobs(3_000, 32, 255, 10, 6.0, 300, 10), 45.0, 6, torch.bfloat16),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_parity_with_oracle(name):
+    make, eps, min_pts, dtype = CASES[name]
+    P = make()
+    cnt_ref, core_ref, label_ref = oracle.dbscan(P, eps, min_pts)
+    cnt, core, label = gpu_run(P, eps, min_pts, dtype)
+    assert_same(cnt, cnt_ref, f"{name} counts")
+    assert_same(core, core_ref, f"{name} core flags")
+    assert_same(label, label_ref, f"{name} labels")
+    # the case must exercise clusters, borders and noise, not a degenerate mix
+    if name.startswith("c"):
+        assert core_ref.sum() > 0 and (label_ref == -1).sum() > 0
+        assert ((core_ref == 0) & (label_ref >= 0)).sum() > 0
+
+
+@pytest.mark.parametrize("name", GOLDEN_FILES)
+def test_golden_fixture_on_gpu(name):
+    P, eps, min_pts, exp = load_golden(name)
+    cnt, core, label = gpu_run(P, eps, min_pts)
+    assert_same(cnt, exp["cnt"], "cnt")
+    assert_same(core, exp["core"], "core")
+    assert_same(label, exp["label"], "label")
+
+
+@pytest.mark.parametrize("n", [1, 2, 127, 128, 129, 255, 256, 257, 1000])
+@pytest.mark.parametrize("d", [2, 3, 6])
+def test_tile_boundaries(n, d):
+    P = synth.uniform_ints(n, d, 40, seed=n * 10 + d)
+    for min_pts in (1, 3):
+        ref = oracle.dbscan(P, 6.0, min_pts)
+        got = gpu_run(P, 6.0, min_pts)
+        for g, e, w in zip(got, ref, ("cnt", "core", "label")):
+            assert_same(g, e, f"n={n} d={d} min_pts={min_pts} {w}")
+
+
+def test_n_zero_is_noop():
+    x = torch.empty((0, 3), device="cuda")
+    labels, core = binding.dbscan_fit_ex(x, 1.0, 2)
+    assert labels.numel() == 0 and core.numel() == 0
+
+
+def test_all_duplicates_one_cluster():
+    P = np.full((700, 3), 17.0, np.float32)
+    cnt, core, label = gpu_run(P, 0.0, 5)
+    assert np.all(cnt == 700) and np.all(core == 1) and np.all(label == 0)
+
+
+def test_eps_zero_and_min_pts_above_n():
+    rng = np.random.default_rng(0)
+    P = rng.integers(0, 6, size=(900, 2)).astype(np.float32)   # many duplicates
+    for eps, mp in ((0.0, 3), (1.0, 5), (2.0, 10_000)):
+        ref = oracle.dbscan(P, eps, mp)
+        got = gpu_run(P, eps, mp)
+        for g, e, w in zip(got, ref, ("cnt", "core", "label")):
+            assert_same(g, e, f"eps={eps} min_pts={mp} {w}")
+
+
+def test_inclusive_boundary_at_full_range():
+    # two points at the ends of [0, 2047] with eps equal to their distance:
+    # the squared distance 2047^2 equals eps^2 and must count (<=)
+    P = np.array([[0.0], [2047.0]], np.float32)
+    cnt, core, label = gpu_run(P, 2047.0, 2)
+    assert_same(cnt, [2, 2], "cnt")
+    assert_same(label, [0, 0], "label")
+    cnt, core, label = gpu_run(P, 2046.0, 2)
+    assert_same(cnt, [1, 1], "cnt")
+
+
+@pytest.mark.parametrize("d,hi", [(3, 2047), (2, 2047), (16, 511)])
+def test_extreme_corners_all_pairs(d, hi):
+    # corners of the box: the largest squared distance (d * hi^2) sits at the
+    # edge of exact float32 integers; eps above it makes every pair a neighbour
+    rng = np.random.default_rng(d)
+    P = (rng.integers(0, 2, size=(300, d)) * hi).astype(np.float32)
+    for eps in (float(hi), float(hi) * np.sqrt(d) + 1.0):
+        ref = oracle.dbscan(P, eps, 4)
+        got = gpu_run(P, eps, 4)
+        for g, e, w in zip(got, ref, ("cnt", "core", "label")):
+            assert_same(g, e, f"d={d} eps={eps} {w}")
+
+
+def test_extremes_bf16_d64():
+    # rows of all-0 and all-255 in bf16 (largest norms of the d=64 workload)
+    rng = np.random.default_rng(3)
+    P = (rng.integers(0, 2, size=(400, 64)) * 255).astype(np.float32)
+    P[:100] = rng.integers(250, 256, size=(100, 64))
+    for eps in (100.0, 2040.0, 2041.0):
+        ref = oracle.dbscan(P, eps, 4)
+        got = gpu_run(P, eps, 4, torch.bfloat16)
+        for g, e, w in zip(got, ref, ("cnt", "core", "label")):
+            assert_same(g, e, f"eps={eps} {w}")
+
+
+def test_dyadic_fractional_coordinates():
+    # quarter-integer coordinates are exact in float32 as well; the
+    # non-integer branch of the threshold must still give "<= eps^2"
+    rng = np.random.default_rng(7)
+    P = (rng.integers(0, 400, size=(3000, 3)) / 4.0).astype(np.float32)
+    for eps in (0.5, 1.25, 2.0):
+        ref = oracle.dbscan(P, eps, 4)
+        got = gpu_run(P, eps, 4)
+        for g, e, w in zip(got, ref, ("cnt", "core", "label")):
+            assert_same(g, e, f"eps={eps} {w}")
+
+
+def test_deterministic_repeats():
+    P = synth.scaled("blobs_1m_d3", 30_000, seed=77)
+    first = gpu_run(P, 10.0, 8)
+    for _ in range(4):
+        again = gpu_run(P, 10.0, 8)
+        for g, e in zip(again, first):
+            assert np.array_equal(g, e)
+
+
+def test_sync_and_host_entry_points_agree():
+    P = synth.scaled("blobs_100k_d2", 12_000, seed=5)
+    _, core_ref, label_ref = oracle.dbscan(P, 20.0, 10)
+    x = torch.from_numpy(P).cuda()
+    labels, core = binding.dbscan_fit(x, 20.0, 10)
+    assert_same(labels.cpu().numpy(), label_ref, "dbscan_fit labels")
+    assert_same(core.cpu().numpy(), core_ref, "dbscan_fit core")
+    hl, hc = binding.dbscan_fit_host(torch.from_numpy(P).pin_memory(), 20.0, 10)
+    assert_same(hl.numpy(), label_ref, "dbscan_fit_host labels")
+    assert_same(hc.numpy(), core_ref, "dbscan_fit_host core")
+    hl, hc = binding.dbscan_fit_host(P, 20.0, 10)    # pageable numpy input
+    assert_same(hl.numpy(), label_ref, "dbscan_fit_host (pageable) labels")
+
+
+def test_device_side_errors_and_bad_pointers():
+    x = torch.tensor([[0.0, 1.0], [float("nan"), 2.0], [3.0, 3.0]], device="cuda")
+    ws = binding.workspace_for(x)
+    binding.dbscan_fit_ex(x, 1.0, 2, workspace=ws)
+    assert binding.dbscan_workspace_status(ws) == binding.Status.INVALID_ARG
+    # a host pointer where device memory is required is refused, not run
+    lib = binding.load()
+    h = torch.zeros((10, 3))
+    lab = torch.empty(10, dtype=torch.int32, device="cuda")
+    core = torch.empty(10, dtype=torch.uint8, device="cuda")
+    st = lib.dbscan_fit_ex(h.data_ptr(), 0, 10, 3, 1.0, 2, lab.data_ptr(), core.data_ptr(),
+                           None, 0, None)
+    assert st == binding.Status.INVALID_ARG
+    # workspace too small
+    y = torch.zeros((1000, 3), device="cuda")
+    small = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.DbscanError):
+        binding.dbscan_fit_ex(y, 1.0, 2, workspace=small)
+    # the context is still usable afterwards
+    cnt, core_, label = gpu_run(np.zeros((5, 2), np.float32), 0.0, 2)
+    assert np.all(cnt == 5)
