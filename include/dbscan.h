@@ -132,6 +132,36 @@ int dbscan_neighbor_counts(const void *points, int32_t dtype, int64_t n,
                            void *workspace, size_t workspace_bytes,
                            void *stream);
 
+/*
+ * Full DBSCAN without any device allocation.  The paper has no counterpart:
+ * this entry point exists for callers that cannot call cudaMalloc -- code
+ * embedded in a host framework whose own allocator has reserved the device
+ * memory (an allocation of ours could fail or fragment its pool), or serving
+ * paths that must not allocate after start-up because an allocation can
+ * synchronise the device.  It runs exactly what dbscan_fit_ex runs, with the
+ * workspace taken from a static device array of DBSCAN_NOALLOC_SCRATCH_BYTES
+ * (64 MiB) that every GPU which loads this library holds until the process
+ * exits.
+ *   points, labels_out, is_core_out: as for dbscan_fit_ex (device pointers).
+ *   stream: cudaStream_t as void*, NULL = legacy default stream; asynchronous.
+ * Limits and rules:
+ *   - problems whose dbscan_workspace_size(n, d, dtype) exceeds
+ *     DBSCAN_NOALLOC_SCRATCH_BYTES are rejected with DBSCAN_ERR_UNSUPPORTED
+ *     (about 838,000 points at d = 3, 82,000 at d = 64);
+ *   - the first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture;
+ *   - every call shares the one array and each call clears the parts that
+ *     must start at zero, so calls that overlap on the GPU (different streams,
+ *     different host threads) race and must be serialised by the caller;
+ *   - device-side errors are not reported (there is no workspace handle to
+ *     read them from); host-side argument errors are returned as usual.
+ */
+#define DBSCAN_NOALLOC_SCRATCH_BYTES (64u << 20)
+int dbscan_fit_noalloc(const void *points, int32_t dtype, int64_t n, int32_t d,
+                       float eps, int32_t min_pts, int32_t *labels_out,
+                       uint8_t *is_core_out, void *stream);
+
 /* Bytes of workspace dbscan_fit_ex needs for this problem shape; 0 when the
  * shape is invalid or unsupported.  Pure host computation. */
 size_t dbscan_workspace_size(int64_t n, int32_t d, int32_t dtype);
