@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="blobs_1m_d3")
+    ap.add_argument("--n", type=int, default=None,
+                    help="run a smaller set drawn like the workload (profiling cases only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -222,7 +224,7 @@ def run_gb300(args, dist: Dist):
     torch.cuda.set_device(dist.local)
     dev = torch.device("cuda", dist.local)
     binding.load()
-    P = synth.generate(args.workload)
+    P = synth.generate(args.workload) if args.n is None else synth.scaled(args.workload, args.n)
     dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     x = torch.from_numpy(P).to(dev).to(dtype)
     n, d = x.shape
@@ -288,7 +290,8 @@ def run_gb300(args, dist: Dist):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": w.name, "n": n, "d": d, "eps": w.eps, "min_pts": w.min_pts,
+            "config": {"workload": w.name if args.n is None else f"{w.name} scaled to n={n}",
+                       "n": n, "d": d, "eps": w.eps, "min_pts": w.min_pts,
                        "input_dtype": w.dtype, "l2": "flushed between steps (256 MiB write, untimed)",
                        "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU"},
             "stages_ms": {k: v / max(calls, 1) for k, v in stage_ms.items()},

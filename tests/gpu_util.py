@@ -64,3 +64,41 @@ def check_sampled(P64, eps, min_pts, cnt, core, label, rows):
             assert label[i] == label[cn].min(), f"border {i}: not the smallest neighbouring label"
         else:
             assert label[i] == -1, f"noise {i} labelled {label[i]}"
+
+
+def kdtree_dbscan(P, eps, min_pts):
+    """Exact DBSCAN for integer coordinates, independent of the oracle: k-d tree
+    pairs within eps + 0.5, an exact integer filter d^2 <= eps^2, scipy's
+    connected components over core-core pairs, smallest-index names, border
+    points to the smallest neighbouring core label."""
+    from scipy.sparse import coo_matrix
+    from scipy.sparse.csgraph import connected_components
+    from scipy.spatial import cKDTree
+
+    X = P.astype(np.int64)
+    n = len(X)
+    thr = int(np.float32(eps) * np.float32(eps))
+    # integer squared distances <= thr imply distance <= sqrt(thr) < eps + 0.5
+    pairs = cKDTree(P.astype(np.float64)).query_pairs(r=float(eps) + 0.5, output_type="ndarray")
+    d2 = ((X[pairs[:, 0]] - X[pairs[:, 1]]) ** 2).sum(1)
+    pairs = pairs[d2 <= thr]
+    a, b = pairs[:, 0], pairs[:, 1]
+    cnt = 1 + np.bincount(a, minlength=n) + np.bincount(b, minlength=n)
+    core = cnt >= min_pts
+    label = np.full(n, -1, np.int64)
+    cc = core[a] & core[b]
+    g = coo_matrix((np.ones(int(cc.sum()), np.int8), (a[cc], b[cc])), shape=(n, n)).tocsr()
+    _, comp = connected_components(g, directed=False)
+    ci = np.flatnonzero(core)
+    name = np.full(comp.max() + 1, np.iinfo(np.int64).max)
+    np.minimum.at(name, comp[ci], ci)
+    label[ci] = name[comp[ci]]
+    big = np.iinfo(np.int64).max
+    border = np.full(n, big)
+    m1 = core[a] & ~core[b]
+    np.minimum.at(border, b[m1], label[a[m1]])
+    m2 = core[b] & ~core[a]
+    np.minimum.at(border, a[m2], label[b[m2]])
+    nc = ~core & (border != big)
+    label[nc] = border[nc]
+    return cnt.astype(np.int32), core.astype(np.uint8), label.astype(np.int32)

@@ -185,6 +185,18 @@ def test_matches_sklearn_on_blobs(name):
     np.testing.assert_array_equal(label == -1, db.labels_ == -1)
 
 
+@pytest.mark.parametrize("name,n", [("blobs_1m_d3", 8000), ("blobs_100k_d2", 6000),
+                                    ("blobs_200k_d16", 2000)])
+def test_matches_kdtree_restatement(name, n):
+    # an exact DBSCAN built from a k-d tree neighbour search and scipy's
+    # connected components (used at full size by the GPU tests)
+    from gpu_util import kdtree_dbscan
+    w = synth.WORKLOADS[name]
+    P = synth.scaled(name, n)
+    for g, e in zip(kdtree_dbscan(P, w.eps, w.min_pts), oracle.dbscan(P, w.eps, w.min_pts)):
+        np.testing.assert_array_equal(g, e)
+
+
 # --------------------------------------------------------------------------
 # symmetries
 # --------------------------------------------------------------------------
