@@ -122,9 +122,9 @@ static void keep_pool(void) {
 }
 
 // ---- stage timing ------------------------------------------------------------
-// Kernels launched by each stage: prep 4, count 1, compact 4, union 1,
-// flatten 1, border 1, finalize 1.
-static const int kStageLaunches[DBSCAN_NUM_STAGES] = {4, 1, 4, 1, 1, 1, 1};
+// Kernels launched by each stage: prep 4, count 1, compact 4, union 7 (four
+// sweep waves and three compressions), flatten 1, border 1, finalize 1.
+static const int kStageLaunches[DBSCAN_NUM_STAGES] = {4, 1, 4, 7, 1, 1, 1};
 
 struct ProfCall {
     cudaEvent_t ev[DBSCAN_NUM_STAGES + 1];

@@ -33,9 +33,9 @@ struct Ctrl {
     int exact;          // 1 when the exactness bound holds (set by setup)
     float thrx;         // row threshold constant, see prep.cu
     int n_all;          // number of points
-    unsigned unit_ctr[4];   // work-unit counters of the three sweeps
+    unsigned unit_ctr[8];   // work-unit counters: count, union waves 1-4, border
     float range_sq;     // sum_k (max_k - min_k)^2
-    int pad1[51];
+    int pad1[47];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl must be 256 bytes");
 

@@ -1,5 +1,5 @@
-// The tiled all-pairs sweeps: neighbour counting (pass 1), core-core
-// union-find (pass 2) and border assignment (pass 3).
+// The tiled all-pairs sweeps on CUDA cores: neighbour counting (pass 1),
+// core-core union-find (pass 2) and border assignment (pass 3).
 //
 // "Design and optimization of DBSCAN Algorithm based on CUDA" stages tiles of
 // points in shared memory (§IV-A3), unrolls the inner loop (§IV-A4), fuses
@@ -15,28 +15,36 @@
 //   cores).
 // * Column tiles stream through a 3-stage cp.async ring in shared memory; the
 //   tile layout (structure of arrays, 128 points per row) makes every load a
-//   conflict-free 16-byte vector.
+//   conflict-free 16-byte vector.  The union and border sweeps also stage one
+//   int per column (the union-find parent, or the final cluster label), so a
+//   neighbour pair is usually settled from shared memory alone.
 // * A thread owns 8 rows x 8 columns per tile.  Per pair the fast path does d
 //   fused multiply-adds (two pairs per packed f32x2 instruction for d <= 4)
-//   into v_ij = nrm_j - 2 c_i . c_j, and a three-input min per two pairs; a
-//   row whose minimum over its 8 columns is not below its threshold T_i has
-//   no neighbour there.  Only rows with a neighbour take the slow path, which
-//   re-tests the 8 pairs one by one and acts on each neighbour pair (count,
-//   union, or border label).  At the densities DBSCAN works at, almost all
-//   row-column blocks are empty, so the per-pair cost is the d FMAs plus half
-//   a min.
+//   into v_ij = nrm_j - 2 c_i . c_j, and half a three-input min; a row whose
+//   minimum over its 8 columns is not below its threshold T_i has no neighbour
+//   there.  Only rows with a neighbour take the slow path, which re-tests the
+//   8 pairs one by one and acts on each neighbour pair.
 #include "dbscan_internal.cuh"
 
-#include <mutex>
 #include <map>
+#include <mutex>
 #include <utility>
 
 namespace dbscan {
 
 constexpr int THREADS = 256;
-constexpr int R = 8;           // rows per thread
-constexpr int C = 8;           // columns per thread per tile
+constexpr int R = 8;             // rows per thread
+constexpr int C = 8;             // columns per thread per tile
 constexpr int UF_CAP = 1 << 22;  // iteration cap of union-find loops
+
+// Counters in Ctrl::unit_ctr.
+constexpr int CTR_COUNT = 0, CTR_UNION0 = 1, CTR_BORDER = 5;
+constexpr int UNION_WAVES = 4;
+// Union waves cover units [edge_w * G, edge_{w+1} * G) for a grid of G CTAs
+// (rows in ascending order, -1 = to the end); the union-find is compressed
+// between waves so that later waves mostly find equal parents in the staged
+// snapshot and never touch global memory.
+static const int kUnionWaveEdges[UNION_WAVES + 1] = {0, 1, 3, 8, -1};
 
 struct SweepArgs {
     const float *rows;     // staged row points
@@ -44,12 +52,13 @@ struct SweepArgs {
     const int *n_rows;     // device-side row count
     const float *cols;     // staged column points
     const int *n_cols;     // device-side column count
+    const int *aux;        // per-column int staged with the tile (parent or label), or null
     int tri;               // 1: rows and cols are one set, sweep the upper triangle
+    int ulo, uhi;          // unit range [ulo * grid, uhi * grid), uhi = -1: to the end
     unsigned *ctr;         // work-unit counter (zeroed before the launch)
     Ctrl *ctrl;
     int *cnt;              // pass 1: neighbour counts
     int *parent;           // pass 2: union-find parents
-    const int *clabel;     // pass 3: label of each core position
     const int *candidx;    // pass 3: original index of each candidate position
     int32_t *labels;       // pass 3: labels (original order)
 };
@@ -91,25 +100,28 @@ __device__ __noinline__ int uf_find(int *parent, int x, Ctrl *ctrl) {
     return x;
 }
 
-__device__ __noinline__ void uf_unite(int *parent, int a, int b, Ctrl *ctrl) {
+// Merge the sets of a and b; returns a node that is an ancestor of both
+// (their common root at the moment of the merge).
+__device__ __noinline__ int uf_unite(int *parent, int a, int b, Ctrl *ctrl) {
     for (int it = 0; it < UF_CAP; ++it) {
         a = uf_find(parent, a, ctrl);
         b = uf_find(parent, b, ctrl);
-        if (a == b) return;
+        if (a == b) return a;
         if (a < b) { int t = a; a = b; b = t; }
         // hook the larger root under the smaller one
-        if (atomicCAS(parent + a, a, b) == a) return;
+        if (atomicCAS(parent + a, a, b) == a) return b;
     }
     set_error(ctrl, DBSCAN_ERR_INTERNAL);
+    return min(a, b);
 }
 
 // ---- work units ------------------------------------------------------------
 struct Sched {
     int nrt, nct, uc, kc;
-    unsigned units;
+    unsigned units, ubegin, uend;
 };
 
-__device__ __forceinline__ Sched make_sched(int n_rows, int n_cols, int tri) {
+__device__ __forceinline__ Sched make_sched(int n_rows, int n_cols, int tri, int ulo, int uhi) {
     Sched s;
     s.nrt = (n_rows + BT - 1) / BT;
     s.nct = (n_cols + BT - 1) / BT;
@@ -121,6 +133,9 @@ __device__ __forceinline__ Sched make_sched(int n_rows, int n_cols, int tri) {
     s.uc = (int)uc;
     s.kc = (s.nct + s.uc - 1) / s.uc;
     s.units = (unsigned)((long long)s.nrt * s.kc);
+    const long long g = gridDim.x;
+    s.ubegin = (unsigned)min((long long)s.units, ulo * g);
+    s.uend = uhi < 0 ? s.units : (unsigned)min((long long)s.units, uhi * g);
     return s;
 }
 
@@ -135,25 +150,31 @@ __device__ __forceinline__ bool decode_unit(unsigned u, const Sched &s, int tri,
     return true;
 }
 
-// ---- per-neighbour-pair actions -------------------------------------------
+// ---- per-row state and per-neighbour-pair actions --------------------------
+// acc is the row's neighbour count (COUNT), an ancestor of the row point in
+// the union-find (UNION), or its smallest neighbouring label (BORDER).
+template <int MODE>
+__device__ __forceinline__ void row_init(const SweepArgs &a, int p, int n_rows, int &acc) {
+    if (MODE == SWEEP_COUNT) acc = 0;
+    else if (MODE == SWEEP_UNION) acc = p < n_rows ? uf_find(a.parent, p, a.ctrl) : -1;
+    else acc = 0x7fffffff;
+}
+
+// aux_q: the staged parent (UNION) or label (BORDER) of column point q.
 template <int MODE>
 __device__ __forceinline__ void on_neighbour(const SweepArgs &a, int p, int q, bool diag,
-                                             int &acc) {
+                                             int aux_q, int &acc) {
     if (MODE == SWEEP_COUNT) {
         if (diag && q < p) return;        // counted from the other side
         acc += 1;
         if (q != p) atomicAdd(a.cnt + q, 1);
     } else if (MODE == SWEEP_UNION) {
         if (diag && q <= p) return;
-        uf_unite(a.parent, p, q, a.ctrl);
+        if (aux_q == acc) return;         // q's parent is an ancestor of p: same set
+        acc = uf_unite(a.parent, acc, aux_q, a.ctrl);
     } else {
-        acc = min(acc, __ldcg(a.clabel + q));
+        acc = min(acc, aux_q);
     }
-}
-
-template <int MODE>
-__device__ __forceinline__ int acc_init() {
-    return MODE == SWEEP_BORDER ? 0x7fffffff : 0;
 }
 
 template <int MODE>
@@ -171,12 +192,19 @@ __device__ __forceinline__ void flush_rows(const SweepArgs &a, int rb, int tr, i
     }
 }
 
-// Issue the cp.async copies of one stage (tiles [tfirst, tfirst + ntiles)).
-__device__ __forceinline__ void issue_stage(float *dst, const float *cols, int tfirst,
-                                            int ntiles, int tile_floats) {
-    const float *src = cols + (size_t)tfirst * tile_floats;
+// Stage layout: tiles_per_stage point tiles, then (with aux) as many x BT ints.
+template <bool AUX>
+__device__ __forceinline__ void issue_stage(float *dst, const SweepArgs &a, int tfirst,
+                                            int ntiles, int tile_floats, int tiles_per_stage) {
+    const float *src = a.cols + (size_t)tfirst * tile_floats;
     const int chunks = ntiles * tile_floats / 4;
     for (int c = threadIdx.x; c < chunks; c += THREADS) cp_async16(dst + 4 * c, src + 4 * c);
+    if (AUX) {
+        const int *asrc = a.aux + (size_t)tfirst * BT;
+        int *adst = reinterpret_cast<int *>(dst + (size_t)tiles_per_stage * tile_floats);
+        const int achunks = ntiles * BT / 4;
+        for (int c = threadIdx.x; c < achunks; c += THREADS) cp_async16(adst + 4 * c, asrc + 4 * c);
+    }
 }
 
 // ===========================================================================
@@ -184,9 +212,11 @@ __device__ __forceinline__ void issue_stage(float *dst, const float *cols, int t
 // ===========================================================================
 template <int D, int MODE>
 __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
+    constexpr bool AUX = MODE != SWEEP_COUNT;
     constexpr int TILE = (D + 1) * BT;
     constexpr int CT = 4;   // tiles per stage
     constexpr int S = 3;    // stages
+    constexpr int STAGE = CT * TILE + (AUX ? CT * BT : 0);
     extern __shared__ __align__(16) float smem[];
     __shared__ unsigned s_unit;
 
@@ -194,14 +224,14 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
     const int tr = tid >> 4, tc = tid & 15;
     const int n_rows = *a.n_rows, n_cols = *a.n_cols;
     if (n_rows <= 0 || n_cols <= 0) return;
-    const Sched sc = make_sched(n_rows, n_cols, a.tri);
+    const Sched sc = make_sched(n_rows, n_cols, a.tri, a.ulo, a.uhi);
 
     for (;;) {
-        if (tid == 0) s_unit = atomicAdd(a.ctr, 1u);
+        if (tid == 0) s_unit = sc.ubegin + atomicAdd(a.ctr, 1u);
         __syncthreads();
         const unsigned u = s_unit;
         __syncthreads();
-        if (u >= sc.units) break;
+        if (u >= sc.uend) break;
         int rb, t0, t1;
         if (!decode_unit(u, sc, a.tri, rb, t0, t1)) continue;
 
@@ -226,13 +256,13 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
         }
         int acc[R];
 #pragma unroll
-        for (int m = 0; m < R; ++m) acc[m] = acc_init<MODE>();
+        for (int m = 0; m < R; ++m) row_init<MODE>(a, rb * BT + slot_of(tr, m), n_rows, acc[m]);
 
         const int nst = (t1 - t0 + CT - 1) / CT;
 #pragma unroll
         for (int s = 0; s < S - 1; ++s) {
-            if (s < nst) issue_stage(smem + s * CT * TILE, a.cols, t0 + s * CT,
-                                     min(CT, t1 - (t0 + s * CT)), TILE);
+            if (s < nst) issue_stage<AUX>(smem + s * STAGE, a, t0 + s * CT,
+                                          min(CT, t1 - (t0 + s * CT)), TILE, CT);
             cp_async_commit();
         }
         for (int g = 0; g < nst; ++g) {
@@ -240,11 +270,12 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
             __syncthreads();
             {
                 int gn = g + S - 1;
-                if (gn < nst) issue_stage(smem + (gn % S) * CT * TILE, a.cols, t0 + gn * CT,
-                                          min(CT, t1 - (t0 + gn * CT)), TILE);
+                if (gn < nst) issue_stage<AUX>(smem + (gn % S) * STAGE, a, t0 + gn * CT,
+                                               min(CT, t1 - (t0 + gn * CT)), TILE, CT);
                 cp_async_commit();
             }
-            const float *sb = smem + (g % S) * CT * TILE;
+            const float *sb = smem + (g % S) * STAGE;
+            const int *saux = reinterpret_cast<const int *>(sb + CT * TILE);
             const int ntile = min(CT, t1 - (t0 + g * CT));
             for (int q = 0; q < ntile; ++q) {
                 const int tile = t0 + g * CT + q;
@@ -284,7 +315,11 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
                             float v = xc[D][c];
 #pragma unroll
                             for (int k = 0; k < D; ++k) v = fmaf(ra[m][k].x, xc[k][c], v);
-                            if (v < rT[m]) on_neighbour<MODE>(a, p, tile * BT + slot_of(tc, c), diag, acc[m]);
+                            if (v < rT[m]) {
+                                const int slot = slot_of(tc, c);
+                                on_neighbour<MODE>(a, p, tile * BT + slot, diag,
+                                                   AUX ? saux[q * BT + slot] : 0, acc[m]);
+                            }
                         }
                     }
                 }
@@ -300,24 +335,26 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
 // ===========================================================================
 template <int MODE, int S>
 __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
+    constexpr bool AUX = MODE != SWEEP_COUNT;
     extern __shared__ __align__(16) float smem[];
     __shared__ unsigned s_unit;
     const int TILE = (D + 1) * BT;
+    const int STAGE = TILE + (AUX ? BT : 0);
     float *rowbuf = smem;                  // D * BT floats: -2 c of the row tile
-    float *stages = smem + D * BT;         // S * TILE floats
+    float *stages = smem + D * BT;         // S * STAGE floats
 
     const int tid = threadIdx.x;
     const int tr = tid >> 4, tc = tid & 15;
     const int n_rows = *a.n_rows, n_cols = *a.n_cols;
     if (n_rows <= 0 || n_cols <= 0) return;
-    const Sched sc = make_sched(n_rows, n_cols, a.tri);
+    const Sched sc = make_sched(n_rows, n_cols, a.tri, a.ulo, a.uhi);
 
     for (;;) {
-        if (tid == 0) s_unit = atomicAdd(a.ctr, 1u);
+        if (tid == 0) s_unit = sc.ubegin + atomicAdd(a.ctr, 1u);
         __syncthreads();
         const unsigned u = s_unit;
         __syncthreads();
-        if (u >= sc.units) break;
+        if (u >= sc.uend) break;
         int rb, t0, t1;
         if (!decode_unit(u, sc, a.tri, rb, t0, t1)) continue;
 
@@ -335,12 +372,12 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
         }
         int acc[R];
 #pragma unroll
-        for (int m = 0; m < R; ++m) acc[m] = acc_init<MODE>();
+        for (int m = 0; m < R; ++m) row_init<MODE>(a, rb * BT + slot_of(tr, m), n_rows, acc[m]);
 
         const int nst = t1 - t0;   // one tile per stage
 #pragma unroll
         for (int s = 0; s < S - 1; ++s) {
-            if (s < nst) issue_stage(stages + s * TILE, a.cols, t0 + s, 1, TILE);
+            if (s < nst) issue_stage<AUX>(stages + s * STAGE, a, t0 + s, 1, TILE, 1);
             cp_async_commit();
         }
         for (int g = 0; g < nst; ++g) {
@@ -348,11 +385,12 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
             __syncthreads();
             {
                 int gn = g + S - 1;
-                if (gn < nst) issue_stage(stages + (gn % S) * TILE, a.cols, t0 + gn, 1, TILE);
+                if (gn < nst) issue_stage<AUX>(stages + (gn % S) * STAGE, a, t0 + gn, 1, TILE, 1);
                 cp_async_commit();
             }
             const int tile = t0 + g;
-            const float *st = stages + (g % S) * TILE;
+            const float *st = stages + (g % S) * STAGE;
+            const int *saux = reinterpret_cast<const int *>(st + TILE);
             float v[R][C];
             {
                 float4 lo = *reinterpret_cast<const float4 *>(st + D * BT + 4 * tc);
@@ -391,12 +429,25 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
                     const int p = rb * BT + slot_of(tr, m);
 #pragma unroll
                     for (int c = 0; c < C; ++c)
-                        if (v[m][c] < rT[m]) on_neighbour<MODE>(a, p, tile * BT + slot_of(tc, c), diag, acc[m]);
+                        if (v[m][c] < rT[m]) {
+                            const int slot = slot_of(tc, c);
+                            on_neighbour<MODE>(a, p, tile * BT + slot, diag, AUX ? saux[slot] : 0,
+                                               acc[m]);
+                        }
                 }
             }
         }
         cp_async_wait<0>();
         flush_rows<MODE>(a, rb, tr, n_rows, acc);
+    }
+}
+
+// Point every core position straight at its root (between union waves).
+__global__ void k_compress(Ctrl *ctrl, int *parent) {
+    const int n_core = ctrl->n_core;
+    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < n_core; p += gridDim.x * blockDim.x) {
+        int r = uf_find(parent, p, ctrl);
+        if (__ldcg(parent + p) != r) __stcg(parent + p, r);
     }
 }
 
@@ -425,7 +476,8 @@ int persistent_ctas(const void *kernel, int threads, size_t smem) {
 template <int D, int MODE>
 static cudaError_t run_small(const SweepArgs &args, cudaStream_t s) {
     auto kernel = k_sweep_small<D, MODE>;
-    const size_t smem = (size_t)3 * 4 * (D + 1) * BT * sizeof(float);
+    const int aux = MODE != SWEEP_COUNT ? 4 * BT : 0;
+    const size_t smem = (size_t)3 * (4 * (D + 1) * BT + aux) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute((const void *)kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -437,7 +489,8 @@ static cudaError_t run_small(const SweepArgs &args, cudaStream_t s) {
 template <int MODE, int S>
 static cudaError_t run_gen(const SweepArgs &args, int d, cudaStream_t s) {
     auto kernel = k_sweep_gen<MODE, S>;
-    const size_t smem = ((size_t)d * BT + (size_t)S * (d + 1) * BT) * sizeof(float);
+    const int aux = MODE != SWEEP_COUNT ? BT : 0;
+    const size_t smem = ((size_t)d * BT + (size_t)S * ((d + 1) * BT + aux)) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute((const void *)kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -462,24 +515,38 @@ cudaError_t launch_count(const Work &w, const Layout &L, cudaStream_t s) {
     SweepArgs a{};
     a.rows = w.staged_all; a.rowT = w.T_all; a.n_rows = &w.ctrl->n_all;
     a.cols = w.staged_all; a.n_cols = &w.ctrl->n_all;
-    a.tri = 1; a.ctr = &w.ctrl->unit_ctr[SWEEP_COUNT]; a.ctrl = w.ctrl; a.cnt = w.cnt;
+    a.tri = 1; a.ulo = 0; a.uhi = -1;
+    a.ctr = &w.ctrl->unit_ctr[CTR_COUNT]; a.ctrl = w.ctrl; a.cnt = w.cnt;
     return dispatch<SWEEP_COUNT>(a, L.d, s);
 }
 
 cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
     SweepArgs a{};
     a.rows = w.staged_core; a.rowT = w.T_core; a.n_rows = &w.ctrl->n_core;
-    a.cols = w.staged_core; a.n_cols = &w.ctrl->n_core;
-    a.tri = 1; a.ctr = &w.ctrl->unit_ctr[SWEEP_UNION]; a.ctrl = w.ctrl; a.parent = w.parent;
-    return dispatch<SWEEP_UNION>(a, L.d, s);
+    a.cols = w.staged_core; a.n_cols = &w.ctrl->n_core; a.aux = w.parent;
+    a.tri = 1; a.ctrl = w.ctrl; a.parent = w.parent;
+    const int grid = persistent_ctas((const void *)k_compress, 256, 0);
+    for (int wv = 0; wv < UNION_WAVES; ++wv) {
+        a.ulo = kUnionWaveEdges[wv];
+        a.uhi = kUnionWaveEdges[wv + 1];
+        a.ctr = &w.ctrl->unit_ctr[CTR_UNION0 + wv];
+        cudaError_t e = dispatch<SWEEP_UNION>(a, L.d, s);
+        if (e != cudaSuccess) return e;
+        if (wv + 1 < UNION_WAVES) {
+            k_compress<<<grid, 256, 0, s>>>(w.ctrl, w.parent);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_border(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s) {
     SweepArgs a{};
     a.rows = w.staged_cand; a.rowT = w.T_cand; a.n_rows = &w.ctrl->n_cand;
-    a.cols = w.staged_core; a.n_cols = &w.ctrl->n_core;
-    a.tri = 0; a.ctr = &w.ctrl->unit_ctr[SWEEP_BORDER]; a.ctrl = w.ctrl;
-    a.clabel = w.clabel; a.candidx = w.candidx; a.labels = labels;
+    a.cols = w.staged_core; a.n_cols = &w.ctrl->n_core; a.aux = w.clabel;
+    a.tri = 0; a.ulo = 0; a.uhi = -1;
+    a.ctr = &w.ctrl->unit_ctr[CTR_BORDER]; a.ctrl = w.ctrl;
+    a.candidx = w.candidx; a.labels = labels;
     return dispatch<SWEEP_BORDER>(a, L.d, s);
 }
 
