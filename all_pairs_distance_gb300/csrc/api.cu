@@ -16,6 +16,8 @@
 #include "dbscan_internal.cuh"
 
 #include <math.h>
+#include <stdlib.h>
+#include <string.h>
 #include <mutex>
 #include <set>
 #include <vector>
@@ -48,8 +50,36 @@ Layout make_layout(int64_t n, int32_t d) {
     L.off_parent = off;      off += align256(per_pt);
     L.off_clabel = off;      off += align256(per_pt);
     L.off_bsum = off;        off += align256((size_t)2 * (L.nscan_blocks + 1) * sizeof(int));
+    // tensor-core operand tiles, sized for the largest path this shape allows
+    size_t kb = 0;
+    for (int kind = TC_TF32; kind <= TC_BF16; ++kind) {
+        const int b = tc_kbytes(kind, d, 3);
+        if (b <= TC_MAX_KBYTES && (size_t)b > kb) kb = (size_t)b;
+    }
+    L.umma_tile_bytes = (size_t)BT * kb;
+    const size_t umma = (size_t)L.ntiles * L.umma_tile_bytes;
+    L.off_ua_all = off;      off += align256(umma);
+    L.off_ub_all = off;      off += align256(umma);
+    L.off_ua_core = off;     off += align256(umma);
+    L.off_ub_core = off;     off += align256(umma);
+    L.off_ua_cand = off;     off += align256(umma);
     L.total = off;
     return L;
+}
+
+// Tensor-core paths this shape may use, narrowed by DBSCAN_FORCE_PATH
+// ("fp32", "tf32" or "bf16") when it is set.
+static int allowed_tc(int d) {
+    int allow = 0;
+    if (tc_kbytes(TC_TF32, d, 3) <= TC_MAX_KBYTES) allow |= TC_ALLOW_TF32;
+    if (tc_kbytes(TC_BF16, d, 3) <= TC_MAX_KBYTES) allow |= TC_ALLOW_BF16;
+    const char *f = getenv("DBSCAN_FORCE_PATH");
+    if (f && *f) {
+        if (!strcmp(f, "fp32")) allow = 0;
+        else if (!strcmp(f, "tf32")) allow &= TC_ALLOW_TF32;
+        else if (!strcmp(f, "bf16")) allow &= TC_ALLOW_BF16;
+    }
+    return allow;
 }
 
 Work carve(void *base, const Layout &L) {
@@ -71,6 +101,11 @@ Work carve(void *base, const Layout &L) {
     w.parent = reinterpret_cast<int *>(b + L.off_parent);
     w.clabel = reinterpret_cast<int *>(b + L.off_clabel);
     w.bsum = reinterpret_cast<int *>(b + L.off_bsum);
+    w.ua_all = reinterpret_cast<uint8_t *>(b + L.off_ua_all);
+    w.ub_all = reinterpret_cast<uint8_t *>(b + L.off_ub_all);
+    w.ua_core = reinterpret_cast<uint8_t *>(b + L.off_ua_core);
+    w.ub_core = reinterpret_cast<uint8_t *>(b + L.off_ub_core);
+    w.ua_cand = reinterpret_cast<uint8_t *>(b + L.off_ua_cand);
     return w;
 }
 
@@ -122,13 +157,31 @@ static void keep_pool(void) {
 }
 
 // ---- stage timing ------------------------------------------------------------
-// Kernels launched by each stage: prep 4, count 1, compact 4, union 7 (four
-// sweep waves and three compressions), flatten 1, border 1, finalize 1.
-static const int kStageLaunches[DBSCAN_NUM_STAGES] = {4, 1, 4, 7, 1, 1, 1};
+// Kernels each stage launches for dimension d.  Every sweep launches its
+// CUDA-core kernel and one kernel per tensor-core path the shape allows
+// (ntc); all but the path chosen on the device return at once.
+//   prep 4 (+1 operand staging), count 1 + ntc, compact 4 (+2 operand
+//   stagings), union 4 waves x (1 + ntc) + 3 compressions, flatten 1,
+//   border 1 + ntc, finalize 1.
+static int stage_launches(int d, int stage) {
+    int ntc = 0;
+    for (int kind = TC_TF32; kind <= TC_BF16; ++kind)
+        if (tc_kbytes(kind, d, 3) <= TC_MAX_KBYTES) ++ntc;
+    const int umma = ntc > 0 ? 1 : 0;
+    switch (stage) {
+    case 0: return 4 + umma;
+    case 1: return 1 + ntc;
+    case 2: return 4 + 2 * umma;
+    case 3: return 4 * (1 + ntc) + 3;
+    case 5: return 1 + ntc;
+    default: return 1;
+    }
+}
 
 struct ProfCall {
     cudaEvent_t ev[DBSCAN_NUM_STAGES + 1];
     int stages;   // number of stages the call ran
+    int d;        // dimension of the call (sets the kernels per stage)
 };
 struct ProfState {
     bool on = false;
@@ -141,7 +194,8 @@ struct StageMarks {
     ProfCall call{};
     bool on = false;
     int next = 0;
-    explicit StageMarks(cudaStream_t s) {
+    StageMarks(cudaStream_t s, int d) {
+        call.d = d;
         if (!g_prof.on) return;
         for (int i = 0; i <= DBSCAN_NUM_STAGES; ++i) {
             if (cudaEventCreate(&call.ev[i]) != cudaSuccess) {
@@ -171,10 +225,11 @@ static int run(const void *points, int dtype, int64_t n, int d, float eps, int m
                int32_t *labels, uint8_t *is_core, int32_t *cnt_out, void *ws, const Layout &L,
                cudaStream_t s) {
     Work w = carve(ws, L);
-    StageMarks marks(s);
+    StageMarks marks(s, d);
     if (cudaMemsetAsync(w.ctrl, 0, sizeof(Ctrl), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     if (cudaMemsetAsync(w.cnt, 0, (size_t)n * sizeof(int), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
-    if (launch_prep(points, dtype, n, d, eps, w, L, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+    if (launch_prep(points, dtype, n, d, eps, allowed_tc(d), w, L, s) != cudaSuccess)
+        return DBSCAN_ERR_CUDA;
     marks.mark(s);
     if (launch_count(w, L, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     marks.mark(s);
@@ -312,7 +367,7 @@ int dbscan_profile_end(float *stage_ms, int32_t max_stages, int64_t *calls,
                 cudaEventElapsedTime(&ms, c.ev[i], c.ev[i + 1]) != cudaSuccess)
                 st = DBSCAN_ERR_CUDA;
             acc[i] += ms;
-            launches += kStageLaunches[i];
+            launches += stage_launches(c.d, i);
         }
         for (int i = 0; i <= c.stages; ++i) cudaEventDestroy(c.ev[i]);
     }

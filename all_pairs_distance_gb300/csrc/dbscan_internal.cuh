@@ -35,7 +35,11 @@ struct Ctrl {
     int n_all;          // number of points
     unsigned unit_ctr[8];   // work-unit counters: count, union waves 1-4, border
     float range_sq;     // sum_k (max_k - min_k)^2
-    int pad1[47];
+    int tc_kind;        // tensor-core path chosen by setup: TC_NONE, TC_TF32, TC_BF16
+    int tc_kpad;        // padded K of the tensor-core operands (elements)
+    int tc_kbytes;      // bytes of one operand row (tc_kpad * element size)
+    int tc_nt;          // digits of the threshold constant in the operands
+    int pad1[43];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl must be 256 bytes");
 
@@ -48,6 +52,8 @@ struct Layout {
     size_t off_ctrl, off_stats, off_staged_all, off_staged_core, off_staged_cand;
     size_t off_T_all, off_T_core, off_T_cand;
     size_t off_cnt, off_cidx, off_candidx, off_parent, off_clabel, off_bsum;
+    size_t umma_tile_bytes;   // bytes of one 128-point operand tile (largest path), 0 = none
+    size_t off_ua_all, off_ub_all, off_ua_core, off_ub_core, off_ua_cand;
     int64_t nscan_blocks;
     size_t total;
 };
@@ -68,6 +74,7 @@ struct Work {
     int *parent;          // [n] union-find parents over core positions
     int *clabel;          // [n] final label of each core position
     int *bsum;            // [2 * nscan_blocks] per-block counts of the compaction scan
+    uint8_t *ua_all, *ub_all, *ua_core, *ub_core, *ua_cand;   // tensor-core operand tiles
 };
 
 Work carve(void *base, const Layout &L);
@@ -75,9 +82,37 @@ Work carve(void *base, const Layout &L);
 // Sweep modes.
 enum SweepMode { SWEEP_COUNT = 0, SWEEP_UNION = 1, SWEEP_BORDER = 2 };
 
+// Tensor-core paths.  The operands carry, per point, the d coordinates plus
+// base-B digits of the squared norms and of the threshold constant, so one
+// MMA yields w_ij = |c_i - c_j|^2 - thrx exactly (see prep.cu):
+//   TF32: elements exact up to 2048, base 2048, 2 digits per norm
+//   BF16: elements exact up to 256,  base 256,  3 digits per norm
+// plus nt (1..3) digits of thrx.
+enum TcKind { TC_NONE = 0, TC_TF32 = 1, TC_BF16 = 2 };
+// Allowed-path mask passed from the host (all by default).
+enum { TC_ALLOW_TF32 = 1, TC_ALLOW_BF16 = 2 };
+constexpr int TC_MAX_KBYTES = 256;   // largest operand row the tensor-core sweep stages
+
+__host__ __device__ inline int tc_norm_digits(int kind) { return kind == TC_TF32 ? 2 : 3; }
+__host__ __device__ inline int tc_kpad(int kind, int d, int nt) {
+    const int used = d + 2 * tc_norm_digits(kind) + nt;
+    return kind == TC_TF32 ? ((used + 7) / 8) * 8 : ((used + 15) / 16) * 16;
+}
+__host__ __device__ inline int tc_kbytes(int kind, int d, int nt) {
+    return tc_kpad(kind, d, nt) * (kind == TC_TF32 ? 4 : 2);
+}
+// Byte offset of (row, byte k) in a 128-row K-major operand tile without
+// swizzle: 8-row x 16-byte core matrices, K-adjacent ones 128 B apart,
+// 8-row groups (kbytes / 16) * 128 B apart.
+__host__ __device__ inline size_t umma_offset(int row, int kbyte, int kbytes) {
+    return (size_t)(row >> 3) * (size_t)(kbytes >> 4) * 128 + (size_t)(kbyte >> 4) * 128 +
+           (size_t)(row & 7) * 16 + (size_t)(kbyte & 15);
+}
+
 // ---- host launch wrappers (each returns cudaGetLastError()) ---------------
-cudaError_t launch_prep(const void *points, int dtype, int64_t n, int d, float eps,
+cudaError_t launch_prep(const void *points, int dtype, int64_t n, int d, float eps, int allow_tc,
                         const Work &w, const Layout &L, cudaStream_t s);
+cudaError_t launch_stage_umma(const Work &w, const Layout &L, int which, cudaStream_t s);
 cudaError_t launch_count(const Work &w, const Layout &L, cudaStream_t s);
 cudaError_t launch_compact(const Work &w, const Layout &L, int min_pts,
                            int32_t *labels, uint8_t *is_core, cudaStream_t s);
@@ -85,6 +120,11 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s);
 cudaError_t launch_flatten(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
 cudaError_t launch_border(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
 cudaError_t launch_finalize(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
+
+cudaError_t launch_count_tc(const Work &w, const Layout &L, cudaStream_t s);
+cudaError_t launch_union_tc_wave(const Work &w, const Layout &L, int wave, int ulo, int uhi,
+                                 cudaStream_t s);
+cudaError_t launch_border_tc(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
 
 int persistent_ctas(const void *kernel, int threads, size_t smem);
 

@@ -17,6 +17,17 @@
 // [-sum_k M_k^2, R] (M_k the largest |c_k|), so for integer data with R < 2^24
 // every value is an exactly representable integer.  Without centring the
 // page's form overflows 2^24 already at d = 3 over [0, 2047].
+//
+// Tensor-core operands.  When every centred coordinate is an integer small
+// enough for the MMA input type (|2c| <= 2048 for tf32, <= 256 for bf16), the
+// pair quantity w_ij = |c_i - c_j|^2 - thrx is written as one dot product
+//     A_i = [-2 c_i,  1, B, ..,   n0_i, n1_i, ..,  -h0, -h1, ..]
+//     B_j = [   c_j,  n0_j, n1_j, .., 1, B, ..,     1,   B, ..]
+// with |c|^2 = sum_k n_k B^k and thrx = sum_k h_k B^k (all digits in [0, B)),
+// every element exactly representable.  The positive terms sum to at most
+// 4 S and the negative ones to at most 2 S + thrx (S = sum_k M_k^2); when both
+// are below 2^24 every partial sum the tensor core forms, in any order, is an
+// exact integer, and w_ij < 0 <=> neighbour.
 #include "dbscan_internal.cuh"
 
 #include <math.h>
@@ -77,10 +88,13 @@ __global__ void k_stats(const void *pts, int dtype, int64_t n, int d, Ctrl *ctrl
     }
 }
 
-// One block: centres, the exactness bound and the threshold constant.
+// One block: centres, the exactness bound, the threshold constant and the
+// tensor-core path (allow: mask of TC_ALLOW_* the caller permits).
 __global__ void k_setup(Ctrl *ctrl, const int *smin, const int *smax, float *centre,
-                        int d, float eps2) {
+                        int d, float eps2, int allow) {
     __shared__ double part[DBSCAN_MAX_D];
+    __shared__ double mpart[DBSCAN_MAX_D];
+    __shared__ double rpart[DBSCAN_MAX_D];
     const bool integral = ctrl->nonint == 0;
     for (int k = threadIdx.x; k < d; k += blockDim.x) {
         float lo = key_float(smin[k]), hi = key_float(smax[k]);
@@ -89,11 +103,18 @@ __global__ void k_setup(Ctrl *ctrl, const int *smin, const int *smax, float *cen
         centre[k] = c;
         double r = (double)hi - (double)lo;
         part[k] = r * r;
+        double m = fmax((double)hi - (double)c, (double)c - (double)lo);
+        mpart[k] = m * m;
+        rpart[k] = r;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        double R = 0.0;
-        for (int k = 0; k < d; ++k) R += part[k];
+        double R = 0.0, S = 0.0, rmax = 0.0;
+        for (int k = 0; k < d; ++k) {
+            R += part[k];
+            S += mpart[k];
+            rmax = fmax(rmax, rpart[k]);
+        }
         ctrl->range_sq = (float)R;
         if (integral) {
             double t = floor((double)eps2);
@@ -103,8 +124,112 @@ __global__ void k_setup(Ctrl *ctrl, const int *smin, const int *smax, float *cen
             ctrl->thrx = eps2;
         }
         ctrl->exact = (integral && R < 16777215.0) ? 1 : 0;
+        // tensor-core eligibility (integer data, exact elements, exact sums)
+        const double thrx = (double)ctrl->thrx;
+        const int nt = thrx < 2048.0 ? 1 : (thrx < 4194304.0 ? 2 : 3);
+        int kind = TC_NONE;
+        if (integral && !ctrl->nonfinite && 4.0 * S < 16777216.0 && 2.0 * S + thrx < 16777216.0) {
+            const int ntb = thrx < 256.0 ? 1 : (thrx < 65536.0 ? 2 : 3);
+            if ((allow & TC_ALLOW_BF16) && rmax <= 256.0 &&
+                tc_kbytes(TC_BF16, d, ntb) <= TC_MAX_KBYTES) {
+                kind = TC_BF16;
+                ctrl->tc_nt = ntb;
+            } else if ((allow & TC_ALLOW_TF32) && rmax <= 2048.0 &&
+                       tc_kbytes(TC_TF32, d, nt) <= TC_MAX_KBYTES) {
+                kind = TC_TF32;
+                ctrl->tc_nt = nt;
+            }
+        }
+        ctrl->tc_kind = kind;
+        ctrl->tc_kpad = kind ? tc_kpad(kind, d, ctrl->tc_nt) : 0;
+        ctrl->tc_kbytes = kind ? tc_kbytes(kind, d, ctrl->tc_nt) : 0;
         if (ctrl->nonfinite) set_error(ctrl, DBSCAN_ERR_INVALID_ARG);
     }
+}
+
+// Write element k of an operand row: float bits for tf32, bf16 otherwise.
+__device__ __forceinline__ void put_elem(uint8_t *tile, int row, int k, int kbytes, int kind,
+                                         float v) {
+    if (kind == TC_TF32) {
+        *reinterpret_cast<float *>(tile + umma_offset(row, 4 * k, kbytes)) = v;
+    } else {
+        *reinterpret_cast<__nv_bfloat16 *>(tile + umma_offset(row, 2 * k, kbytes)) =
+            __float2bfloat16_rn(v);
+    }
+}
+
+// Tensor-core operand tiles from the staged points: A (row form) and,
+// optionally, B (column form).  Tiles are packed back to back (128 x kbytes
+// each) so that consecutive tiles can be copied in one piece.  Slots at or
+// beyond *count are zero; the sweep masks them out by index.
+__global__ void k_stage_umma(const Ctrl *ctrl, const int *count, const float *staged, int d,
+                             int64_t npad, uint8_t *ua, uint8_t *ub) {
+    const int kind = ctrl->tc_kind;
+    if (kind == TC_NONE) return;
+    const int kpad = ctrl->tc_kpad, kbytes = ctrl->tc_kbytes, nt = ctrl->tc_nt;
+    const size_t tile_stride = (size_t)BT * kbytes;
+    const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= npad) return;
+    const int64_t tile = p / BT;
+    const int row = (int)(p % BT);
+    uint8_t *ta = ua + (size_t)tile * tile_stride;
+    uint8_t *tb = ub ? ub + (size_t)tile * tile_stride : nullptr;
+    if (p >= *count) {
+        for (int k = 0; k < kpad; ++k) {
+            put_elem(ta, row, k, kbytes, kind, 0.f);
+            if (tb) put_elem(tb, row, k, kbytes, kind, 0.f);
+        }
+        return;
+    }
+    const int base = kind == TC_TF32 ? 2048 : 256;
+    const int nd = tc_norm_digits(kind);
+    const float *src = staged + (size_t)tile * (size_t)(d + 1) * BT + row;
+    int k = 0;
+    for (; k < d; ++k) {
+        const float c = src[(size_t)k * BT];
+        put_elem(ta, row, k, kbytes, kind, -2.f * c);
+        if (tb) put_elem(tb, row, k, kbytes, kind, c);
+    }
+    const int nrm = (int)src[(size_t)d * BT];
+    // column norm: B holds its digits, A the powers of the base
+    int pw = 1, nr = nrm;
+    for (int j = 0; j < nd; ++j, ++k, pw *= base, nr /= base) {
+        put_elem(ta, row, k, kbytes, kind, (float)pw);
+        if (tb) put_elem(tb, row, k, kbytes, kind, (float)(nr % base));
+    }
+    // row norm: A holds its digits, B the powers of the base
+    pw = 1, nr = nrm;
+    for (int j = 0; j < nd; ++j, ++k, pw *= base, nr /= base) {
+        put_elem(ta, row, k, kbytes, kind, (float)(nr % base));
+        if (tb) put_elem(tb, row, k, kbytes, kind, (float)pw);
+    }
+    // threshold constant: -digits in A, powers in B
+    pw = 1;
+    int th = (int)ctrl->thrx;
+    for (int j = 0; j < nt; ++j, ++k, pw *= base, th /= base) {
+        put_elem(ta, row, k, kbytes, kind, (float)(-(th % base)));
+        if (tb) put_elem(tb, row, k, kbytes, kind, (float)pw);
+    }
+    for (; k < kpad; ++k) {
+        put_elem(ta, row, k, kbytes, kind, 0.f);
+        if (tb) put_elem(tb, row, k, kbytes, kind, 0.f);
+    }
+}
+
+cudaError_t launch_stage_umma(const Work &w, const Layout &L, int which, cudaStream_t s) {
+    if (L.umma_tile_bytes == 0) return cudaSuccess;
+    const int64_t npad = L.ntiles * BT;
+    const int blocks = (int)((npad + 255) / 256);
+    if (which == 0)
+        k_stage_umma<<<blocks, 256, 0, s>>>(w.ctrl, &w.ctrl->n_all, w.staged_all, L.d, npad,
+                                            w.ua_all, w.ub_all);
+    else if (which == 1)
+        k_stage_umma<<<blocks, 256, 0, s>>>(w.ctrl, &w.ctrl->n_core, w.staged_core, L.d, npad,
+                                            w.ua_core, w.ub_core);
+    else
+        k_stage_umma<<<blocks, 256, 0, s>>>(w.ctrl, &w.ctrl->n_cand, w.staged_cand, L.d, npad,
+                                            w.ua_cand, nullptr);
+    return cudaGetLastError();
 }
 
 // One thread per (padded) point: centred coordinates and norm into the
@@ -140,7 +265,7 @@ __global__ void k_stage(const void *pts, int dtype, int64_t n, int d, const Ctrl
     }
 }
 
-cudaError_t launch_prep(const void *points, int dtype, int64_t n, int d, float eps,
+cudaError_t launch_prep(const void *points, int dtype, int64_t n, int d, float eps, int allow_tc,
                         const Work &w, const Layout &L, cudaStream_t s) {
     const float eps2 = eps * eps;
     k_init_stats<<<1, 256, 0, s>>>(w.ctrl, w.stat_min, w.stat_max, n, d);
@@ -150,12 +275,15 @@ cudaError_t launch_prep(const void *points, int dtype, int64_t n, int d, float e
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     k_stats<<<blocks, 256, 0, s>>>(points, dtype, n, d, w.ctrl, w.stat_min, w.stat_max);
-    k_setup<<<1, 256, 0, s>>>(w.ctrl, w.stat_min, w.stat_max, w.centre, d, eps2);
+    k_setup<<<1, 256, 0, s>>>(w.ctrl, w.stat_min, w.stat_max, w.centre, d, eps2,
+                              L.umma_tile_bytes ? allow_tc : 0);
     const int64_t npad = L.ntiles * BT;
     int sblocks = (int)((npad + 255) / 256);
     k_stage<<<sblocks, 256, d * sizeof(float), s>>>(points, dtype, n, d, w.ctrl, w.centre,
                                                      w.staged_all, w.T_all, npad);
-    return cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_stage_umma(w, L, 0, s);
 }
 
 }  // namespace dbscan

@@ -220,6 +220,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
     extern __shared__ __align__(16) float smem[];
     __shared__ unsigned s_unit;
 
+    if (a.ctrl->tc_kind != TC_NONE) return;   // the tensor-core sweep handles this data
     const int tid = threadIdx.x;
     const int tr = tid >> 4, tc = tid & 15;
     const int n_rows = *a.n_rows, n_cols = *a.n_cols;
@@ -343,6 +344,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
     float *rowbuf = smem;                  // D * BT floats: -2 c of the row tile
     float *stages = smem + D * BT;         // S * STAGE floats
 
+    if (a.ctrl->tc_kind != TC_NONE) return;   // the tensor-core sweep handles this data
     const int tid = threadIdx.x;
     const int tr = tid >> 4, tc = tid & 15;
     const int n_rows = *a.n_rows, n_cols = *a.n_cols;
@@ -517,7 +519,9 @@ cudaError_t launch_count(const Work &w, const Layout &L, cudaStream_t s) {
     a.cols = w.staged_all; a.n_cols = &w.ctrl->n_all;
     a.tri = 1; a.ulo = 0; a.uhi = -1;
     a.ctr = &w.ctrl->unit_ctr[CTR_COUNT]; a.ctrl = w.ctrl; a.cnt = w.cnt;
-    return dispatch<SWEEP_COUNT>(a, L.d, s);
+    cudaError_t e = dispatch<SWEEP_COUNT>(a, L.d, s);
+    if (e != cudaSuccess) return e;
+    return launch_count_tc(w, L, s);
 }
 
 cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
@@ -531,6 +535,8 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
         a.uhi = kUnionWaveEdges[wv + 1];
         a.ctr = &w.ctrl->unit_ctr[CTR_UNION0 + wv];
         cudaError_t e = dispatch<SWEEP_UNION>(a, L.d, s);
+        if (e != cudaSuccess) return e;
+        e = launch_union_tc_wave(w, L, wv, a.ulo, a.uhi, s);
         if (e != cudaSuccess) return e;
         if (wv + 1 < UNION_WAVES) {
             k_compress<<<grid, 256, 0, s>>>(w.ctrl, w.parent);
@@ -547,7 +553,9 @@ cudaError_t launch_border(const Work &w, const Layout &L, int32_t *labels, cudaS
     a.tri = 0; a.ulo = 0; a.uhi = -1;
     a.ctr = &w.ctrl->unit_ctr[CTR_BORDER]; a.ctrl = w.ctrl;
     a.candidx = w.candidx; a.labels = labels;
-    return dispatch<SWEEP_BORDER>(a, L.d, s);
+    cudaError_t e = dispatch<SWEEP_BORDER>(a, L.d, s);
+    if (e != cudaSuccess) return e;
+    return launch_border_tc(w, L, labels, s);
 }
 
 }  // namespace dbscan

@@ -1,0 +1,582 @@
+// Tensor-core sweeps (tcgen05): the same three passes as sweep.cu -- count,
+// union, border -- with the pair quantity produced by the MMA unit.
+//
+// The squared distance is a dense contraction once the point-only terms are
+// hoisted ("Design and optimization of DBSCAN Algorithm based on CUDA",
+// §IV-B2).  prep.cu writes each point as a tf32 or bf16 operand row whose dot
+// product with another point's row is exactly w_ij = |c_i - c_j|^2 - thrx, so
+// one 128 x 128 x K MMA evaluates a whole tile and a pair is a neighbour iff
+// w_ij < 0.  The CUDA cores only read the accumulator and test signs.
+//
+// CTA = 18 warps, one per SM (the CTA owns all 512 TMEM columns):
+//   warp 16     producer: pulls work units and bulk-copies (cp.async.bulk) the
+//               row operand tile of a unit and groups of up to 8 consecutive
+//               column tiles (plus their aux ints) into a ring of shared-memory
+//               stages; lanes take turns issuing, since the bulk copies of one
+//               thread complete one after another;
+//   warp 17     MMA: one thread issues a 128 x 256 x K MMA per pair of column
+//               tiles into one of two 256-column TMEM accumulators and commits
+//               completion to mbarriers;
+//   warps 0-15  epilogue: each warp reads its 32 rows x 64 columns of every
+//               accumulator (tcgen05.ld), ORs the sign bits of each 32 x 32
+//               block and, only where a block holds a neighbour, builds exact
+//               per-row bit masks.  Counting credits the row with a popcount
+//               and the columns through a warp bit transpose; union and border
+//               act on each neighbour pair as on CUDA cores.
+// Every wait on an mbarrier is bounded; on timeout the CTA records
+// DBSCAN_ERR_INTERNAL, stops issuing work, waits (bounded) for its own copies
+// and MMAs in flight, frees its TMEM and returns.
+#include "dbscan_internal.cuh"
+
+#include <map>
+#include <mutex>
+
+namespace dbscan {
+namespace {
+
+constexpr int EPI_WARPS = 16;                       // four epilogue warpgroups
+constexpr int TC_THREADS = (EPI_WARPS + 2) * 32;
+constexpr int PRODUCER_WARP = EPI_WARPS, MMA_WARP = EPI_WARPS + 1;
+constexpr int NACC = 2;                 // TMEM accumulators of 256 columns
+constexpr int ACC_COLS = 256;
+constexpr int TMEM_COLS = 512;
+constexpr int TC_MAX_STAGES = 4;
+constexpr int TC_MAX_GROUP = 8;         // column tiles per stage (one bulk copy)
+constexpr int ISSUE_LANES = 8;          // producer lanes that take turns issuing copies
+constexpr long long WAIT_LIMIT = 8000000000LL;   // clock cycles (about 4 s)
+constexpr int UF_CAP = 1 << 22;
+
+constexpr int F_FIRST = 1, F_LAST = 2, F_DIAG = 4, F_TERM = 8;
+
+struct TcArgs {
+    const uint8_t *ua, *ub;   // row / column operand tiles, packed 128 x kbytes each
+    const int *n_rows, *n_cols;
+    const int *aux;           // per-column int staged with the tiles (parent or label), or null
+    int tri, ulo, uhi;
+    unsigned *ctr;
+    Ctrl *ctrl;
+    int *cnt, *parent;
+    const int *candidx;
+    int32_t *labels;
+    int stages;               // ring depth
+    int group;                // column tiles per stage
+    int stage_bytes;          // bytes reserved per stage (group tiles + group x BT ints)
+    int tile_bytes_max;       // bytes reserved per operand tile
+};
+
+struct Meta {
+    int rb, t_first, ntiles, flags, abuf;
+};
+
+// ---- PTX wrappers ------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait; false on timeout or when another role aborted.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                       Ctrl *ctrl) {
+    long long start = 0;
+    for (unsigned it = 0;; ++it) {
+        if (mbar_try(bar, parity)) return true;
+        if ((it & 63) == 63) {
+            if (*abort_flag) return false;
+            const long long now = clock64();
+            if (start == 0) start = now;
+            else if (now - start > WAIT_LIMIT) {
+                set_error(ctrl, DBSCAN_ERR_INTERNAL);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+// Bounded wait that ignores the abort flag (draining copies in flight).
+__device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+    const long long start = clock64();
+    while (!mbar_try(bar, parity))
+        if (clock64() - start > WAIT_LIMIT) return;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)(128u >> 4) << 16;                   // leading (K) core-matrix stride
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;         // 8-row group stride
+    d |= (uint64_t)1 << 46;                             // tcgen05 descriptor version
+    return d;                                           // no swizzle, base offset 0
+}
+// D f32, A and B of format fmt, both K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t umma_idesc(int fmt, int n) {
+    return (1u << 4) | ((uint32_t)fmt << 7) | ((uint32_t)fmt << 10) | (((uint32_t)n >> 3) << 17) |
+           ((128u >> 4) << 24);
+}
+template <int KIND>
+__device__ __forceinline__ void umma(uint32_t tmem, uint64_t da, uint64_t db, uint32_t idesc,
+                                     uint32_t accumulate) {
+    if (KIND == TC_TF32)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n"
+            ::"r"(tmem), "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
+            ::"r"(tmem), "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---- union-find (same invariants as the CUDA-core sweep) ---------------------
+__device__ __noinline__ int tc_find(int *parent, int x, Ctrl *ctrl) {
+    for (int it = 0; it < UF_CAP; ++it) {
+        int p = __ldcg(parent + x);
+        if (p == x) return x;
+        int gp = __ldcg(parent + p);
+        if (gp != p) __stcg(parent + x, gp);
+        x = gp;
+    }
+    set_error(ctrl, DBSCAN_ERR_INTERNAL);
+    return x;
+}
+__device__ __noinline__ int tc_unite(int *parent, int a, int b, Ctrl *ctrl) {
+    for (int it = 0; it < UF_CAP; ++it) {
+        a = tc_find(parent, a, ctrl);
+        b = tc_find(parent, b, ctrl);
+        if (a == b) return a;
+        if (a < b) { int t = a; a = b; b = t; }
+        if (atomicCAS(parent + a, a, b) == a) return b;
+    }
+    set_error(ctrl, DBSCAN_ERR_INTERNAL);
+    return min(a, b);
+}
+
+// 32 x 32 bit transpose across a warp: lane i bit j -> lane j bit i.
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
+    const uint32_t masks[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+    for (int st = 0; st < 5; ++st) {
+        const int s = 16 >> st;
+        const uint32_t m = masks[st];
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, s);
+        x = (lane & s) ? ((x & ~m) | ((y >> s) & m)) : ((x & m) | ((y & m) << s));
+    }
+    return x;
+}
+
+// ---- unit schedule (as in the CUDA-core sweep) ---------------------------------
+struct TcSched {
+    int nrt, nct, uc, kc;
+    unsigned units, ubegin, uend;
+};
+__device__ __forceinline__ TcSched tc_sched(int n_rows, int n_cols, int tri, int ulo, int uhi) {
+    TcSched s;
+    s.nrt = (n_rows + BT - 1) / BT;
+    s.nct = (n_cols + BT - 1) / BT;
+    long long total = tri ? (long long)s.nrt * (s.nrt + 1) / 2 : (long long)s.nrt * s.nct;
+    long long target = 8LL * gridDim.x;
+    long long uc = (total + target - 1) / target;
+    if (uc < 1) uc = 1;
+    if (uc > s.nct) uc = s.nct;
+    s.uc = (int)uc;
+    s.kc = (s.nct + s.uc - 1) / s.uc;
+    s.units = (unsigned)((long long)s.nrt * s.kc);
+    const long long g = gridDim.x;
+    s.ubegin = (unsigned)min((long long)s.units, ulo * g);
+    s.uend = uhi < 0 ? s.units : (unsigned)min((long long)s.units, uhi * g);
+    return s;
+}
+
+// ---- the kernel --------------------------------------------------------------------
+template <int MODE, int KIND>
+__global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
+    Ctrl *ctrl = a.ctrl;
+    if (ctrl->tc_kind != KIND) return;     // another path was selected for this data
+    const int n_rows = *a.n_rows, n_cols = *a.n_cols;
+    if (n_rows <= 0 || n_cols <= 0) return;
+    constexpr bool AUX = MODE != SWEEP_COUNT;
+    constexpr unsigned FULL = 0xffffffffu;
+
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int S = a.stages, G = a.group;
+    // layout: [A0 | A1 | stage 0 .. stage S-1 | barriers | meta | misc]; a stage
+    // holds up to G column tiles back to back, then G x BT ints of aux data
+    uint8_t *sA = smem;
+    uint8_t *sStage = smem + 2 * (size_t)a.tile_bytes_max;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + (size_t)S * a.stage_bytes);
+    uint64_t *b_full = bars, *b_empty = bars + TC_MAX_STAGES;
+    uint64_t *a_full = bars + 2 * TC_MAX_STAGES, *a_empty = a_full + 2;
+    uint64_t *acc_full = a_empty + 2, *acc_empty = acc_full + NACC;
+    uint64_t *drain_bar = acc_empty + NACC;
+    Meta *meta = reinterpret_cast<Meta *>(drain_bar + 1);
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(meta + TC_MAX_STAGES);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kbytes = ctrl->tc_kbytes;
+    const uint32_t tile_bytes = 128u * (uint32_t)kbytes;   // one packed 128-point tile
+    const uint32_t sbo = (uint32_t)(kbytes >> 4) * 128u;
+    const int ksteps = kbytes / 32;        // 8 tf32 or 16 bf16 elements per MMA
+
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(smem_addr(&b_full[i]), 1);
+            mbar_init(smem_addr(&b_empty[i]), 1 + EPI_WARPS);   // MMA commit + every epilogue warp
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_addr(&a_full[i]), 1);
+            mbar_init(smem_addr(&a_empty[i]), 1);
+        }
+        for (int i = 0; i < NACC; ++i) {
+            mbar_init(smem_addr(&acc_full[i]), 1);
+            mbar_init(smem_addr(&acc_empty[i]), EPI_WARPS);
+        }
+        mbar_init(smem_addr(drain_bar), 1);
+        *s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == MMA_WARP) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_addr(s_tmem)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    const TcSched sc = tc_sched(n_rows, n_cols, a.tri, a.ulo, a.uhi);
+
+    if (warp == PRODUCER_WARP) {
+        // The whole warp walks the schedule; the copies of consecutive stages
+        // are issued by different lanes, since one thread's bulk copies
+        // complete one after another.
+        int k = 0, ua = 0, a_issued = 0;
+        bool ok = true;
+        for (;;) {
+            unsigned u = 0;
+            if (lane == 0) u = sc.ubegin + atomicAdd(a.ctr, 1u);
+            u = __shfl_sync(FULL, u, 0);
+            if (u >= sc.uend) break;
+            const int rb = (int)(u / sc.kc);
+            const int c = (int)(u % sc.kc);
+            const int t0 = a.tri ? rb + c * sc.uc : c * sc.uc;
+            if (t0 >= sc.nct) continue;
+            const int t1 = min(t0 + sc.uc, sc.nct);
+            const int ab = ua & 1;
+            ok = __all_sync(FULL, mbar_wait(smem_addr(&a_empty[ab]), ((ua >> 1) & 1) ^ 1, s_abort, ctrl));
+            if (!ok) break;
+            if (lane == ISSUE_LANES + (ua % ISSUE_LANES)) {
+                mbar_expect_tx(smem_addr(&a_full[ab]), tile_bytes);
+                bulk_g2s(smem_addr(sA + (size_t)ab * a.tile_bytes_max),
+                         a.ua + (size_t)rb * tile_bytes, tile_bytes, smem_addr(&a_full[ab]));
+            }
+            a_issued = ua + 1;
+            for (int tf = t0; tf < t1; tf += G) {
+                const int s = k % S;
+                const int nt = min(G, t1 - tf);
+                ok = __all_sync(FULL, mbar_wait(smem_addr(&b_empty[s]), ((k / S) & 1) ^ 1, s_abort, ctrl));
+                if (!ok) break;
+                if (lane == 0) {
+                    Meta m;
+                    m.rb = rb;
+                    m.t_first = tf;
+                    m.ntiles = nt;
+                    m.flags = (tf == t0 ? F_FIRST : 0) | (tf + nt == t1 ? F_LAST : 0);
+                    m.abuf = ab;
+                    meta[s] = m;
+                }
+                __syncwarp();
+                if (lane == k % ISSUE_LANES) {
+                    uint8_t *dst = sStage + (size_t)s * a.stage_bytes;
+                    mbar_expect_tx(smem_addr(&b_full[s]),
+                                   (uint32_t)nt * tile_bytes + (AUX ? (uint32_t)nt * BT * 4u : 0u));
+                    bulk_g2s(smem_addr(dst), a.ub + (size_t)tf * tile_bytes, (uint32_t)nt * tile_bytes,
+                             smem_addr(&b_full[s]));
+                    if (AUX)
+                        bulk_g2s(smem_addr(dst + (size_t)G * a.tile_bytes_max), a.aux + (size_t)tf * BT,
+                                 (uint32_t)nt * BT * 4u, smem_addr(&b_full[s]));
+                }
+                ++k;
+            }
+            ++ua;
+            if (!ok) break;
+        }
+        if (ok) {   // terminate marker (every consumer reads every stage)
+            const int s = k % S;
+            ok = __all_sync(FULL, mbar_wait(smem_addr(&b_empty[s]), ((k / S) & 1) ^ 1, s_abort, ctrl));
+            if (ok && lane == 0) {
+                meta[s].flags = F_TERM;
+                mbar_arrive(smem_addr(&b_full[s]));
+            }
+        }
+        if (!ok && lane == 0) {   // let the copies already issued land before the CTA exits
+            for (int j = max(0, k - S); j < k; ++j) mbar_drain(smem_addr(&b_full[j % S]), (j / S) & 1);
+            for (int j = max(0, a_issued - 2); j < a_issued; ++j)
+                mbar_drain(smem_addr(&a_full[j & 1]), (j >> 1) & 1);
+        }
+    } else if (warp == MMA_WARP) {
+        if (lane == 0) {
+            const int fmt = KIND == TC_TF32 ? 2 : 1;
+            const uint32_t idesc256 = umma_idesc(fmt, 256), idesc128 = umma_idesc(fmt, 128);
+            int k = 0, ua = 0, it = 0;
+            bool issued = false, ok = true;
+            for (;;) {
+                const int s = k % S;
+                if (!mbar_wait(smem_addr(&b_full[s]), (k / S) & 1, s_abort, ctrl)) break;
+                const Meta m = meta[s];
+                if (m.flags & F_TERM) break;
+                if (m.flags & F_FIRST)
+                    if (!mbar_wait(smem_addr(&a_full[m.abuf]), (ua >> 1) & 1, s_abort, ctrl)) break;
+                const uint32_t abase = smem_addr(sA + (size_t)m.abuf * a.tile_bytes_max);
+                const uint32_t sbase = smem_addr(sStage + (size_t)s * a.stage_bytes);
+                for (int i = 0; 2 * i < m.ntiles; ++i, ++it) {
+                    const int b = it % NACC;
+                    if (!(ok = mbar_wait(smem_addr(&acc_empty[b]), ((it / NACC) & 1) ^ 1, s_abort, ctrl)))
+                        break;
+                    tc_fence_after();
+                    // a pair of consecutive column tiles is one 256-row B operand
+                    const uint32_t bbase = sbase + (uint32_t)(2 * i) * tile_bytes;
+                    const uint32_t idesc = 2 * i + 1 < m.ntiles ? idesc256 : idesc128;
+                    for (int ks = 0; ks < ksteps; ++ks)
+                        umma<KIND>(tmem + (uint32_t)(b * ACC_COLS), umma_desc(abase + ks * 256, sbo),
+                                   umma_desc(bbase + ks * 256, sbo), idesc, ks > 0 ? 1u : 0u);
+                    issued = true;
+                    umma_commit(smem_addr(&acc_full[b]));
+                }
+                if (!ok) break;
+                umma_commit(smem_addr(&b_empty[s]));
+                if (m.flags & F_LAST) {
+                    umma_commit(smem_addr(&a_empty[m.abuf]));
+                    ++ua;
+                }
+                ++k;
+            }
+            if (issued) {   // no MMA may be in flight when TMEM is freed
+                umma_commit(smem_addr(drain_bar));
+                mbar_drain(smem_addr(drain_bar), 0);
+            }
+        }
+    } else {
+        // ---------------- epilogue: 16 warps split each 256-column item ----------------
+        const int wg = warp >> 2, wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const int cw = wg * 64;                 // this warp's 64 columns of the item
+        const int h = cw >> 7, cb0 = cw & 127;  // tile of the pair, column offset in it
+        int last_rb = -1, acc = -1;             // UNION: a known ancestor of this row's point
+        int k = 0, it = 0;
+        for (;;) {
+            const int s = k % S;
+            // every lane waits; the warp goes on only if all lanes saw the phase
+            if (!__all_sync(FULL, mbar_wait(smem_addr(&b_full[s]), (k / S) & 1, s_abort, ctrl))) break;
+            const Meta m = meta[s];
+            if (m.flags & F_TERM) break;
+            const int p = m.rb * BT + row;
+            const bool rowvalid = p < n_rows;
+            if (MODE == SWEEP_UNION && m.rb != last_rb) {
+                acc = rowvalid ? tc_find(a.parent, p, ctrl) : -1;
+                last_rb = m.rb;
+            }
+            const int *saux = reinterpret_cast<const int *>(sStage + (size_t)s * a.stage_bytes +
+                                                            (size_t)G * a.tile_bytes_max);
+            int rowadd = 0, rowmin = 0x7fffffff;
+            bool ok = true;
+            for (int i = 0; 2 * i < m.ntiles; ++i, ++it) {
+                const int b = it % NACC;
+                if (!(ok = __all_sync(FULL, mbar_wait(smem_addr(&acc_full[b]), (it / NACC) & 1, s_abort, ctrl))))
+                    break;
+                tc_fence_after();
+                const int ti = 2 * i + h;             // tile within the stage
+                const bool have = ti < m.ntiles;      // warp-uniform
+                uint32_t v0[32], v1[32];
+                if (have) {
+                    const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(b * ACC_COLS + cw);
+                    tmem_ld32(taddr, v0);
+                    tmem_ld32(taddr + 32, v1);
+                    tmem_ld_wait();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&acc_empty[b]));
+                if (!have) continue;
+                const int tile = m.t_first + ti;
+                const bool diag = a.tri && tile == m.rb;
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    uint32_t (&v)[32] = blk ? v1 : v0;
+                    const int cb = cb0 + blk * 32;            // column offset in the tile
+                    const int qbase = tile * BT + cb;
+                    uint32_t o = 0;
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) o |= v[c] | v[c + 1];
+                    if (!__any_sync(FULL, rowvalid && (o >> 31))) continue;
+                    uint32_t mask = 0;
+#pragma unroll
+                    for (int c = 31; c >= 0; --c) mask = __funnelshift_l(v[c], mask, 1);   // bit c = w < 0
+                    const int nv = n_cols - qbase;
+                    mask &= nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
+                    if (!rowvalid) mask = 0;
+                    if (MODE == SWEEP_COUNT) {
+                        rowadd += __popc(mask);
+                        if (!diag) {   // the diagonal tile is counted from both sides already
+                            const int cc = __popc(warp_transpose32(mask, lane));
+                            if (cc) atomicAdd(a.cnt + qbase + lane, cc);
+                        }
+                    } else {
+                        while (mask) {
+                            const int cq = __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            const int q = qbase + cq;
+                            const int aq = saux[ti * BT + cb + cq];
+                            if (MODE == SWEEP_UNION) {
+                                if (diag && q <= p) continue;
+                                if (aq == acc) continue;
+                                acc = tc_unite(a.parent, acc, aq, ctrl);
+                            } else {
+                                rowmin = min(rowmin, aq);
+                            }
+                        }
+                    }
+                }
+            }
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&b_empty[s]));
+            if (MODE == SWEEP_COUNT && rowadd) atomicAdd(a.cnt + p, rowadd);
+            if (MODE == SWEEP_BORDER && rowmin != 0x7fffffff) atomicMin(a.labels + a.candidx[p], rowmin);
+            ++k;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == MMA_WARP)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                     : "memory");
+}
+
+// Bytes of shared memory the kernel needs.
+size_t tc_smem_bytes(int tile_bytes, int stage_bytes, int stages) {
+    return 2 * (size_t)tile_bytes + (size_t)stages * stage_bytes +
+           (2 * TC_MAX_STAGES + 4 + 2 * NACC + 1) * sizeof(uint64_t) + TC_MAX_STAGES * sizeof(Meta) +
+           16;
+}
+
+template <int MODE, int KIND>
+cudaError_t run_tc(TcArgs a, const Layout &L, cudaStream_t s) {
+    const int kb = tc_kbytes(KIND, L.d, 3);   // largest operand row this path can need
+    if (L.umma_tile_bytes == 0 || kb > TC_MAX_KBYTES) return cudaSuccess;   // never selected
+    auto kernel = k_sweep_tc<MODE, KIND>;
+    const int tile = 128 * kb;
+    const int aux = MODE != SWEEP_COUNT ? BT * 4 : 0;
+    const size_t budget = 200 * 1024;
+    int group = TC_MAX_GROUP;
+    while (group > 2 && 2 * (size_t)tile + 2 * (size_t)group * (tile + aux) > budget) group -= 2;
+    const int stage_bytes = group * (tile + aux);
+    int stages = (int)((budget - 2 * (size_t)tile) / stage_bytes);
+    if (stages > TC_MAX_STAGES) stages = TC_MAX_STAGES;
+    if (stages < 2) stages = 2;
+    size_t smem = tc_smem_bytes(tile, stage_bytes, stages);
+    if (smem < 120 * 1024) smem = 120 * 1024;   // one CTA per SM: it owns all of TMEM
+    cudaError_t e = cudaFuncSetAttribute((const void *)kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    a.stages = stages;
+    a.group = group;
+    a.stage_bytes = stage_bytes;
+    a.tile_bytes_max = tile;
+    kernel<<<sms, TC_THREADS, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t run_tc_both(const TcArgs &a, const Layout &L, cudaStream_t s) {
+    cudaError_t e = run_tc<MODE, TC_TF32>(a, L, s);
+    if (e != cudaSuccess) return e;
+    return run_tc<MODE, TC_BF16>(a, L, s);
+}
+
+}  // namespace
+
+cudaError_t launch_count_tc(const Work &w, const Layout &L, cudaStream_t s) {
+    TcArgs a{};
+    a.ua = w.ua_all; a.ub = w.ub_all;
+    a.n_rows = &w.ctrl->n_all; a.n_cols = &w.ctrl->n_all;
+    a.tri = 1; a.ulo = 0; a.uhi = -1;
+    a.ctr = &w.ctrl->unit_ctr[0]; a.ctrl = w.ctrl; a.cnt = w.cnt;
+    return run_tc_both<SWEEP_COUNT>(a, L, s);
+}
+
+cudaError_t launch_union_tc_wave(const Work &w, const Layout &L, int wave, int ulo, int uhi,
+                                 cudaStream_t s) {
+    TcArgs a{};
+    a.ua = w.ua_core; a.ub = w.ub_core;
+    a.n_rows = &w.ctrl->n_core; a.n_cols = &w.ctrl->n_core; a.aux = w.parent;
+    a.tri = 1; a.ulo = ulo; a.uhi = uhi;
+    a.ctr = &w.ctrl->unit_ctr[1 + wave]; a.ctrl = w.ctrl; a.parent = w.parent;
+    return run_tc_both<SWEEP_UNION>(a, L, s);
+}
+
+cudaError_t launch_border_tc(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s) {
+    TcArgs a{};
+    a.ua = w.ua_cand; a.ub = w.ub_core;
+    a.n_rows = &w.ctrl->n_cand; a.n_cols = &w.ctrl->n_core; a.aux = w.clabel;
+    a.tri = 0; a.ulo = 0; a.uhi = -1;
+    a.ctr = &w.ctrl->unit_ctr[5]; a.ctrl = w.ctrl;
+    a.candidx = w.candidx; a.labels = labels;
+    return run_tc_both<SWEEP_BORDER>(a, L, s);
+}
+
+}  // namespace dbscan
