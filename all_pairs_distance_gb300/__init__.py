@@ -9,7 +9,7 @@ first call does, and raises if it has not been built.
 __all__ = [
     "dbscan_fit", "dbscan_fit_ex", "dbscan_fit_host", "dbscan_neighbor_counts",
     "dbscan_workspace_size", "dbscan_workspace_status", "dbscan_strerror",
-    "dbscan_profile_begin", "dbscan_profile_end",
+    "dbscan_workspace_info", "dbscan_profile_begin", "dbscan_profile_end",
 ]
 
 _BINDING_NAMES = set(__all__) | {"DbscanError", "Status", "library_path", "load", "workspace_for"}

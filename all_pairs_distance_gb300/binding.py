@@ -68,6 +68,8 @@ def load():
         lib.dbscan_workspace_size.restype = sz
         lib.dbscan_workspace_status.argtypes = [P, P]
         lib.dbscan_workspace_status.restype = ctypes.c_int
+        lib.dbscan_workspace_info.argtypes = [P, P, P, i32]
+        lib.dbscan_workspace_info.restype = ctypes.c_int
         lib.dbscan_profile_begin.argtypes = []
         lib.dbscan_profile_begin.restype = ctypes.c_int
         lib.dbscan_profile_end.argtypes = [P, i32, P, P]
@@ -179,6 +181,18 @@ def dbscan_fit_host(points, eps: float, min_pts: int, *, labels=None, is_core=No
 
 def dbscan_workspace_status(workspace: torch.Tensor, stream=None) -> int:
     return int(load().dbscan_workspace_status(workspace.data_ptr(), _stream_handle(stream)))
+
+
+PATHS = {0: "fp32", 1: "tf32", 2: "bf16"}
+
+
+def dbscan_workspace_info(workspace: torch.Tensor, stream=None) -> dict:
+    """Path chosen, core / candidate counts and exactness of the last call."""
+    out = (ctypes.c_int64 * 5)()
+    _check(load().dbscan_workspace_info(workspace.data_ptr(), _stream_handle(stream), out, 5),
+           "dbscan_workspace_info")
+    return {"path": PATHS.get(int(out[0]), str(out[0])), "n_core": int(out[1]),
+            "n_cand": int(out[2]), "exact": bool(out[3]), "kpad": int(out[4])}
 
 
 STAGES = ("prep", "count", "compact", "union", "flatten", "border", "finalize")

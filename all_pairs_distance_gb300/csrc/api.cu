@@ -346,6 +346,17 @@ int dbscan_neighbor_counts(const void *points, int32_t dtype, int64_t n, int32_t
                       workspace_bytes, stream);
 }
 
+int dbscan_workspace_info(const void *workspace, void *stream, int64_t *info, int32_t n) {
+    if (!workspace || !info || n < 1) return DBSCAN_ERR_INVALID_ARG;
+    Ctrl c;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DBSCAN_ERR_CUDA;
+    if (cudaMemcpy(&c, workspace, sizeof(Ctrl), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return DBSCAN_ERR_CUDA;
+    const int64_t v[5] = {c.tc_kind, c.n_core, c.n_cand, c.exact, c.tc_kpad};
+    for (int i = 0; i < n && i < 5; ++i) info[i] = v[i];
+    return DBSCAN_OK;
+}
+
 int dbscan_profile_begin(void) {
     for (auto &c : g_prof.calls)
         for (int i = 0; i <= c.stages; ++i) cudaEventDestroy(c.ev[i]);

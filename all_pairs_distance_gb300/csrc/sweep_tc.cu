@@ -17,12 +17,17 @@
 //   warp 17     MMA: one thread issues a 128 x 256 x K MMA per pair of column
 //               tiles into one of two 256-column TMEM accumulators and commits
 //               completion to mbarriers;
-//   warps 0-15  epilogue: each warp reads its 32 rows x 64 columns of every
-//               accumulator (tcgen05.ld), ORs the sign bits of each 32 x 32
+//   warps 0-15  epilogue: two groups of 8 warps take alternate tile pairs
+//               (one accumulator each), so one group's TMEM loads overlap the
+//               other's arithmetic.  A warp reads its 32 rows x 128 columns
+//               (tcgen05.ld, 64 at a time), ORs the sign bits of each 32 x 32
 //               block and, only where a block holds a neighbour, builds exact
 //               per-row bit masks.  Counting credits the row with a popcount
-//               and the columns through a warp bit transpose; union and border
-//               act on each neighbour pair as on CUDA cores.
+//               and the columns by atomics (few neighbours) or a warp bit
+//               transpose (many); union and border act on each neighbour pair
+//               as on CUDA cores.
+// The producer and MMA roles poll their barriers without suspending: their
+// reaction time is on the critical path of the accumulator round trip.
 // Every wait on an mbarrier is bounded; on timeout the CTA records
 // DBSCAN_ERR_INTERNAL, stops issuing work, waits (bounded) for its own copies
 // and MMAs in flight, frees its TMEM and returns.
@@ -34,7 +39,7 @@
 namespace dbscan {
 namespace {
 
-constexpr int EPI_WARPS = 16;                       // four epilogue warpgroups
+constexpr int EPI_WARPS = 16;                       // two groups of two warpgroups
 constexpr int TC_THREADS = (EPI_WARPS + 2) * 32;
 constexpr int PRODUCER_WARP = EPI_WARPS, MMA_WARP = EPI_WARPS + 1;
 constexpr int NACC = 2;                 // TMEM accumulators of 256 columns
@@ -82,23 +87,40 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
+// try_wait with a suspend-time hint: a waiting thread sleeps until the phase
+// completes (or about 100 us pass) instead of spinning on the issue slots.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(100000u)
+        : "memory");
+    return ok != 0;
+}
+// Non-blocking probe of a phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}\n"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
 }
-// Bounded wait; false on timeout or when another role aborted.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                       Ctrl *ctrl) {
+// Bounded wait; false on timeout or when another role aborted.  SPIN polls
+// without suspending (a suspended thread resumes hundreds of cycles after
+// the phase completes): used by the single-thread producer and MMA roles,
+// whose reaction time is on the critical path; the epilogue warps suspend.
+template <bool SPIN>
+__device__ __noinline__ bool mbar_wait_t(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         Ctrl *ctrl) {
     long long start = 0;
     for (unsigned it = 0;; ++it) {
-        if (mbar_try(bar, parity)) return true;
-        if ((it & 63) == 63) {
+        if (SPIN ? mbar_test(bar, parity) : mbar_try(bar, parity)) return true;
+        if ((it & (SPIN ? 1023 : 63)) == (SPIN ? 1023 : 63)) {
             if (*abort_flag) return false;
             const long long now = clock64();
             if (start == 0) start = now;
@@ -109,6 +131,14 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
             }
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          Ctrl *ctrl) {
+    return mbar_wait_t<false>(bar, parity, abort_flag, ctrl);
+}
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          Ctrl *ctrl) {
+    return mbar_wait_t<true>(bar, parity, abort_flag, ctrl);
 }
 // Bounded wait that ignores the abort flag (draining copies in flight).
 __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
@@ -279,7 +309,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         }
         for (int i = 0; i < NACC; ++i) {
             mbar_init(smem_addr(&acc_full[i]), 1);
-            mbar_init(smem_addr(&acc_empty[i]), EPI_WARPS);
+            mbar_init(smem_addr(&acc_empty[i]), EPI_WARPS / 2);   // the group that owns it
         }
         mbar_init(smem_addr(drain_bar), 1);
         *s_abort = 0;
@@ -313,7 +343,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             if (t0 >= sc.nct) continue;
             const int t1 = min(t0 + sc.uc, sc.nct);
             const int ab = ua & 1;
-            ok = __all_sync(FULL, mbar_wait(smem_addr(&a_empty[ab]), ((ua >> 1) & 1) ^ 1, s_abort, ctrl));
+            ok = __all_sync(FULL, mbar_spin(smem_addr(&a_empty[ab]), ((ua >> 1) & 1) ^ 1, s_abort, ctrl));
             if (!ok) break;
             if (lane == ISSUE_LANES + (ua % ISSUE_LANES)) {
                 mbar_expect_tx(smem_addr(&a_full[ab]), tile_bytes);
@@ -324,7 +354,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             for (int tf = t0; tf < t1; tf += G) {
                 const int s = k % S;
                 const int nt = min(G, t1 - tf);
-                ok = __all_sync(FULL, mbar_wait(smem_addr(&b_empty[s]), ((k / S) & 1) ^ 1, s_abort, ctrl));
+                ok = __all_sync(FULL, mbar_spin(smem_addr(&b_empty[s]), ((k / S) & 1) ^ 1, s_abort, ctrl));
                 if (!ok) break;
                 if (lane == 0) {
                     Meta m;
@@ -353,7 +383,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         }
         if (ok) {   // terminate marker (every consumer reads every stage)
             const int s = k % S;
-            ok = __all_sync(FULL, mbar_wait(smem_addr(&b_empty[s]), ((k / S) & 1) ^ 1, s_abort, ctrl));
+            ok = __all_sync(FULL, mbar_spin(smem_addr(&b_empty[s]), ((k / S) & 1) ^ 1, s_abort, ctrl));
             if (ok && lane == 0) {
                 meta[s].flags = F_TERM;
                 mbar_arrive(smem_addr(&b_full[s]));
@@ -372,16 +402,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             bool issued = false, ok = true;
             for (;;) {
                 const int s = k % S;
-                if (!mbar_wait(smem_addr(&b_full[s]), (k / S) & 1, s_abort, ctrl)) break;
+                if (!mbar_spin(smem_addr(&b_full[s]), (k / S) & 1, s_abort, ctrl)) break;
                 const Meta m = meta[s];
                 if (m.flags & F_TERM) break;
                 if (m.flags & F_FIRST)
-                    if (!mbar_wait(smem_addr(&a_full[m.abuf]), (ua >> 1) & 1, s_abort, ctrl)) break;
+                    if (!mbar_spin(smem_addr(&a_full[m.abuf]), (ua >> 1) & 1, s_abort, ctrl)) break;
                 const uint32_t abase = smem_addr(sA + (size_t)m.abuf * a.tile_bytes_max);
                 const uint32_t sbase = smem_addr(sStage + (size_t)s * a.stage_bytes);
                 for (int i = 0; 2 * i < m.ntiles; ++i, ++it) {
                     const int b = it % NACC;
-                    if (!(ok = mbar_wait(smem_addr(&acc_empty[b]), ((it / NACC) & 1) ^ 1, s_abort, ctrl)))
+                    if (!(ok = mbar_spin(smem_addr(&acc_empty[b]), ((it / NACC) & 1) ^ 1, s_abort, ctrl)))
                         break;
                     tc_fence_after();
                     // a pair of consecutive column tiles is one 256-row B operand
@@ -407,11 +437,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             }
         }
     } else {
-        // ---------------- epilogue: 16 warps split each 256-column item ----------------
-        const int wg = warp >> 2, wq = warp & 3;
+        // ---------------- epilogue: two groups of 8 warps, alternate items ----------------
+        // Group g takes the items (tile pairs) with index parity g, which the
+        // MMA writes into accumulator g; while one group loads from TMEM the
+        // other computes.  Warp w8 of a group reads TMEM lanes 32*(w8 % 4)..
+        // and the tile w8 / 4 of the pair, 64 columns at a time.
+        const int grp = warp >> 3, w8 = warp & 7, wq = w8 & 3, hw = w8 >> 2;
         const int row = wq * 32 + lane;
-        const int cw = wg * 64;                 // this warp's 64 columns of the item
-        const int h = cw >> 7, cb0 = cw & 127;  // tile of the pair, column offset in it
         int last_rb = -1, acc = -1;             // UNION: a known ancestor of this row's point
         int k = 0, it = 0;
         for (;;) {
@@ -431,58 +463,79 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             int rowadd = 0, rowmin = 0x7fffffff;
             bool ok = true;
             for (int i = 0; 2 * i < m.ntiles; ++i, ++it) {
-                const int b = it % NACC;
-                if (!(ok = __all_sync(FULL, mbar_wait(smem_addr(&acc_full[b]), (it / NACC) & 1, s_abort, ctrl))))
+                if ((it & 1) != grp) continue;        // the other group's item
+                const int b = grp;                    // == it % NACC
+                if (!(ok = __all_sync(FULL, mbar_wait(smem_addr(&acc_full[b]), (it >> 1) & 1, s_abort, ctrl))))
                     break;
                 tc_fence_after();
-                const int ti = 2 * i + h;             // tile within the stage
+                const int ti = 2 * i + hw;            // tile within the stage
                 const bool have = ti < m.ntiles;      // warp-uniform
-                uint32_t v0[32], v1[32];
-                if (have) {
-                    const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(b * ACC_COLS + cw);
-                    tmem_ld32(taddr, v0);
-                    tmem_ld32(taddr + 32, v1);
-                    tmem_ld_wait();
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&acc_empty[b]));
-                if (!have) continue;
                 const int tile = m.t_first + ti;
                 const bool diag = a.tri && tile == m.rb;
+                const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(b * ACC_COLS + hw * 128);
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t v0[32], v1[32];
+                    if (have) {
+                        tmem_ld32(taddr + hh * 64, v0);
+                        tmem_ld32(taddr + hh * 64 + 32, v1);
+                        tmem_ld_wait();
+                    }
+                    if (hh == 1) {   // every TMEM read of this item is done: free the accumulator
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_addr(&acc_empty[b]));
+                    }
+                    if (!have) continue;
 #pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
-                    uint32_t (&v)[32] = blk ? v1 : v0;
-                    const int cb = cb0 + blk * 32;            // column offset in the tile
-                    const int qbase = tile * BT + cb;
-                    uint32_t o = 0;
+                    for (int blk = 0; blk < 2; ++blk) {
+                        uint32_t (&v)[32] = blk ? v1 : v0;
+                        const int cb = hh * 64 + blk * 32;        // column offset in the tile
+                        const int qbase = tile * BT + cb;
+                        uint32_t o = 0;
 #pragma unroll
-                    for (int c = 0; c < 32; c += 2) o |= v[c] | v[c + 1];
-                    if (!__any_sync(FULL, rowvalid && (o >> 31))) continue;
-                    uint32_t mask = 0;
+                        for (int c = 0; c < 32; c += 2) o |= v[c] | v[c + 1];
+                        if (!__any_sync(FULL, rowvalid && (o >> 31))) continue;
+                        // bit c = (w_c < 0), built in four independent 8-bit chains
+                        uint32_t m8[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-                    for (int c = 31; c >= 0; --c) mask = __funnelshift_l(v[c], mask, 1);   // bit c = w < 0
-                    const int nv = n_cols - qbase;
-                    mask &= nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
-                    if (!rowvalid) mask = 0;
-                    if (MODE == SWEEP_COUNT) {
-                        rowadd += __popc(mask);
-                        if (!diag) {   // the diagonal tile is counted from both sides already
-                            const int cc = __popc(warp_transpose32(mask, lane));
-                            if (cc) atomicAdd(a.cnt + qbase + lane, cc);
-                        }
-                    } else {
-                        while (mask) {
-                            const int cq = __ffs(mask) - 1;
-                            mask &= mask - 1;
-                            const int q = qbase + cq;
-                            const int aq = saux[ti * BT + cb + cq];
-                            if (MODE == SWEEP_UNION) {
-                                if (diag && q <= p) continue;
-                                if (aq == acc) continue;
-                                acc = tc_unite(a.parent, acc, aq, ctrl);
-                            } else {
-                                rowmin = min(rowmin, aq);
+                        for (int c = 7; c >= 0; --c)
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) m8[g] = __funnelshift_l(v[8 * g + c], m8[g], 1);
+                        uint32_t mask = m8[0] | (m8[1] << 8) | (m8[2] << 16) | (m8[3] << 24);
+                        const int nv = n_cols - qbase;
+                        mask &= nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
+                        if (!rowvalid) mask = 0;
+                        if (MODE == SWEEP_COUNT) {
+                            const int nh = __popc(mask);
+                            rowadd += nh;
+                            if (!diag) {   // the diagonal tile is counted from both sides already
+                                if (__any_sync(FULL, nh > 2)) {
+                                    // many neighbours: per-column sums through a bit transpose
+                                    const int cc = __popc(warp_transpose32(mask, lane));
+                                    if (cc) atomicAdd(a.cnt + qbase + lane, cc);
+                                } else {
+                                    // few: credit each neighbour's column directly
+                                    while (mask) {
+                                        const int cq = __ffs(mask) - 1;
+                                        mask &= mask - 1;
+                                        atomicAdd(a.cnt + qbase + cq, 1);
+                                    }
+                                }
+                            }
+                        } else {
+                            while (mask) {
+                                const int cq = __ffs(mask) - 1;
+                                mask &= mask - 1;
+                                const int q = qbase + cq;
+                                const int aq = saux[ti * BT + cb + cq];
+                                if (MODE == SWEEP_UNION) {
+                                    if (diag && q <= p) continue;
+                                    if (aq == acc) continue;
+                                    acc = tc_unite(a.parent, acc, aq, ctrl);
+                                } else {
+                                    rowmin = min(rowmin, aq);
+                                }
                             }
                         }
                     }

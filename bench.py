@@ -35,6 +35,8 @@ UNIT = "pair evals/s"
 FP32_LANES_PER_SM = 128          # FP32 FMA lanes per Blackwell SM
 SM_COUNT_FALLBACK = 152
 SM_MAX_MHZ_FALLBACK = 2070.0
+BF16_FALLBACK_TFLOPS = 1900.0    # recipe fallback when no measured peak exists
+TF32_PER_BF16 = 1.1 / 2.25       # nominal dense tf32 / bf16 ratio
 
 
 def parse():
@@ -269,7 +271,8 @@ def run_gb300(args, dist: Dist):
     if st != 0:
         raise RuntimeError(f"device status {binding.dbscan_strerror(st)}")
 
-    # roofline of the dominant kernel (the count sweep)
+    # roofline of the dominant kernel (the count sweep) on the path the data took
+    info = binding.dbscan_workspace_info(ws)
     count_ms = stage_ms["count"] / max(calls, 1)
     peaks = measured_peaks()
     props = torch.cuda.get_device_properties(dev)
@@ -277,14 +280,30 @@ def run_gb300(args, dist: Dist):
     max_mhz = (peaks or {}).get("sm_max_mhz", SM_MAX_MHZ_FALLBACK)
     fp32_peak = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12
     achieved = count_flops(n, d) / (count_ms * 1e-3) / 1e12
-    traffic = recorded_traffic(os.path.join(ROOT, "all_pairs_distance_gb300", "csrc", "sweep.cu"),
-                               w.name)
-    roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
-                "frac": achieved / fp32_peak, "traffic": traffic,
-                "kernel": "count sweep (fp32 FFMA, upper triangle)",
-                "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
-                               f"{max_mhz:.0f} MHz (max SM clock"
-                               + (", MEASURED_PEAKS.json)" if peaks else ", recipe fallback)")}
+    src = "sweep_tc.cu" if info["path"] != "fp32" else "sweep.cu"
+    traffic = recorded_traffic(os.path.join(ROOT, "all_pairs_distance_gb300", "csrc", src), w.name)
+    if info["path"] == "fp32":
+        roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
+                    "frac": achieved / fp32_peak, "traffic": traffic,
+                    "kernel": "count sweep on CUDA cores (fp32 FFMA, upper triangle)",
+                    "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
+                                   f"{max_mhz:.0f} MHz (max SM clock"
+                                   + (", MEASURED_PEAKS.json)" if peaks else ", recipe fallback)")}
+    else:
+        bf16 = (peaks or {}).get("bf16_tflops", BF16_FALLBACK_TFLOPS)
+        peak = bf16 if info["path"] == "bf16" else bf16 * TF32_PER_BF16
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": traffic,
+                    "kernel": f"count sweep on tensor cores (tcgen05 {info['path']}, K={info['kpad']}, "
+                              f"upper triangle)",
+                    "peak_source": ("measured bf16 burst (MEASURED_PEAKS.json)" if peaks else
+                                    "recipe fallback bf16") +
+                                   ("" if info["path"] == "bf16" else
+                                    f" x {TF32_PER_BF16:.3f} (nominal tf32/bf16 ratio 1.1/2.25)"),
+                    "fp32_equivalent": {"achieved": achieved, "peak": fp32_peak,
+                                        "frac": achieved / fp32_peak,
+                                        "note": "same algorithmic FLOP (2d per unordered pair) "
+                                                "against the derived FP32 CUDA-core peak"}}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
@@ -295,6 +314,8 @@ def run_gb300(args, dist: Dist):
                        "input_dtype": w.dtype, "l2": "flushed between steps (256 MiB write, untimed)",
                        "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU"},
             "stages_ms": {k: v / max(calls, 1) for k, v in stage_ms.items()},
+            "path": info["path"], "n_core": info["n_core"], "n_cand": info["n_cand"],
+            "exact": info["exact"],
             "count_pair_evals_per_s": float(n) * n / (count_ms * 1e-3),
             "roofline": roofline, "gpu_launches": launches, "clocks": clk}
 

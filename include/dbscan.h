@@ -171,6 +171,22 @@ size_t dbscan_workspace_size(int64_t n, int32_t d, int32_t dtype);
 int dbscan_workspace_status(const void *workspace, void *stream);
 
 /*
+ * Facts about the last call that used `workspace` (synchronises `stream`
+ * first).  Fills up to n of, in this order:
+ *   0  arithmetic path of the sweeps: 0 CUDA-core fp32, 1 tf32 tensor cores,
+ *      2 bf16 tensor cores
+ *   1  number of core points
+ *   2  number of border candidates (non-core points with a neighbour
+ *      besides themselves)
+ *   3  1 when every coordinate was an integer and sum_k (max_k - min_k)^2 <
+ *      2^24, i.e. the results are exact (see "Exactness" above), else 0
+ *   4  padded operand width K of the tensor-core path (0 on CUDA cores)
+ * info is a host pointer to n int64 values.  Returns DBSCAN_OK,
+ * DBSCAN_ERR_INVALID_ARG for a NULL pointer or n < 1, or DBSCAN_ERR_CUDA.
+ */
+int dbscan_workspace_info(const void *workspace, void *stream, int64_t *info, int32_t n);
+
+/*
  * Stage timing (measurement support, not part of the computation).
  * Between dbscan_profile_begin() and dbscan_profile_end(), every call made
  * on the same host thread records CUDA events on its own stream around its

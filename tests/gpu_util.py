@@ -7,13 +7,16 @@ import oracle
 from all_pairs_distance_gb300 import binding
 
 
-def gpu_run(P, eps, min_pts, dtype=torch.float32, counts=True):
-    """(cnt, core, label) from the CUDA library for host array P."""
+def gpu_run(P, eps, min_pts, dtype=torch.float32, counts=True, info=None):
+    """(cnt, core, label) from the CUDA library for host array P.  When
+    ``info`` is a dict it receives dbscan_workspace_info of the fit."""
     x = torch.from_numpy(np.ascontiguousarray(P)).to("cuda").to(dtype)
     ws = binding.workspace_for(x)
     labels, core = binding.dbscan_fit_ex(x, eps, min_pts, workspace=ws)
     st = binding.dbscan_workspace_status(ws)
     assert st == 0, binding.dbscan_strerror(st)
+    if info is not None:
+        info.update(binding.dbscan_workspace_info(ws))
     cnt = None
     if counts:
         cnt = binding.dbscan_neighbor_counts(x, eps, workspace=ws)

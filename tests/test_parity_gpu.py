@@ -194,13 +194,19 @@ def test_device_side_errors_and_bad_pointers():
 
 
 PATH_CASES = {
-    "c4_like_12k_d3": (lambda: synth.scaled("blobs_1m_d3", 12_007, seed=31), 10.0, 8, torch.float32),
-    "c2_like_9k_d2": (lambda: synth.scaled("blobs_100k_d2", 9_001, seed=32), 20.0, 10, torch.float32),
-    "c3_like_3k_d16": (lambda: synth.scaled("blobs_200k_d16", 3_001, seed=33), 120.0, 20, torch.float32),
-    "c5_like_3k_d64": (lambda: synth.scaled("blobs_500k_d64", 2_999, seed=34), 100.0, 16, torch.bfloat16),
-    "small_box_d3": (lambda: synth.uniform_ints(4_000, 3, 200, 35), 9.0, 6, torch.float32),
-    "corners_d3": (lambda: (np.random.default_rng(36).integers(0, 2, size=(700, 3)) * 2047).astype(np.float32),
-                   2047.0, 5, torch.float32),
+    # name: (points, eps, min_pts, dtype, tensor-core paths the data qualifies for)
+    "c4_like_12k_d3": (lambda: synth.scaled("blobs_1m_d3", 12_007, seed=31), 10.0, 8, torch.float32,
+                       {"tf32"}),
+    "c2_like_9k_d2": (lambda: synth.scaled("blobs_100k_d2", 9_001, seed=32), 20.0, 10, torch.float32,
+                      {"tf32"}),
+    "c3_like_3k_d16": (lambda: synth.scaled("blobs_200k_d16", 3_001, seed=33), 120.0, 20,
+                       torch.float32, {"tf32"}),
+    "c5_like_3k_d64": (lambda: synth.scaled("blobs_500k_d64", 2_999, seed=34), 100.0, 16,
+                       torch.bfloat16, {"bf16"}),
+    "small_box_d3": (lambda: synth.uniform_ints(4_000, 3, 200, 35), 9.0, 6, torch.float32,
+                     {"tf32", "bf16"}),
+    "corners_d3": (lambda: (np.random.default_rng(36).integers(0, 2, size=(700, 3)) * 2047)
+                   .astype(np.float32), 2047.0, 5, torch.float32, {"tf32"}),
 }
 
 
@@ -210,9 +216,25 @@ def test_parity_every_path(name, path, monkeypatch):
     # the library picks a path per call from the data; forcing one narrows the
     # choice (a path the data cannot use exactly falls back to CUDA cores)
     monkeypatch.setenv("DBSCAN_FORCE_PATH", path)
-    make, eps, min_pts, dtype = PATH_CASES[name]
+    make, eps, min_pts, dtype, eligible = PATH_CASES[name]
     P = make()
     ref = oracle.dbscan(P, eps, min_pts)
-    got = gpu_run(P, eps, min_pts, dtype)
+    info = {}
+    got = gpu_run(P, eps, min_pts, dtype, info=info)
+    assert info["path"] == (path if path in eligible else "fp32")
+    assert info["exact"]
+    assert info["n_core"] == int(ref[1].sum())
     for g, e, w in zip(got, ref, ("cnt", "core", "label")):
         assert_same(g, e, f"{name} [{path}] {w}")
+
+
+def test_default_path_choice():
+    # without forcing, integer data in a 2048-wide box goes to tf32 tensor
+    # cores, a 256-wide box to bf16, and a wider box stays on CUDA cores
+    for P, expect in ((synth.uniform_ints(3000, 3, 2047, 1), "tf32"),
+                      (synth.uniform_ints(3000, 3, 255, 2), "bf16"),
+                      (synth.uniform_ints(3000, 2, 3000, 3), "fp32"),
+                      (synth.uniform_ints(3000, 2, 100, 4) + np.float32(0.5), "fp32")):
+        info = {}
+        gpu_run(P, 4.0, 3, info=info, counts=False)
+        assert info["path"] == expect, (expect, info)
