@@ -63,6 +63,15 @@ Layout make_layout(int64_t n, int32_t d) {
     L.off_ua_core = off;     off += align256(umma);
     L.off_ub_core = off;     off += align256(umma);
     L.off_ua_cand = off;     off += align256(umma);
+    // locality order
+    L.order_bits = order_bits(n);
+    const size_t nbins = (size_t)1 << L.order_bits;
+    L.off_bin = off;         off += align256((size_t)n * sizeof(int));
+    L.off_perm = off;        off += align256(per_pt);
+    L.off_hist = off;        off += align256(nbins * sizeof(int));
+    L.off_bstart = off;      off += align256(nbins * sizeof(int));
+    L.off_btot = off;        off += align256((nbins / 1024 + 1) * sizeof(int));
+    L.off_rootmin = off;     off += align256(per_pt);
     L.total = off;
     return L;
 }
@@ -106,6 +115,12 @@ Work carve(void *base, const Layout &L) {
     w.ua_core = reinterpret_cast<uint8_t *>(b + L.off_ua_core);
     w.ub_core = reinterpret_cast<uint8_t *>(b + L.off_ub_core);
     w.ua_cand = reinterpret_cast<uint8_t *>(b + L.off_ua_cand);
+    w.bin = reinterpret_cast<int *>(b + L.off_bin);
+    w.perm = reinterpret_cast<int *>(b + L.off_perm);
+    w.hist = reinterpret_cast<int *>(b + L.off_hist);
+    w.bstart = reinterpret_cast<int *>(b + L.off_bstart);
+    w.btot = reinterpret_cast<int *>(b + L.off_btot);
+    w.rootmin = reinterpret_cast<int *>(b + L.off_rootmin);
     return w;
 }
 
@@ -160,19 +175,20 @@ static void keep_pool(void) {
 // Kernels each stage launches for dimension d.  Every sweep launches its
 // CUDA-core kernel and one kernel per tensor-core path the shape allows
 // (ntc); all but the path chosen on the device return at once.
-//   prep 4 (+1 operand staging), count 1 + ntc, compact 4 (+2 operand
-//   stagings), union 4 waves x (1 + ntc) + 3 compressions, flatten 1,
-//   border 1 + ntc, finalize 1.
+//   prep 4 + 5 locality order (+1 operand staging), count 1 + ntc,
+//   compact 4 (+2 operand stagings), union 1 tile-local + 4 waves x
+//   (1 + ntc) + 3 compressions, flatten 2, border 1 + ntc, finalize 1.
 static int stage_launches(int d, int stage) {
     int ntc = 0;
     for (int kind = TC_TF32; kind <= TC_BF16; ++kind)
         if (tc_kbytes(kind, d, 3) <= TC_MAX_KBYTES) ++ntc;
     const int umma = ntc > 0 ? 1 : 0;
     switch (stage) {
-    case 0: return 4 + umma;
+    case 0: return 9 + umma;
     case 1: return 1 + ntc;
     case 2: return 4 + 2 * umma;
-    case 3: return 4 * (1 + ntc) + 3;
+    case 3: return 1 + 4 * (1 + ntc) + 3;
+    case 4: return 2;
     case 5: return 1 + ntc;
     default: return 1;
     }
@@ -234,9 +250,7 @@ static int run(const void *points, int dtype, int64_t n, int d, float eps, int m
     if (launch_count(w, L, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     marks.mark(s);
     if (cnt_out) {
-        if (cudaMemcpyAsync(cnt_out, w.cnt, (size_t)n * sizeof(int), cudaMemcpyDeviceToDevice, s) !=
-            cudaSuccess)
-            return DBSCAN_ERR_CUDA;
+        if (launch_unpermute_counts(w, L, cnt_out, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
         return DBSCAN_OK;
     }
     if (launch_compact(w, L, min_pts, labels, is_core, s) != cudaSuccess) return DBSCAN_ERR_CUDA;

@@ -5,11 +5,12 @@
 // CUDA", §II (a point is core when at least MinPts points lie within eps of
 // it).  The page's primitive-cluster construction (§IV-B, a cluster matrix
 // with a valid flag per column) and its merge kernel (§IV-C) need O(N^2)
-// memory; here the core points are compacted (ascending index order, so a
-// position order equals the original index order), merged by union-find in
-// the core-core sweep, and flattened to the smallest original index of each
-// component.  Non-core points with at least one neighbour besides themselves
-// are the border candidates scanned by the border sweep; the rest are noise.
+// memory; here the core points are compacted (stable, in the staged locality
+// order), merged by union-find in the core-core sweep, and each component is
+// named by the smallest input index among its core points.  Non-core points
+// with at least one neighbour besides themselves are the border candidates
+// scanned by the border sweep; the rest are noise.  Every array indexed by
+// position p maps to the caller's numbering through perm[p].
 #include "dbscan_internal.cuh"
 
 namespace dbscan {
@@ -18,8 +19,8 @@ constexpr int CT_THREADS = 256;
 constexpr int PER_THREAD = SCAN_BLOCK / CT_THREADS;  // 4
 
 // Pass A: flags, is_core output, initial labels, per-block counts.
-__global__ void k_flags(const int *cnt, int64_t n, int min_pts, uint8_t *is_core,
-                        int32_t *labels, int *bsum, int64_t nblocks) {
+__global__ void k_flags(const int *cnt, const int *perm, int64_t n, int min_pts,
+                        uint8_t *is_core, int32_t *labels, int *bsum, int64_t nblocks) {
     __shared__ int s_core, s_cand;
     if (threadIdx.x == 0) { s_core = 0; s_cand = 0; }
     __syncthreads();
@@ -31,8 +32,9 @@ __global__ void k_flags(const int *cnt, int64_t n, int min_pts, uint8_t *is_core
         int c = cnt[i];
         bool core = c >= min_pts;
         bool cand = !core && c >= 2;
-        is_core[i] = core ? 1 : 0;
-        labels[i] = cand ? 0x7fffffff : -1;
+        const int src = perm[i];
+        is_core[src] = core ? 1 : 0;
+        labels[src] = cand ? 0x7fffffff : -1;
         ncore += core;
         ncand += cand;
     }
@@ -99,10 +101,11 @@ __device__ __forceinline__ void copy_staged(const float *src_tiles, float *dst_t
 
 // Pass C: stable scatter of core points and candidates with their staged
 // coordinates and thresholds; parent[pos] = pos.
-__global__ void k_scatter(const int *cnt, int64_t n, int d, int min_pts, const int *bsum,
-                          int64_t nblocks, const float *staged_all, const float *T_all,
-                          float *staged_core, float *T_core, int *cidx, int *parent,
-                          float *staged_cand, float *T_cand, int *candidx) {
+__global__ void k_scatter(const int *cnt, const int *perm, int64_t n, int d, int min_pts,
+                          const int *bsum, int64_t nblocks, const float *staged_all,
+                          const float *T_all, float *staged_core, float *T_core, int *cidx,
+                          int *parent, int *rootmin, float *staged_cand, float *T_cand,
+                          int *candidx) {
     __shared__ int wsum[2][CT_THREADS / 32];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     int off_core = bsum[blockIdx.x];
@@ -130,12 +133,13 @@ __global__ void k_scatter(const int *cnt, int64_t n, int d, int min_pts, const i
         pc += __popc(bc & below);
         pd += __popc(bd & below);
         if (core) {
-            cidx[pc] = (int)i;
+            cidx[pc] = perm[i];
             parent[pc] = pc;
+            rootmin[pc] = 0x7fffffff;
             copy_staged(staged_all, staged_core, d, i, pc);
             T_core[pc] = T_all[i];
         } else if (cand) {
-            candidx[pd] = (int)i;
+            candidx[pd] = perm[i];
             copy_staged(staged_all, staged_cand, d, i, pd);
             T_cand[pd] = T_all[i];
         }
@@ -164,9 +168,9 @@ __global__ void k_pad_tails(const Ctrl *ctrl, int d, float *staged_core, float *
 }
 
 // Flatten: every core position to its root (the smallest position of its
-// component), label = original index of that root.
-__global__ void k_flatten(Ctrl *ctrl, int *parent, const int *cidx, int *clabel,
-                          int32_t *labels) {
+// component); the root collects the smallest input index of its component.
+__global__ void k_flatten(Ctrl *ctrl, const int *parent, const int *cidx, int *clabel,
+                          int *rootmin) {
     const int n_core = ctrl->n_core;
     for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < n_core; p += gridDim.x * blockDim.x) {
         int x = p;
@@ -177,7 +181,17 @@ __global__ void k_flatten(Ctrl *ctrl, int *parent, const int *cidx, int *clabel,
             x = q;
         }
         if (it == (1 << 22)) set_error(ctrl, DBSCAN_ERR_INTERNAL);
-        const int lab = cidx[x];
+        clabel[p] = x;
+        atomicMin(rootmin + x, cidx[p]);
+    }
+}
+
+// Label of every core point: its component's smallest input index.
+__global__ void k_core_labels(const Ctrl *ctrl, const int *cidx, const int *rootmin,
+                              int *clabel, int32_t *labels) {
+    const int n_core = ctrl->n_core;
+    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < n_core; p += gridDim.x * blockDim.x) {
+        const int lab = rootmin[clabel[p]];
         clabel[p] = lab;
         labels[cidx[p]] = lab;
     }
@@ -203,12 +217,13 @@ static int grid_for(int64_t n, int threads, const void *kernel) {
 cudaError_t launch_compact(const Work &w, const Layout &L, int min_pts, int32_t *labels,
                            uint8_t *is_core, cudaStream_t s) {
     const int64_t nb = L.nscan_blocks;
-    k_flags<<<(unsigned)nb, CT_THREADS, 0, s>>>(w.cnt, L.n, min_pts, is_core, labels, w.bsum, nb);
+    k_flags<<<(unsigned)nb, CT_THREADS, 0, s>>>(w.cnt, w.perm, L.n, min_pts, is_core, labels,
+                                                w.bsum, nb);
     k_scan_blocks<<<1, 1024, 0, s>>>(w.bsum, nb, w.ctrl);
-    k_scatter<<<(unsigned)nb, CT_THREADS, 0, s>>>(w.cnt, L.n, L.d, min_pts, w.bsum, nb,
+    k_scatter<<<(unsigned)nb, CT_THREADS, 0, s>>>(w.cnt, w.perm, L.n, L.d, min_pts, w.bsum, nb,
                                                   w.staged_all, w.T_all, w.staged_core, w.T_core,
-                                                  w.cidx, w.parent, w.staged_cand, w.T_cand,
-                                                  w.candidx);
+                                                  w.cidx, w.parent, w.rootmin, w.staged_cand,
+                                                  w.T_cand, w.candidx);
     k_pad_tails<<<1, 128, 0, s>>>(w.ctrl, L.d, w.staged_core, w.T_core, w.staged_cand, w.T_cand);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -218,7 +233,9 @@ cudaError_t launch_compact(const Work &w, const Layout &L, int min_pts, int32_t 
 
 cudaError_t launch_flatten(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s) {
     k_flatten<<<grid_for(L.n, 256, (const void *)k_flatten), 256, 0, s>>>(w.ctrl, w.parent, w.cidx,
-                                                                          w.clabel, labels);
+                                                                          w.clabel, w.rootmin);
+    k_core_labels<<<grid_for(L.n, 256, (const void *)k_core_labels), 256, 0, s>>>(
+        w.ctrl, w.cidx, w.rootmin, w.clabel, labels);
     return cudaGetLastError();
 }
 

@@ -39,7 +39,9 @@ struct Ctrl {
     int tc_kpad;        // padded K of the tensor-core operands (elements)
     int tc_kbytes;      // bytes of one operand row (tc_kpad * element size)
     int tc_nt;          // digits of the threshold constant in the operands
-    int pad1[43];
+    float ord_lo[3];    // locality order: lower bound of each key axis
+    float ord_scale[3]; // locality order: quantisation scale of each key axis
+    int pad1[37];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl must be 256 bytes");
 
@@ -54,6 +56,8 @@ struct Layout {
     size_t off_cnt, off_cidx, off_candidx, off_parent, off_clabel, off_bsum;
     size_t umma_tile_bytes;   // bytes of one 128-point operand tile (largest path), 0 = none
     size_t off_ua_all, off_ub_all, off_ua_core, off_ub_core, off_ua_cand;
+    int order_bits;       // bins of the locality order: 2^order_bits
+    size_t off_bin, off_perm, off_hist, off_bstart, off_btot, off_rootmin;
     int64_t nscan_blocks;
     size_t total;
 };
@@ -69,12 +73,17 @@ struct Work {
     float *staged_all, *staged_core, *staged_cand;
     float *T_all, *T_core, *T_cand;
     int *cnt;             // [n] neighbour counts
-    int *cidx;            // [n] original index of each core point, ascending
-    int *candidx;         // [n] original index of each border candidate, ascending
+    int *cidx;            // [n] input index of each core position (staged order)
+    int *candidx;         // [n] input index of each border-candidate position
     int *parent;          // [n] union-find parents over core positions
-    int *clabel;          // [n] final label of each core position
+    int *clabel;          // [n] root, then final label, of each core position
     int *bsum;            // [2 * nscan_blocks] per-block counts of the compaction scan
     uint8_t *ua_all, *ub_all, *ua_core, *ub_core, *ua_cand;   // tensor-core operand tiles
+    int *bin;             // [n] locality bin of each input point
+    int *perm;            // [ntiles * BT] input index of each staged position
+    int *hist, *bstart;   // [2^order_bits] bin counts and bin starts
+    int *btot;            // [2^order_bits / 1024] bin-block offsets
+    int *rootmin;         // [n] smallest input index of each union-find root's component
 };
 
 Work carve(void *base, const Layout &L);
@@ -110,6 +119,11 @@ __host__ __device__ inline size_t umma_offset(int row, int kbyte, int kbytes) {
 }
 
 // ---- host launch wrappers (each returns cudaGetLastError()) ---------------
+int order_bits(int64_t n);
+cudaError_t launch_order(const void *points, int dtype, int64_t n, int d, const Work &w,
+                         const Layout &L, cudaStream_t s);
+cudaError_t launch_unpermute_counts(const Work &w, const Layout &L, int32_t *cnt_out,
+                                    cudaStream_t s);
 cudaError_t launch_prep(const void *points, int dtype, int64_t n, int d, float eps, int allow_tc,
                         const Work &w, const Layout &L, cudaStream_t s);
 cudaError_t launch_stage_umma(const Work &w, const Layout &L, int which, cudaStream_t s);
@@ -131,6 +145,13 @@ int persistent_ctas(const void *kernel, int threads, size_t smem);
 // ---- device helpers --------------------------------------------------------
 __device__ __forceinline__ void set_error(Ctrl *c, int code) {
     atomicCAS(&c->err, 0, code);
+}
+
+// Element e of the caller's row-major point array.
+__device__ __forceinline__ float load_point(const void *p, int dtype, size_t e) {
+    if (dtype == DBSCAN_BF16)
+        return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[e]);
+    return reinterpret_cast<const float *>(p)[e];
 }
 
 // Monotone map float -> int so that integer min/max order equals float order.

@@ -34,12 +34,6 @@
 
 namespace dbscan {
 
-__device__ __forceinline__ float load_point(const void *p, int dtype, size_t e) {
-    if (dtype == DBSCAN_BF16)
-        return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[e]);
-    return reinterpret_cast<const float *>(p)[e];
-}
-
 __global__ void k_init_stats(Ctrl *ctrl, int *smin, int *smax, int64_t n, int d) {
     for (int k = threadIdx.x; k < DBSCAN_MAX_D; k += blockDim.x) {
         smin[k] = 0x7fffffff;
@@ -232,10 +226,11 @@ cudaError_t launch_stage_umma(const Work &w, const Layout &L, int which, cudaStr
     return cudaGetLastError();
 }
 
-// One thread per (padded) point: centred coordinates and norm into the
-// tiled layout, row threshold into T.
+// One thread per (padded) position p: the centred coordinates and norm of
+// input point perm[p] into the tiled layout, its row threshold into T[p].
 __global__ void k_stage(const void *pts, int dtype, int64_t n, int d, const Ctrl *ctrl,
-                        const float *centre, float *staged, float *T, int64_t npad) {
+                        const float *centre, const int *perm, float *staged, float *T,
+                        int64_t npad) {
     extern __shared__ float s_centre[];
     for (int k = threadIdx.x; k < d; k += blockDim.x) s_centre[k] = centre[k];
     __syncthreads();
@@ -250,9 +245,10 @@ __global__ void k_stage(const void *pts, int dtype, int64_t n, int d, const Ctrl
         T[i] = PAD_THRESH;
         return;
     }
+    const int64_t src = perm[i];
     float nrm = 0.f;
     for (int k = 0; k < d; ++k) {
-        float c = load_point(pts, dtype, (size_t)i * d + k) - s_centre[k];
+        float c = load_point(pts, dtype, (size_t)src * d + k) - s_centre[k];
         base[(size_t)k * BT] = c;
         nrm = fmaf(c, c, nrm);
     }
@@ -277,11 +273,13 @@ cudaError_t launch_prep(const void *points, int dtype, int64_t n, int d, float e
     k_stats<<<blocks, 256, 0, s>>>(points, dtype, n, d, w.ctrl, w.stat_min, w.stat_max);
     k_setup<<<1, 256, 0, s>>>(w.ctrl, w.stat_min, w.stat_max, w.centre, d, eps2,
                               L.umma_tile_bytes ? allow_tc : 0);
+    cudaError_t e = launch_order(points, dtype, n, d, w, L, s);
+    if (e != cudaSuccess) return e;
     const int64_t npad = L.ntiles * BT;
     int sblocks = (int)((npad + 255) / 256);
     k_stage<<<sblocks, 256, d * sizeof(float), s>>>(points, dtype, n, d, w.ctrl, w.centre,
-                                                     w.staged_all, w.T_all, npad);
-    cudaError_t e = cudaGetLastError();
+                                                     w.perm, w.staged_all, w.T_all, npad);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_stage_umma(w, L, 0, s);
 }

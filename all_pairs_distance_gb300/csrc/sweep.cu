@@ -444,6 +444,60 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
     }
 }
 
+// ---- tile-local union before the core-core sweep -------------------------------
+// With the points in locality order most core-core neighbour pairs fall inside
+// a diagonal tile.  One CTA per core tile joins the tile's own neighbour pairs
+// in a shared-memory union-find and points every position at the smallest
+// position of its tile-local component, so that the sweep's staged parent
+// snapshots already carry those roots and the sweep skips such pairs without
+// touching global memory.  Same hit test as the sweep (v_ij < T_i).
+__device__ __forceinline__ int sm_find(volatile int *sp, int x) {
+    for (int it = 0; it < BT && sp[x] != x; ++it) x = sp[x];
+    return x;
+}
+
+__global__ void k_local_union(const Ctrl *ctrl, const float *staged, const float *T, int d,
+                              int *parent) {
+    extern __shared__ float s_pts[];   // (d + 1) * BT staged floats, then BT parents
+    volatile int *sp = reinterpret_cast<volatile int *>(s_pts + (size_t)(d + 1) * BT);
+    const int n_core = ctrl->n_core;
+    const int ntiles = (n_core + BT - 1) / BT;
+    const int i = threadIdx.x;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const int base = t * BT;
+        const int nv = min(BT, n_core - base);
+        __syncthreads();
+        const float *src = staged + (size_t)t * (size_t)(d + 1) * BT;
+        for (int e = i; e < (d + 1) * BT; e += BT) s_pts[e] = src[e];
+        sp[i] = i;
+        __syncthreads();
+        if (i < nv) {
+            const float Ti = T[base + i];
+            // pairs (i, i + sh mod BT), sh = 1..63, and sh = 64 for i < 64: every
+            // unordered pair of the tile once, 63 or 64 per thread
+            const int shmax = i < BT / 2 ? BT / 2 : BT / 2 - 1;
+            for (int sh = 1; sh <= shmax; ++sh) {
+                const int j = (i + sh) & (BT - 1);
+                if (j >= nv) continue;
+                float v = s_pts[(size_t)d * BT + j];
+                for (int k = 0; k < d; ++k)
+                    v = fmaf(-2.f * s_pts[(size_t)k * BT + i], s_pts[(size_t)k * BT + j], v);
+                if (!(v < Ti)) continue;
+                int ra = i, rb = j;
+                for (int it = 0; it < 2 * BT; ++it) {
+                    ra = sm_find(sp, ra);
+                    rb = sm_find(sp, rb);
+                    if (ra == rb) break;
+                    if (ra < rb) { const int tmp = ra; ra = rb; rb = tmp; }
+                    if (atomicCAS((int *)&sp[ra], ra, rb) == ra) break;
+                }
+            }
+        }
+        __syncthreads();
+        if (i < nv) parent[base + i] = base + sm_find(sp, i);
+    }
+}
+
 // Point every core position straight at its root (between union waves).
 __global__ void k_compress(Ctrl *ctrl, int *parent) {
     const int n_core = ctrl->n_core;
@@ -530,6 +584,18 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
     a.cols = w.staged_core; a.n_cols = &w.ctrl->n_core; a.aux = w.parent;
     a.tri = 1; a.ctrl = w.ctrl; a.parent = w.parent;
     const int grid = persistent_ctas((const void *)k_compress, 256, 0);
+    const size_t lsmem = (size_t)(L.d + 1) * BT * sizeof(float) + BT * sizeof(int);
+    if (cudaFuncSetAttribute((const void *)k_local_union,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lsmem) != cudaSuccess)
+        return cudaGetLastError();
+    int dev = 0, sms = 1, per = 1;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, (const void *)k_local_union, BT, lsmem);
+    int64_t lgrid = (int64_t)sms * (per < 1 ? 1 : per);
+    if (lgrid > L.ntiles) lgrid = L.ntiles;
+    if (lgrid < 1) lgrid = 1;
+    k_local_union<<<(unsigned)lgrid, BT, lsmem, s>>>(w.ctrl, w.staged_core, w.T_core, L.d, w.parent);
     for (int wv = 0; wv < UNION_WAVES; ++wv) {
         a.ulo = kUnionWaveEdges[wv];
         a.uhi = kUnionWaveEdges[wv + 1];

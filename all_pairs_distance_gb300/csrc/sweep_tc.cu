@@ -445,6 +445,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         const int grp = warp >> 3, w8 = warp & 7, wq = w8 & 3, hw = w8 >> 2;
         const int row = wq * 32 + lane;
         int last_rb = -1, acc = -1;             // UNION: a known ancestor of this row's point
+        int lastq = -1;                         // UNION: last staged parent joined to this row
         int k = 0, it = 0;
         for (;;) {
             const int s = k % S;
@@ -457,6 +458,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             if (MODE == SWEEP_UNION && m.rb != last_rb) {
                 acc = rowvalid ? tc_find(a.parent, p, ctrl) : -1;
                 last_rb = m.rb;
+                lastq = -1;
             }
             const int *saux = reinterpret_cast<const int *>(sStage + (size_t)s * a.stage_bytes +
                                                             (size_t)G * a.tile_bytes_max);
@@ -531,7 +533,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                                 const int aq = saux[ti * BT + cb + cq];
                                 if (MODE == SWEEP_UNION) {
                                     if (diag && q <= p) continue;
-                                    if (aq == acc) continue;
+                                    if (aq == acc || aq == lastq) continue;
+                                    lastq = aq;   // aq joins this row's set for good
                                     acc = tc_unite(a.parent, acc, aq, ctrl);
                                 } else {
                                     rowmin = min(rowmin, aq);
