@@ -76,12 +76,13 @@ Layout make_layout(int64_t n, int32_t d) {
     return L;
 }
 
-// Tensor-core paths this shape may use, narrowed by DBSCAN_FORCE_PATH
-// ("fp32", "tf32" or "bf16") when it is set.
-static int allowed_tc(int d) {
+// Tensor-core paths this call may use (operand rows within TC_MAX_KBYTES for
+// the threshold digits eps allows), narrowed by DBSCAN_FORCE_PATH ("fp32",
+// "tf32" or "bf16") when it is set.
+static int allowed_tc(int d, float eps2) {
     int allow = 0;
-    if (tc_kbytes(TC_TF32, d, 3) <= TC_MAX_KBYTES) allow |= TC_ALLOW_TF32;
-    if (tc_kbytes(TC_BF16, d, 3) <= TC_MAX_KBYTES) allow |= TC_ALLOW_BF16;
+    if (tc_kbytes(TC_TF32, d, tc_nt_bound(TC_TF32, eps2)) <= TC_MAX_KBYTES) allow |= TC_ALLOW_TF32;
+    if (tc_kbytes(TC_BF16, d, tc_nt_bound(TC_BF16, eps2)) <= TC_MAX_KBYTES) allow |= TC_ALLOW_BF16;
     const char *f = getenv("DBSCAN_FORCE_PATH");
     if (f && *f) {
         if (!strcmp(f, "fp32")) allow = 0;
@@ -244,7 +245,7 @@ static int run(const void *points, int dtype, int64_t n, int d, float eps, int m
     StageMarks marks(s, d);
     if (cudaMemsetAsync(w.ctrl, 0, sizeof(Ctrl), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     if (cudaMemsetAsync(w.cnt, 0, (size_t)n * sizeof(int), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
-    if (launch_prep(points, dtype, n, d, eps, allowed_tc(d), w, L, s) != cudaSuccess)
+    if (launch_prep(points, dtype, n, d, eps, allowed_tc(d, L.eps2), w, L, s) != cudaSuccess)
         return DBSCAN_ERR_CUDA;
     marks.mark(s);
     if (launch_count(w, L, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
@@ -285,7 +286,8 @@ static int fit_common(const void *points, int32_t dtype, int64_t n, int32_t d, f
     if (n == 0) return DBSCAN_OK;
     if (!points) return DBSCAN_ERR_INVALID_ARG;
     if (!cnt_out && (!labels || !is_core)) return DBSCAN_ERR_INVALID_ARG;
-    const Layout L = make_layout(n, d);
+    Layout L = make_layout(n, d);
+    L.eps2 = eps * eps;
     if (workspace) {
         if (workspace_bytes < L.total) return DBSCAN_ERR_INVALID_ARG;
         if (reinterpret_cast<uintptr_t>(workspace) & 255) return DBSCAN_ERR_INVALID_ARG;
@@ -418,7 +420,8 @@ int dbscan_fit_host(const void *points_host, int32_t dtype, int64_t n, int32_t d
     if (n == 0) return DBSCAN_OK;
     if (!points_host || !labels_host || !is_core_host) return DBSCAN_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const Layout L = make_layout(n, d);
+    Layout L = make_layout(n, d);
+    L.eps2 = eps * eps;
     const size_t esz = dtype == DBSCAN_BF16 ? 2 : 4;
     const size_t pbytes = align256((size_t)n * d * esz);
     const size_t lbytes = align256((size_t)n * sizeof(int32_t));

@@ -49,6 +49,7 @@ static_assert(sizeof(Ctrl) == 256, "Ctrl must be 256 bytes");
 struct Layout {
     int64_t n;
     int32_t d;
+    float eps2;           // fl32(eps * eps) of the call (0 in a bare size query)
     int64_t ntiles;       // ceil(n / BT)
     size_t tile_floats;   // (d + 1) * BT
     size_t off_ctrl, off_stats, off_staged_all, off_staged_core, off_staged_cand;
@@ -109,6 +110,18 @@ __host__ __device__ inline int tc_kpad(int kind, int d, int nt) {
 }
 __host__ __device__ inline int tc_kbytes(int kind, int d, int nt) {
     return tc_kpad(kind, d, nt) * (kind == TC_TF32 ? 4 : 2);
+}
+// Digits of the threshold constant thrx (<= floor(eps2) + 1, see prep.cu)
+// in the operands of a path: the host sizes the sweep's shared-memory tiles
+// with this bound, the device takes the digits of the actual thrx.
+__host__ __device__ inline int tc_nt_for(int kind, double thrx) {
+    if (kind == TC_TF32) return thrx < 2048.0 ? 1 : (thrx < 4194304.0 ? 2 : 3);
+    return thrx < 256.0 ? 1 : (thrx < 65536.0 ? 2 : 3);
+}
+inline int tc_nt_bound(int kind, float eps2) {
+    double t = (double)eps2;
+    t = t < 16777216.0 ? (double)(long long)t : t;   // floor for the values that matter
+    return tc_nt_for(kind, t + 1.0);
 }
 // Byte offset of (row, byte k) in a 128-row K-major operand tile without
 // swizzle: 8-row x 16-byte core matrices, K-adjacent ones 128 B apart,

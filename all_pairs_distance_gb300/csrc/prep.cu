@@ -120,10 +120,10 @@ __global__ void k_setup(Ctrl *ctrl, const int *smin, const int *smax, float *cen
         ctrl->exact = (integral && R < 16777215.0) ? 1 : 0;
         // tensor-core eligibility (integer data, exact elements, exact sums)
         const double thrx = (double)ctrl->thrx;
-        const int nt = thrx < 2048.0 ? 1 : (thrx < 4194304.0 ? 2 : 3);
+        const int nt = tc_nt_for(TC_TF32, thrx);
         int kind = TC_NONE;
         if (integral && !ctrl->nonfinite && 4.0 * S < 16777216.0 && 2.0 * S + thrx < 16777216.0) {
-            const int ntb = thrx < 256.0 ? 1 : (thrx < 65536.0 ? 2 : 3);
+            const int ntb = tc_nt_for(TC_BF16, thrx);
             if ((allow & TC_ALLOW_BF16) && rmax <= 256.0 &&
                 tc_kbytes(TC_BF16, d, ntb) <= TC_MAX_KBYTES) {
                 kind = TC_BF16;

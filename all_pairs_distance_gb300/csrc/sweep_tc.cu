@@ -10,19 +10,20 @@
 //
 // CTA = 18 warps, one per SM (the CTA owns all 512 TMEM columns):
 //   warp 16     producer: pulls work units and bulk-copies (cp.async.bulk) the
-//               row operand tile of a unit and groups of up to 8 consecutive
+//               row operand tile of a unit and groups of up to 32 consecutive
 //               column tiles (plus their aux ints) into a ring of shared-memory
 //               stages; lanes take turns issuing, since the bulk copies of one
 //               thread complete one after another;
 //   warp 17     MMA: one thread issues a 128 x 256 x K MMA per pair of column
 //               tiles into one of two 256-column TMEM accumulators and commits
 //               completion to mbarriers;
-//   warps 0-15  epilogue: two groups of 8 warps take alternate tile pairs
-//               (one accumulator each), so one group's TMEM loads overlap the
-//               other's arithmetic.  A warp reads its 32 rows x 128 columns
-//               (tcgen05.ld, 64 at a time), ORs the sign bits of each 32 x 32
-//               block and, only where a block holds a neighbour, builds exact
-//               per-row bit masks.  Counting credits the row with a popcount
+//   warps 0-15  epilogue: every warp reads every tile pair, 32 rows x 64
+//               columns (two tcgen05.ld), and frees the accumulator before it
+//               tests anything -- the accumulator round trip is bound by how
+//               fast TMEM is drained, and TMEM read bandwidth grows with the
+//               number of warps loading.  A warp ORs the sign bits of its 64
+//               columns and, only where a 32 x 32 block holds a neighbour,
+//               builds exact per-row bit masks.  Counting credits the row with a popcount
 //               and the columns by atomics (few neighbours) or a warp bit
 //               transpose (many); union and border act on each neighbour pair
 //               as on CUDA cores.
@@ -45,8 +46,8 @@ constexpr int PRODUCER_WARP = EPI_WARPS, MMA_WARP = EPI_WARPS + 1;
 constexpr int NACC = 2;                 // TMEM accumulators of 256 columns
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
-constexpr int TC_MAX_STAGES = 4;
-constexpr int TC_MAX_GROUP = 8;         // column tiles per stage (one bulk copy)
+constexpr int TC_MAX_STAGES = 8;
+constexpr int TC_MAX_GROUP = 32;        // column tiles per stage (one bulk copy)
 constexpr int ISSUE_LANES = 8;          // producer lanes that take turns issuing copies
 constexpr long long WAIT_LIMIT = 8000000000LL;   // clock cycles (about 4 s)
 constexpr int UF_CAP = 1 << 22;
@@ -231,6 +232,22 @@ __device__ __noinline__ int tc_unite(int *parent, int a, int b, Ctrl *ctrl) {
     return min(a, b);
 }
 
+// OR of 64 words as a shallow tree of three-input ORs.
+__device__ __forceinline__ uint32_t or64(const uint32_t (&a)[32], const uint32_t (&b)[32]) {
+    uint32_t t[22];
+#pragma unroll
+    for (int g = 0; g < 10; ++g) t[g] = a[3 * g] | a[3 * g + 1] | a[3 * g + 2];
+    t[10] = a[30] | a[31] | b[0];
+#pragma unroll
+    for (int g = 0; g < 10; ++g) t[11 + g] = b[3 * g + 1] | b[3 * g + 2] | b[3 * g + 3];
+    t[21] = b[31];
+    uint32_t u[8];
+#pragma unroll
+    for (int g = 0; g < 7; ++g) u[g] = t[3 * g] | t[3 * g + 1] | t[3 * g + 2];
+    u[7] = t[21];
+    return (u[0] | u[1] | u[2]) | (u[3] | u[4] | u[5]) | (u[6] | u[7]);
+}
+
 // 32 x 32 bit transpose across a warp: lane i bit j -> lane j bit i.
 __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
     const uint32_t masks[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
@@ -297,6 +314,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
     const uint32_t tile_bytes = 128u * (uint32_t)kbytes;   // one packed 128-point tile
     const uint32_t sbo = (uint32_t)(kbytes >> 4) * 128u;
     const int ksteps = kbytes / 32;        // 8 tf32 or 16 bf16 elements per MMA
+    if (tile_bytes > (uint32_t)a.tile_bytes_max) {   // the host sized the tiles for less
+        if (tid == 0) set_error(ctrl, DBSCAN_ERR_INTERNAL);
+        return;
+    }
 
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
@@ -309,7 +330,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         }
         for (int i = 0; i < NACC; ++i) {
             mbar_init(smem_addr(&acc_full[i]), 1);
-            mbar_init(smem_addr(&acc_empty[i]), EPI_WARPS / 2);   // the group that owns it
+            mbar_init(smem_addr(&acc_empty[i]), EPI_WARPS);   // every epilogue warp
         }
         mbar_init(smem_addr(drain_bar), 1);
         *s_abort = 0;
@@ -437,12 +458,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             }
         }
     } else {
-        // ---------------- epilogue: two groups of 8 warps, alternate items ----------------
-        // Group g takes the items (tile pairs) with index parity g, which the
-        // MMA writes into accumulator g; while one group loads from TMEM the
-        // other computes.  Warp w8 of a group reads TMEM lanes 32*(w8 % 4)..
-        // and the tile w8 / 4 of the pair, 64 columns at a time.
-        const int grp = warp >> 3, w8 = warp & 7, wq = w8 & 3, hw = w8 >> 2;
+        // ---------------- epilogue: all 16 warps read every item ----------------
+        // Warp w reads TMEM lanes 32*(w % 4).. (the lanes its position in a
+        // warpgroup may access) and the 64 columns 64*(w / 4).. of the
+        // 256-column item, releases the accumulator as soon as its two loads
+        // have landed, and only then tests the values: the accumulator round
+        // trip is bounded by how fast TMEM is drained, which takes every warp.
+        const int wq = warp & 3, cq = warp >> 2;
         const int row = wq * 32 + lane;
         int last_rb = -1, acc = -1;             // UNION: a known ancestor of this row's point
         int lastq = -1;                         // UNION: last staged parent joined to this row
@@ -465,80 +487,76 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             int rowadd = 0, rowmin = 0x7fffffff;
             bool ok = true;
             for (int i = 0; 2 * i < m.ntiles; ++i, ++it) {
-                if ((it & 1) != grp) continue;        // the other group's item
-                const int b = grp;                    // == it % NACC
-                if (!(ok = __all_sync(FULL, mbar_wait(smem_addr(&acc_full[b]), (it >> 1) & 1, s_abort, ctrl))))
+                const int b = it % NACC;
+                if (!(ok = __all_sync(FULL, mbar_wait(smem_addr(&acc_full[b]), (it / NACC) & 1, s_abort, ctrl))))
                     break;
                 tc_fence_after();
-                const int ti = 2 * i + hw;            // tile within the stage
+                const int ti = 2 * i + (cq >> 1);     // tile within the stage
                 const bool have = ti < m.ntiles;      // warp-uniform
                 const int tile = m.t_first + ti;
                 const bool diag = a.tri && tile == m.rb;
-                const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(b * ACC_COLS + hw * 128);
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t v0[32], v1[32];
-                    if (have) {
-                        tmem_ld32(taddr + hh * 64, v0);
-                        tmem_ld32(taddr + hh * 64 + 32, v1);
-                        tmem_ld_wait();
-                    }
-                    if (hh == 1) {   // every TMEM read of this item is done: free the accumulator
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_addr(&acc_empty[b]));
-                    }
-                    if (!have) continue;
+                uint32_t v0[32], v1[32];
+                if (have) {
+                    const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) +
+                                           (uint32_t)(b * ACC_COLS + cq * 64);
+                    tmem_ld32(taddr, v0);
+                    tmem_ld32(taddr + 32, v1);
+                    tmem_ld_wait();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&acc_empty[b]));
+                if (!have) continue;
+                if (!__any_sync(FULL, rowvalid && (or64(v0, v1) >> 31))) continue;
 #pragma unroll
-                    for (int blk = 0; blk < 2; ++blk) {
-                        uint32_t (&v)[32] = blk ? v1 : v0;
-                        const int cb = hh * 64 + blk * 32;        // column offset in the tile
-                        const int qbase = tile * BT + cb;
-                        uint32_t o = 0;
+                for (int blk = 0; blk < 2; ++blk) {
+                    uint32_t (&v)[32] = blk ? v1 : v0;
+                    const int cb = (cq & 1) * 64 + blk * 32;   // column offset in the tile
+                    const int qbase = tile * BT + cb;
+                    uint32_t o = 0;
 #pragma unroll
-                        for (int c = 0; c < 32; c += 2) o |= v[c] | v[c + 1];
-                        if (!__any_sync(FULL, rowvalid && (o >> 31))) continue;
-                        // bit c = (w_c < 0), built in four independent 8-bit chains
-                        uint32_t m8[4] = {0u, 0u, 0u, 0u};
+                    for (int c = 0; c < 32; c += 2) o |= v[c] | v[c + 1];
+                    if (!__any_sync(FULL, rowvalid && (o >> 31))) continue;
+                    // bit c = (w_c < 0), built in four independent 8-bit chains
+                    uint32_t m8[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-                        for (int c = 7; c >= 0; --c)
+                    for (int c = 7; c >= 0; --c)
 #pragma unroll
-                            for (int g = 0; g < 4; ++g) m8[g] = __funnelshift_l(v[8 * g + c], m8[g], 1);
-                        uint32_t mask = m8[0] | (m8[1] << 8) | (m8[2] << 16) | (m8[3] << 24);
-                        const int nv = n_cols - qbase;
-                        mask &= nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
-                        if (!rowvalid) mask = 0;
-                        if (MODE == SWEEP_COUNT) {
-                            const int nh = __popc(mask);
-                            rowadd += nh;
-                            if (!diag) {   // the diagonal tile is counted from both sides already
-                                if (__any_sync(FULL, nh > 2)) {
-                                    // many neighbours: per-column sums through a bit transpose
-                                    const int cc = __popc(warp_transpose32(mask, lane));
-                                    if (cc) atomicAdd(a.cnt + qbase + lane, cc);
-                                } else {
-                                    // few: credit each neighbour's column directly
-                                    while (mask) {
-                                        const int cq = __ffs(mask) - 1;
-                                        mask &= mask - 1;
-                                        atomicAdd(a.cnt + qbase + cq, 1);
-                                    }
+                        for (int g = 0; g < 4; ++g) m8[g] = __funnelshift_l(v[8 * g + c], m8[g], 1);
+                    uint32_t mask = m8[0] | (m8[1] << 8) | (m8[2] << 16) | (m8[3] << 24);
+                    const int nv = n_cols - qbase;
+                    mask &= nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
+                    if (!rowvalid) mask = 0;
+                    if (MODE == SWEEP_COUNT) {
+                        const int nh = __popc(mask);
+                        rowadd += nh;
+                        if (!diag) {   // the diagonal tile is counted from both sides already
+                            if (__any_sync(FULL, nh > 2)) {
+                                // many neighbours: per-column sums through a bit transpose
+                                const int cc = __popc(warp_transpose32(mask, lane));
+                                if (cc) atomicAdd(a.cnt + qbase + lane, cc);
+                            } else {
+                                // few: credit each neighbour's column directly
+                                while (mask) {
+                                    const int cq2 = __ffs(mask) - 1;
+                                    mask &= mask - 1;
+                                    atomicAdd(a.cnt + qbase + cq2, 1);
                                 }
                             }
-                        } else {
-                            while (mask) {
-                                const int cq = __ffs(mask) - 1;
-                                mask &= mask - 1;
-                                const int q = qbase + cq;
-                                const int aq = saux[ti * BT + cb + cq];
-                                if (MODE == SWEEP_UNION) {
-                                    if (diag && q <= p) continue;
-                                    if (aq == acc || aq == lastq) continue;
-                                    lastq = aq;   // aq joins this row's set for good
-                                    acc = tc_unite(a.parent, acc, aq, ctrl);
-                                } else {
-                                    rowmin = min(rowmin, aq);
-                                }
+                        }
+                    } else {
+                        while (mask) {
+                            const int cq2 = __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            const int q = qbase + cq2;
+                            const int aq = saux[ti * BT + cb + cq2];
+                            if (MODE == SWEEP_UNION) {
+                                if (diag && q <= p) continue;
+                                if (aq == acc || aq == lastq) continue;
+                                lastq = aq;   // aq joins this row's set for good
+                                acc = tc_unite(a.parent, acc, aq, ctrl);
+                            } else {
+                                rowmin = min(rowmin, aq);
                             }
                         }
                     }
@@ -569,12 +587,18 @@ size_t tc_smem_bytes(int tile_bytes, int stage_bytes, int stages) {
 
 template <int MODE, int KIND>
 cudaError_t run_tc(TcArgs a, const Layout &L, cudaStream_t s) {
-    const int kb = tc_kbytes(KIND, L.d, 3);   // largest operand row this path can need
+    // largest operand row this path can need for this eps (the device's choice
+    // of threshold digits never exceeds the host's bound)
+    const int kb = tc_kbytes(KIND, L.d, tc_nt_bound(KIND, L.eps2));
     if (L.umma_tile_bytes == 0 || kb > TC_MAX_KBYTES) return cudaSuccess;   // never selected
     auto kernel = k_sweep_tc<MODE, KIND>;
     const int tile = 128 * kb;
     const int aux = MODE != SWEEP_COUNT ? BT * 4 : 0;
-    const size_t budget = 200 * 1024;
+    const size_t budget = 224 * 1024;
+    // Few, large stages: every stage costs a round of barrier handshakes
+    // between the producer, the MMA thread and all epilogue warps, so the
+    // group is the largest even number of tiles (<= 32) for which two stages
+    // and the two row tiles fit; deeper rings did not help.
     int group = TC_MAX_GROUP;
     while (group > 2 && 2 * (size_t)tile + 2 * (size_t)group * (tile + aux) > budget) group -= 2;
     const int stage_bytes = group * (tile + aux);
