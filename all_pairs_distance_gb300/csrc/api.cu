@@ -58,11 +58,15 @@ Layout make_layout(int64_t n, int32_t d) {
     }
     L.umma_tile_bytes = (size_t)BT * kb;
     const size_t umma = (size_t)L.ntiles * L.umma_tile_bytes;
+    // Row and column operand arrays.  The all-point operands die with the
+    // count sweep, the core row operands with the union sweep, so the core
+    // operands reuse the all-point arrays and the candidate rows (staged after
+    // the union) reuse the row array.
     L.off_ua_all = off;      off += align256(umma);
     L.off_ub_all = off;      off += align256(umma);
-    L.off_ua_core = off;     off += align256(umma);
-    L.off_ub_core = off;     off += align256(umma);
-    L.off_ua_cand = off;     off += align256(umma);
+    L.off_ua_core = L.off_ua_all;
+    L.off_ub_core = L.off_ub_all;
+    L.off_ua_cand = L.off_ua_all;
     // locality order
     L.order_bits = order_bits(n);
     const size_t nbins = (size_t)1 << L.order_bits;
@@ -177,8 +181,9 @@ static void keep_pool(void) {
 // CUDA-core kernel and one kernel per tensor-core path the shape allows
 // (ntc); all but the path chosen on the device return at once.
 //   prep 4 + 5 locality order (+1 operand staging), count 1 + ntc,
-//   compact 4 (+2 operand stagings), union 1 tile-local + 4 waves x
-//   (1 + ntc) + 3 compressions, flatten 2, border 1 + ntc, finalize 1.
+//   compact 4 (+1 operand staging), union 1 tile-local + 4 waves x
+//   (1 + ntc) + 3 compressions, flatten 2, border (+1 operand staging)
+//   1 + ntc, finalize 1.
 static int stage_launches(int d, int stage) {
     int ntc = 0;
     for (int kind = TC_TF32; kind <= TC_BF16; ++kind)
@@ -187,10 +192,10 @@ static int stage_launches(int d, int stage) {
     switch (stage) {
     case 0: return 9 + umma;
     case 1: return 1 + ntc;
-    case 2: return 4 + 2 * umma;
+    case 2: return 4 + umma;
     case 3: return 1 + 4 * (1 + ntc) + 3;
     case 4: return 2;
-    case 5: return 1 + ntc;
+    case 5: return umma + 1 + ntc;
     default: return 1;
     }
 }
@@ -260,6 +265,7 @@ static int run(const void *points, int dtype, int64_t n, int d, float eps, int m
     marks.mark(s);
     if (launch_flatten(w, L, labels, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     marks.mark(s);
+    if (launch_stage_umma(w, L, 2, s) != cudaSuccess) return DBSCAN_ERR_CUDA;   // candidate rows
     if (launch_border(w, L, labels, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     marks.mark(s);
     if (launch_finalize(w, L, labels, s) != cudaSuccess) return DBSCAN_ERR_CUDA;

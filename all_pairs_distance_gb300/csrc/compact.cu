@@ -227,8 +227,7 @@ cudaError_t launch_compact(const Work &w, const Layout &L, int min_pts, int32_t 
     k_pad_tails<<<1, 128, 0, s>>>(w.ctrl, L.d, w.staged_core, w.T_core, w.staged_cand, w.T_cand);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if ((e = launch_stage_umma(w, L, 1, s)) != cudaSuccess) return e;
-    return launch_stage_umma(w, L, 2, s);
+    return launch_stage_umma(w, L, 1, s);   // core operands (candidate rows: after the union)
 }
 
 cudaError_t launch_flatten(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s) {

@@ -189,8 +189,9 @@ def run_reference(args, dist: Dist):
     import oracle
     from all_pairs_distance_gb300 import synth
     w = synth.WORKLOADS[args.workload]
-    P = synth.generate(args.workload)
-    m = 20_000 if w.d <= 4 else 6_000
+    P = synth.generate(args.workload) if args.n is None else synth.scaled(args.workload, args.n)
+    n = len(P)
+    m = min(n, 20_000 if w.d <= 4 else 6_000)
     S = P[:m]
     for _ in range(args.warmup):
         oracle.dbscan(S, w.eps, w.min_pts)
@@ -201,13 +202,14 @@ def run_reference(args, dist: Dist):
         times.append(time.perf_counter() - t)
     step = sum(times) / len(times)
     value = m * m / step
-    sample = (f"first {m} of {w.n} points of {w.name} per step, full oracle DBSCAN "
+    name = w.name if args.n is None else f"{w.name} scaled to n={n}"
+    sample = (f"first {m} of {n} points of {name} per step, full oracle DBSCAN "
               f"(count + BFS), single-threaded")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": w.name, "n": w.n, "d": w.d, "eps": w.eps,
+            "config": {"workload": name, "n": n, "d": w.d, "eps": w.eps,
                        "min_pts": w.min_pts, "sample_points": m},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample},
@@ -282,24 +284,33 @@ def run_gb300(args, dist: Dist):
     achieved = count_flops(n, d) / (count_ms * 1e-3) / 1e12
     src = "sweep_tc.cu" if info["path"] != "fp32" else "sweep.cu"
     traffic = recorded_traffic(os.path.join(ROOT, "all_pairs_distance_gb300", "csrc", src), w.name)
-    if info["path"] == "fp32":
-        roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
-                    "frac": achieved / fp32_peak, "traffic": traffic,
-                    "kernel": "count sweep on CUDA cores (fp32 FFMA, upper triangle)",
-                    "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
-                                   f"{max_mhz:.0f} MHz (max SM clock"
-                                   + (", MEASURED_PEAKS.json)" if peaks else ", recipe fallback)")}
-    else:
+    # d <= 16: the distance pass is d FMAs per pair, so its roofline is the FP32
+    # CUDA-core peak whichever unit evaluates it; d > 16: the bf16 tensor peak.
+    tc_peak = None
+    if info["path"] != "fp32":
         bf16 = (peaks or {}).get("bf16_tflops", BF16_FALLBACK_TFLOPS)
-        peak = bf16 if info["path"] == "bf16" else bf16 * TF32_PER_BF16
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": traffic,
-                    "kernel": f"count sweep on tensor cores (tcgen05 {info['path']}, K={info['kpad']}, "
-                              f"upper triangle)",
-                    "peak_source": ("measured bf16 burst (MEASURED_PEAKS.json)" if peaks else
-                                    "recipe fallback bf16") +
-                                   ("" if info["path"] == "bf16" else
-                                    f" x {TF32_PER_BF16:.3f} (nominal tf32/bf16 ratio 1.1/2.25)"),
+        tc_peak = bf16 if info["path"] == "bf16" else bf16 * TF32_PER_BF16
+        tc_source = (("measured bf16 burst (MEASURED_PEAKS.json)" if peaks else "recipe fallback bf16") +
+                     ("" if info["path"] == "bf16" else
+                      f" x {TF32_PER_BF16:.3f} (nominal tf32/bf16 ratio 1.1/2.25)"))
+    kname = ("count sweep on CUDA cores (fp32 FFMA, upper triangle)" if info["path"] == "fp32" else
+             f"count sweep on tensor cores (tcgen05 {info['path']}, K={info['kpad']}, upper triangle)")
+    fp32_source = (f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
+                   f"{max_mhz:.0f} MHz (max SM clock" +
+                   (", MEASURED_PEAKS.json)" if peaks else ", recipe fallback)"))
+    if d <= 16 or info["path"] == "fp32":
+        roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
+                    "frac": achieved / fp32_peak, "traffic": traffic, "kernel": kname,
+                    "peak_source": fp32_source + " -- of derived FP32 FMA peak"}
+        if tc_peak is not None:
+            roofline["tensor_pipe"] = {"achieved": achieved, "peak": tc_peak,
+                                       "frac": achieved / tc_peak, "peak_source": tc_source,
+                                       "note": "the same algorithmic FLOP against the tensor peak of "
+                                               "the MMA kind the sweep runs on"}
+    else:
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                    "frac": achieved / tc_peak, "traffic": traffic, "kernel": kname,
+                    "peak_source": tc_source + " -- of measured",
                     "fp32_equivalent": {"achieved": achieved, "peak": fp32_peak,
                                         "frac": achieved / fp32_peak,
                                         "note": "same algorithmic FLOP (2d per unordered pair) "
@@ -307,7 +318,8 @@ def run_gb300(args, dist: Dist):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": {"fp32": "f32", "tf32": "tf32", "bf16": "bf16"}[info["path"]],
             "data": "synthetic",
             "config": {"workload": w.name if args.n is None else f"{w.name} scaled to n={n}",
                        "n": n, "d": d, "eps": w.eps, "min_pts": w.min_pts,

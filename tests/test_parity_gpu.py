@@ -99,6 +99,40 @@ def test_eps_zero_and_min_pts_above_n():
             assert_same(g, e, f"eps={eps} min_pts={mp} {w}")
 
 
+def test_min_pts_one_every_point_is_core():
+    P = synth.scaled("blobs_100k_d2", 6_000, seed=11)
+    ref = oracle.dbscan(P, 20.0, 1)
+    got = gpu_run(P, 20.0, 1)
+    assert np.all(got[1] == 1)
+    for g, e, w in zip(got, ref, ("cnt", "core", "label")):
+        assert_same(g, e, f"min_pts=1 {w}")
+
+
+@pytest.mark.parametrize("order", ["sorted", "reversed", "interleaved"])
+def test_input_order_does_not_matter(order, monkeypatch):
+    # the kernels sort the points into a locality order of their own; results
+    # are defined on input indices, so any input order must match the oracle
+    # run on that same order (already sorted input included)
+    P = synth.scaled("blobs_1m_d3", 12_000, seed=12)
+    if order == "sorted":
+        P = P[np.lexsort(P.T[::-1])]
+    elif order == "reversed":
+        P = P[np.lexsort(P.T[::-1])][::-1]
+    else:
+        idx = np.lexsort(P.T[::-1])
+        P = P[np.concatenate([idx[0::2], idx[1::2]])]
+    P = np.ascontiguousarray(P)
+    ref = oracle.dbscan(P, 10.0, 8)
+    for path in ("fp32", "default"):
+        if path == "fp32":
+            monkeypatch.setenv("DBSCAN_FORCE_PATH", "fp32")
+        else:
+            monkeypatch.delenv("DBSCAN_FORCE_PATH", raising=False)
+        got = gpu_run(P, 10.0, 8)
+        for g, e, w in zip(got, ref, ("cnt", "core", "label")):
+            assert_same(g, e, f"{order} path={path} {w}")
+
+
 def test_inclusive_boundary_at_full_range():
     # two points at the ends of [0, 2047] with eps equal to their distance:
     # the squared distance 2047^2 equals eps^2 and must count (<=)
