@@ -39,12 +39,12 @@ constexpr int UF_CAP = 1 << 22;  // iteration cap of union-find loops
 
 // Counters in Ctrl::unit_ctr.
 constexpr int CTR_COUNT = 0, CTR_UNION0 = 1, CTR_BORDER = 5;
-constexpr int UNION_WAVES = 4;
+constexpr int UNION_WAVES = 2;
 // Union waves cover units [edge_w * G, edge_{w+1} * G) for a grid of G CTAs
 // (rows in ascending order, -1 = to the end); the union-find is compressed
 // between waves so that later waves mostly find equal parents in the staged
 // snapshot and never touch global memory.
-static const int kUnionWaveEdges[UNION_WAVES + 1] = {0, 1, 3, 8, -1};
+static const int kUnionWaveEdges[UNION_WAVES + 1] = {0, 2, -1};
 
 struct SweepArgs {
     const float *rows;     // staged row points

@@ -27,8 +27,10 @@
 //               and the columns by atomics (few neighbours) or a warp bit
 //               transpose (many); union and border act on each neighbour pair
 //               as on CUDA cores.
-// The producer and MMA roles poll their barriers without suspending: their
-// reaction time is on the critical path of the accumulator round trip.
+// Every role polls its barriers without suspending: each reaction (MMA issue,
+// accumulator drain, stage refill) lies on the critical path of the
+// accumulator round trip, and a suspended thread resumes hundreds of cycles
+// after the phase completes.
 // Every wait on an mbarrier is bounded; on timeout the CTA records
 // DBSCAN_ERR_INTERNAL, stops issuing work, waits (bounded) for its own copies
 // and MMAs in flight, frees its TMEM and returns.
@@ -111,17 +113,14 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait; false on timeout or when another role aborted.  SPIN polls
-// without suspending (a suspended thread resumes hundreds of cycles after
-// the phase completes): used by the single-thread producer and MMA roles,
-// whose reaction time is on the critical path; the epilogue warps suspend.
-template <bool SPIN>
-__device__ __noinline__ bool mbar_wait_t(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         Ctrl *ctrl) {
+// Bounded wait that polls without suspending; false on timeout or when
+// another role aborted.
+__device__ __noinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                       Ctrl *ctrl) {
     long long start = 0;
     for (unsigned it = 0;; ++it) {
-        if (SPIN ? mbar_test(bar, parity) : mbar_try(bar, parity)) return true;
-        if ((it & (SPIN ? 1023 : 63)) == (SPIN ? 1023 : 63)) {
+        if (mbar_test(bar, parity)) return true;
+        if ((it & 1023) == 1023) {
             if (*abort_flag) return false;
             const long long now = clock64();
             if (start == 0) start = now;
@@ -132,14 +131,6 @@ __device__ __noinline__ bool mbar_wait_t(uint32_t bar, uint32_t parity, volatile
             }
         }
     }
-}
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          Ctrl *ctrl) {
-    return mbar_wait_t<false>(bar, parity, abort_flag, ctrl);
-}
-__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          Ctrl *ctrl) {
-    return mbar_wait_t<true>(bar, parity, abort_flag, ctrl);
 }
 // Bounded wait that ignores the abort flag (draining copies in flight).
 __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
@@ -322,7 +313,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_addr(&b_full[i]), 1);
-            mbar_init(smem_addr(&b_empty[i]), 1 + EPI_WARPS);   // MMA commit + every epilogue warp
+            // every epilogue warp; a warp arrives only after it has seen the
+            // accumulator commit of the stage's last tile pair, which implies that
+            // every MMA reading the stage has completed
+            mbar_init(smem_addr(&b_empty[i]), EPI_WARPS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_addr(&a_full[i]), 1);
@@ -445,7 +439,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                     umma_commit(smem_addr(&acc_full[b]));
                 }
                 if (!ok) break;
-                umma_commit(smem_addr(&b_empty[s]));
                 if (m.flags & F_LAST) {
                     umma_commit(smem_addr(&a_empty[m.abuf]));
                     ++ua;
@@ -472,7 +465,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         for (;;) {
             const int s = k % S;
             // every lane waits; the warp goes on only if all lanes saw the phase
-            if (!__all_sync(FULL, mbar_wait(smem_addr(&b_full[s]), (k / S) & 1, s_abort, ctrl))) break;
+            if (!__all_sync(FULL, mbar_spin(smem_addr(&b_full[s]), (k / S) & 1, s_abort, ctrl))) break;
             const Meta m = meta[s];
             if (m.flags & F_TERM) break;
             const int p = m.rb * BT + row;
@@ -488,7 +481,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             bool ok = true;
             for (int i = 0; 2 * i < m.ntiles; ++i, ++it) {
                 const int b = it % NACC;
-                if (!(ok = __all_sync(FULL, mbar_wait(smem_addr(&acc_full[b]), (it / NACC) & 1, s_abort, ctrl))))
+                if (!(ok = __all_sync(FULL, mbar_spin(smem_addr(&acc_full[b]), (it / NACC) & 1, s_abort, ctrl))))
                     break;
                 tc_fence_after();
                 const int ti = 2 * i + (cq >> 1);     // tile within the stage
