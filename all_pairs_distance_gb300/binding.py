@@ -183,7 +183,7 @@ def dbscan_workspace_status(workspace: torch.Tensor, stream=None) -> int:
     return int(load().dbscan_workspace_status(workspace.data_ptr(), _stream_handle(stream)))
 
 
-PATHS = {0: "fp32", 1: "tf32", 2: "bf16"}
+PATHS = {0: "fp32", 1: "tf32", 2: "bf16", 3: "f16"}
 
 
 def dbscan_workspace_info(workspace: torch.Tensor, stream=None) -> dict:

@@ -52,9 +52,10 @@ Layout make_layout(int64_t n, int32_t d) {
     L.off_bsum = off;        off += align256((size_t)2 * (L.nscan_blocks + 1) * sizeof(int));
     // tensor-core operand tiles, sized for the largest path this shape allows
     size_t kb = 0;
-    for (int kind = TC_TF32; kind <= TC_BF16; ++kind) {
-        const int b = tc_kbytes(kind, d, 3);
-        if (b <= TC_MAX_KBYTES && (size_t)b > kb) kb = (size_t)b;
+    for (int kind = TC_TF32; kind <= TC_F16; ++kind) {
+        const int nt = kind == TC_F16 ? 2 : 3;   // the most threshold digits a kind takes
+        const int b = tc_kbytes(kind, d, nt);
+        if (tc_fits(kind, d, nt) && (size_t)b > kb) kb = (size_t)b;
     }
     L.umma_tile_bytes = (size_t)BT * kb;
     const size_t umma = (size_t)L.ntiles * L.umma_tile_bytes;
@@ -80,18 +81,20 @@ Layout make_layout(int64_t n, int32_t d) {
     return L;
 }
 
-// Tensor-core paths this call may use (operand rows within TC_MAX_KBYTES for
-// the threshold digits eps allows), narrowed by DBSCAN_FORCE_PATH ("fp32",
-// "tf32" or "bf16") when it is set.
+// Tensor-core paths this call may use (operand rows that fit the kind for the
+// threshold digits eps allows), narrowed by DBSCAN_FORCE_PATH ("fp32", "tf32",
+// "bf16" or "f16") when it is set.
 static int allowed_tc(int d, float eps2) {
     int allow = 0;
-    if (tc_kbytes(TC_TF32, d, tc_nt_bound(TC_TF32, eps2)) <= TC_MAX_KBYTES) allow |= TC_ALLOW_TF32;
-    if (tc_kbytes(TC_BF16, d, tc_nt_bound(TC_BF16, eps2)) <= TC_MAX_KBYTES) allow |= TC_ALLOW_BF16;
+    if (tc_fits(TC_TF32, d, tc_nt_bound(TC_TF32, eps2))) allow |= TC_ALLOW_TF32;
+    if (tc_fits(TC_BF16, d, tc_nt_bound(TC_BF16, eps2))) allow |= TC_ALLOW_BF16;
+    if (tc_fits(TC_F16, d, tc_nt_bound(TC_F16, eps2))) allow |= TC_ALLOW_F16;
     const char *f = getenv("DBSCAN_FORCE_PATH");
     if (f && *f) {
         if (!strcmp(f, "fp32")) allow = 0;
         else if (!strcmp(f, "tf32")) allow &= TC_ALLOW_TF32;
         else if (!strcmp(f, "bf16")) allow &= TC_ALLOW_BF16;
+        else if (!strcmp(f, "f16")) allow &= TC_ALLOW_F16;
     }
     return allow;
 }
@@ -184,10 +187,10 @@ static void keep_pool(void) {
 //   compact 4 (+1 operand staging), union 1 tile-local + 2 waves x
 //   (1 + ntc) + 1 compression, flatten 2, border (+1 operand staging)
 //   1 + ntc, finalize 1.
-static int stage_launches(int d, int stage) {
+static int stage_launches(int d, float eps2, int stage) {
     int ntc = 0;
-    for (int kind = TC_TF32; kind <= TC_BF16; ++kind)
-        if (tc_kbytes(kind, d, 3) <= TC_MAX_KBYTES) ++ntc;
+    for (int kind = TC_TF32; kind <= TC_F16; ++kind)
+        if (tc_fits(kind, d, tc_nt_bound(kind, eps2))) ++ntc;
     const int umma = ntc > 0 ? 1 : 0;
     switch (stage) {
     case 0: return 9 + umma;
@@ -204,6 +207,7 @@ struct ProfCall {
     cudaEvent_t ev[DBSCAN_NUM_STAGES + 1];
     int stages;   // number of stages the call ran
     int d;        // dimension of the call (sets the kernels per stage)
+    float eps2;   // eps^2 of the call (sets the tensor-core kinds launched)
 };
 struct ProfState {
     bool on = false;
@@ -216,8 +220,9 @@ struct StageMarks {
     ProfCall call{};
     bool on = false;
     int next = 0;
-    StageMarks(cudaStream_t s, int d) {
+    StageMarks(cudaStream_t s, int d, float eps2) {
         call.d = d;
+        call.eps2 = eps2;
         if (!g_prof.on) return;
         for (int i = 0; i <= DBSCAN_NUM_STAGES; ++i) {
             if (cudaEventCreate(&call.ev[i]) != cudaSuccess) {
@@ -247,7 +252,7 @@ static int run(const void *points, int dtype, int64_t n, int d, float eps, int m
                int32_t *labels, uint8_t *is_core, int32_t *cnt_out, void *ws, const Layout &L,
                cudaStream_t s) {
     Work w = carve(ws, L);
-    StageMarks marks(s, d);
+    StageMarks marks(s, d, L.eps2);
     if (cudaMemsetAsync(w.ctrl, 0, sizeof(Ctrl), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     if (cudaMemsetAsync(w.cnt, 0, (size_t)n * sizeof(int), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     if (launch_prep(points, dtype, n, d, eps, allowed_tc(d, L.eps2), w, L, s) != cudaSuccess)
@@ -400,7 +405,7 @@ int dbscan_profile_end(float *stage_ms, int32_t max_stages, int64_t *calls,
                 cudaEventElapsedTime(&ms, c.ev[i], c.ev[i + 1]) != cudaSuccess)
                 st = DBSCAN_ERR_CUDA;
             acc[i] += ms;
-            launches += stage_launches(c.d, i);
+            launches += stage_launches(c.d, c.eps2, i);
         }
         for (int i = 0; i <= c.stages; ++i) cudaEventDestroy(c.ev[i]);
     }

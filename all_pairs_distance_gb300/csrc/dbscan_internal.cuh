@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 #include <stddef.h>
 
@@ -95,15 +96,19 @@ enum SweepMode { SWEEP_COUNT = 0, SWEEP_UNION = 1, SWEEP_BORDER = 2 };
 // Tensor-core paths.  The operands carry, per point, the d coordinates plus
 // base-B digits of the squared norms and of the threshold constant, so one
 // MMA yields w_ij = |c_i - c_j|^2 - thrx exactly (see prep.cu):
-//   TF32: elements exact up to 2048, base 2048, 2 digits per norm
-//   BF16: elements exact up to 256,  base 256,  3 digits per norm
-// plus nt (1..3) digits of thrx.
-enum TcKind { TC_NONE = 0, TC_TF32 = 1, TC_BF16 = 2 };
+//   TF32: elements exact up to 2048, base 2048, 2 digits per norm, f32 accumulator
+//   BF16: elements exact up to 256,  base 256,  3 digits per norm, f32 accumulator
+//   F16:  elements exact up to 2048, base 2048, 2 digits per norm, f16 accumulator;
+//         only when every operand row fits one K = 16 MMA, so the exact sum is
+//         rounded to f16 once (its sign, all the sweep reads, survives)
+// plus nt digits of thrx (1..3; at most 2 for F16, whose largest power is B).
+enum TcKind { TC_NONE = 0, TC_TF32 = 1, TC_BF16 = 2, TC_F16 = 3 };
 // Allowed-path mask passed from the host (all by default).
-enum { TC_ALLOW_TF32 = 1, TC_ALLOW_BF16 = 2 };
+enum { TC_ALLOW_TF32 = 1, TC_ALLOW_BF16 = 2, TC_ALLOW_F16 = 4 };
 constexpr int TC_MAX_KBYTES = 256;   // largest operand row the tensor-core sweep stages
+constexpr int TC_F16_KBYTES = 32;    // the one K = 16 MMA of the F16 path
 
-__host__ __device__ inline int tc_norm_digits(int kind) { return kind == TC_TF32 ? 2 : 3; }
+__host__ __device__ inline int tc_norm_digits(int kind) { return kind == TC_BF16 ? 3 : 2; }
 __host__ __device__ inline int tc_kpad(int kind, int d, int nt) {
     const int used = d + 2 * tc_norm_digits(kind) + nt;
     return kind == TC_TF32 ? ((used + 7) / 8) * 8 : ((used + 15) / 16) * 16;
@@ -111,11 +116,16 @@ __host__ __device__ inline int tc_kpad(int kind, int d, int nt) {
 __host__ __device__ inline int tc_kbytes(int kind, int d, int nt) {
     return tc_kpad(kind, d, nt) * (kind == TC_TF32 ? 4 : 2);
 }
+// Whether a kind can hold the operand rows of dimension d with nt threshold digits.
+__host__ __device__ inline bool tc_fits(int kind, int d, int nt) {
+    if (kind == TC_F16) return nt <= 2 && tc_kbytes(kind, d, nt) <= TC_F16_KBYTES;
+    return tc_kbytes(kind, d, nt) <= TC_MAX_KBYTES;
+}
 // Digits of the threshold constant thrx (<= floor(eps2) + 1, see prep.cu)
 // in the operands of a path: the host sizes the sweep's shared-memory tiles
 // with this bound, the device takes the digits of the actual thrx.
 __host__ __device__ inline int tc_nt_for(int kind, double thrx) {
-    if (kind == TC_TF32) return thrx < 2048.0 ? 1 : (thrx < 4194304.0 ? 2 : 3);
+    if (kind != TC_BF16) return thrx < 2048.0 ? 1 : (thrx < 4194304.0 ? 2 : 3);
     return thrx < 256.0 ? 1 : (thrx < 65536.0 ? 2 : 3);
 }
 inline int tc_nt_bound(int kind, float eps2) {

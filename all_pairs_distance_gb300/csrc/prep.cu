@@ -19,7 +19,7 @@
 // page's form overflows 2^24 already at d = 3 over [0, 2047].
 //
 // Tensor-core operands.  When every centred coordinate is an integer small
-// enough for the MMA input type (|2c| <= 2048 for tf32, <= 256 for bf16), the
+// enough for the MMA input type (|2c| <= 2048 for tf32 and f16, <= 256 for bf16), the
 // pair quantity w_ij = |c_i - c_j|^2 - thrx is written as one dot product
 //     A_i = [-2 c_i,  1, B, ..,   n0_i, n1_i, ..,  -h0, -h1, ..]
 //     B_j = [   c_j,  n0_j, n1_j, .., 1, B, ..,     1,   B, ..]
@@ -123,13 +123,15 @@ __global__ void k_setup(Ctrl *ctrl, const int *smin, const int *smax, float *cen
         const int nt = tc_nt_for(TC_TF32, thrx);
         int kind = TC_NONE;
         if (integral && !ctrl->nonfinite && 4.0 * S < 16777216.0 && 2.0 * S + thrx < 16777216.0) {
+            // preference: F16 (one MMA, half-width accumulator reads), then BF16, then TF32
             const int ntb = tc_nt_for(TC_BF16, thrx);
-            if ((allow & TC_ALLOW_BF16) && rmax <= 256.0 &&
-                tc_kbytes(TC_BF16, d, ntb) <= TC_MAX_KBYTES) {
+            if ((allow & TC_ALLOW_F16) && rmax <= 2048.0 && tc_fits(TC_F16, d, nt)) {
+                kind = TC_F16;
+                ctrl->tc_nt = nt;
+            } else if ((allow & TC_ALLOW_BF16) && rmax <= 256.0 && tc_fits(TC_BF16, d, ntb)) {
                 kind = TC_BF16;
                 ctrl->tc_nt = ntb;
-            } else if ((allow & TC_ALLOW_TF32) && rmax <= 2048.0 &&
-                       tc_kbytes(TC_TF32, d, nt) <= TC_MAX_KBYTES) {
+            } else if ((allow & TC_ALLOW_TF32) && rmax <= 2048.0 && tc_fits(TC_TF32, d, nt)) {
                 kind = TC_TF32;
                 ctrl->tc_nt = nt;
             }
@@ -141,11 +143,13 @@ __global__ void k_setup(Ctrl *ctrl, const int *smin, const int *smax, float *cen
     }
 }
 
-// Write element k of an operand row: float bits for tf32, bf16 otherwise.
+// Write element k of an operand row: float bits for tf32, f16 or bf16 otherwise.
 __device__ __forceinline__ void put_elem(uint8_t *tile, int row, int k, int kbytes, int kind,
                                          float v) {
     if (kind == TC_TF32) {
         *reinterpret_cast<float *>(tile + umma_offset(row, 4 * k, kbytes)) = v;
+    } else if (kind == TC_F16) {
+        *reinterpret_cast<__half *>(tile + umma_offset(row, 2 * k, kbytes)) = __float2half_rn(v);
     } else {
         *reinterpret_cast<__nv_bfloat16 *>(tile + umma_offset(row, 2 * k, kbytes)) =
             __float2bfloat16_rn(v);
@@ -175,7 +179,7 @@ __global__ void k_stage_umma(const Ctrl *ctrl, const int *count, const float *st
         }
         return;
     }
-    const int base = kind == TC_TF32 ? 2048 : 256;
+    const int base = kind == TC_BF16 ? 256 : 2048;
     const int nd = tc_norm_digits(kind);
     const float *src = staged + (size_t)tile * (size_t)(d + 1) * BT + row;
     int k = 0;

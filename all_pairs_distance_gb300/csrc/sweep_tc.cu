@@ -153,10 +153,10 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t sbo) {
     d |= (uint64_t)1 << 46;                             // tcgen05 descriptor version
     return d;                                           // no swizzle, base offset 0
 }
-// D f32, A and B of format fmt, both K-major, M = 128, N = n.
-__device__ __forceinline__ uint32_t umma_idesc(int fmt, int n) {
-    return (1u << 4) | ((uint32_t)fmt << 7) | ((uint32_t)fmt << 10) | (((uint32_t)n >> 3) << 17) |
-           ((128u >> 4) << 24);
+// D f32 (or f16), A and B of format fmt, both K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t umma_idesc(int fmt, int n, bool f32acc) {
+    return ((f32acc ? 1u : 0u) << 4) | ((uint32_t)fmt << 7) | ((uint32_t)fmt << 10) |
+           (((uint32_t)n >> 3) << 17) | ((128u >> 4) << 24);
 }
 template <int KIND>
 __device__ __forceinline__ void umma(uint32_t tmem, uint64_t da, uint64_t db, uint32_t idesc,
@@ -195,6 +195,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[31])
         : "r"(taddr));
 }
+// 32 lanes x 64 columns of an f16 accumulator, two columns per register:
+// column 2j in bits 0-15 of r[j], column 2j + 1 in bits 16-31.
+__device__ __forceinline__ void tmem_ld32p(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.pack::16b.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -221,6 +236,15 @@ __device__ __noinline__ int tc_unite(int *parent, int a, int b, Ctrl *ctrl) {
     }
     set_error(ctrl, DBSCAN_ERR_INTERNAL);
     return min(a, b);
+}
+
+// OR of 32 words as a shallow tree of three-input ORs.
+__device__ __forceinline__ uint32_t or32(const uint32_t (&a)[32]) {
+    uint32_t t[11];
+#pragma unroll
+    for (int g = 0; g < 10; ++g) t[g] = a[3 * g] | a[3 * g + 1] | a[3 * g + 2];
+    t[10] = a[30] | a[31];
+    return (t[0] | t[1] | t[2]) | (t[3] | t[4] | t[5]) | (t[6] | t[7] | t[8]) | (t[9] | t[10]);
 }
 
 // OR of 64 words as a shallow tree of three-input ORs.
@@ -304,7 +328,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
     const int kbytes = ctrl->tc_kbytes;
     const uint32_t tile_bytes = 128u * (uint32_t)kbytes;   // one packed 128-point tile
     const uint32_t sbo = (uint32_t)(kbytes >> 4) * 128u;
-    const int ksteps = kbytes / 32;        // 8 tf32 or 16 bf16 elements per MMA
+    const int ksteps = kbytes / 32;        // 8 tf32 or 16 f16/bf16 elements per MMA
     if (tile_bytes > (uint32_t)a.tile_bytes_max) {   // the host sized the tiles for less
         if (tid == 0) set_error(ctrl, DBSCAN_ERR_INTERNAL);
         return;
@@ -411,8 +435,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         }
     } else if (warp == MMA_WARP) {
         if (lane == 0) {
-            const int fmt = KIND == TC_TF32 ? 2 : 1;
-            const uint32_t idesc256 = umma_idesc(fmt, 256), idesc128 = umma_idesc(fmt, 128);
+            const int fmt = KIND == TC_TF32 ? 2 : (KIND == TC_BF16 ? 1 : 0);
+            const bool f32acc = KIND != TC_F16;
+            const uint32_t idesc256 = umma_idesc(fmt, 256, f32acc), idesc128 = umma_idesc(fmt, 128, f32acc);
             int k = 0, ua = 0, it = 0;
             bool issued = false, ok = true;
             for (;;) {
@@ -488,35 +513,63 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                 const bool have = ti < m.ntiles;      // warp-uniform
                 const int tile = m.t_first + ti;
                 const bool diag = a.tri && tile == m.rb;
+                // f32 accumulator: v0, v1 = columns 0-31, 32-63 of the warp's 64;
+                // f16 accumulator: v0 = all 64 columns, two per register
                 uint32_t v0[32], v1[32];
                 if (have) {
                     const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) +
                                            (uint32_t)(b * ACC_COLS + cq * 64);
-                    tmem_ld32(taddr, v0);
-                    tmem_ld32(taddr + 32, v1);
+                    if (KIND == TC_F16) {
+                        tmem_ld32p(taddr, v0);
+                    } else {
+                        tmem_ld32(taddr, v0);
+                        tmem_ld32(taddr + 32, v1);
+                    }
                     tmem_ld_wait();
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&acc_empty[b]));
                 if (!have) continue;
-                if (!__any_sync(FULL, rowvalid && (or64(v0, v1) >> 31))) continue;
+                const uint32_t neg = KIND == TC_F16 ? (or32(v0) & 0x80008000u) : (or64(v0, v1) >> 31);
+                if (!__any_sync(FULL, rowvalid && neg)) continue;
 #pragma unroll
                 for (int blk = 0; blk < 2; ++blk) {
-                    uint32_t (&v)[32] = blk ? v1 : v0;
                     const int cb = (cq & 1) * 64 + blk * 32;   // column offset in the tile
                     const int qbase = tile * BT + cb;
-                    uint32_t o = 0;
+                    // bit c of mask = (w_c < 0) for the block's 32 columns
+                    uint32_t mask;
+                    if (KIND == TC_F16) {
+                        uint32_t o = 0;
 #pragma unroll
-                    for (int c = 0; c < 32; c += 2) o |= v[c] | v[c + 1];
-                    if (!__any_sync(FULL, rowvalid && (o >> 31))) continue;
-                    // bit c = (w_c < 0), built in four independent 8-bit chains
-                    uint32_t m8[4] = {0u, 0u, 0u, 0u};
+                        for (int c = 0; c < 16; c += 2) o |= v0[16 * blk + c] | v0[16 * blk + c + 1];
+                        if (!__any_sync(FULL, rowvalid && (o & 0x80008000u))) continue;
+                        // two 16-column chains; register j holds columns 2j (bit 15)
+                        // and 2j + 1 (bit 31)
+                        uint32_t m16[2] = {0u, 0u};
 #pragma unroll
-                    for (int c = 7; c >= 0; --c)
+                        for (int j = 7; j >= 0; --j)
 #pragma unroll
-                        for (int g = 0; g < 4; ++g) m8[g] = __funnelshift_l(v[8 * g + c], m8[g], 1);
-                    uint32_t mask = m8[0] | (m8[1] << 8) | (m8[2] << 16) | (m8[3] << 24);
+                            for (int g = 0; g < 2; ++g) {
+                                const uint32_t r = v0[16 * blk + 8 * g + j];
+                                m16[g] = __funnelshift_l(r, m16[g], 1);
+                                m16[g] = __funnelshift_l(r << 16, m16[g], 1);
+                            }
+                        mask = m16[0] | (m16[1] << 16);
+                    } else {
+                        uint32_t (&v)[32] = blk ? v1 : v0;
+                        uint32_t o = 0;
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) o |= v[c] | v[c + 1];
+                        if (!__any_sync(FULL, rowvalid && (o >> 31))) continue;
+                        // four independent 8-column chains
+                        uint32_t m8[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                        for (int c = 7; c >= 0; --c)
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) m8[g] = __funnelshift_l(v[8 * g + c], m8[g], 1);
+                        mask = m8[0] | (m8[1] << 8) | (m8[2] << 16) | (m8[3] << 24);
+                    }
                     const int nv = n_cols - qbase;
                     mask &= nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
                     if (!rowvalid) mask = 0;
@@ -582,8 +635,9 @@ template <int MODE, int KIND>
 cudaError_t run_tc(TcArgs a, const Layout &L, cudaStream_t s) {
     // largest operand row this path can need for this eps (the device's choice
     // of threshold digits never exceeds the host's bound)
-    const int kb = tc_kbytes(KIND, L.d, tc_nt_bound(KIND, L.eps2));
-    if (L.umma_tile_bytes == 0 || kb > TC_MAX_KBYTES) return cudaSuccess;   // never selected
+    const int ntb = tc_nt_bound(KIND, L.eps2);
+    const int kb = tc_kbytes(KIND, L.d, ntb);
+    if (L.umma_tile_bytes == 0 || !tc_fits(KIND, L.d, ntb)) return cudaSuccess;   // never selected
     auto kernel = k_sweep_tc<MODE, KIND>;
     const int tile = 128 * kb;
     const int aux = MODE != SWEEP_COUNT ? BT * 4 : 0;
@@ -618,7 +672,8 @@ template <int MODE>
 cudaError_t run_tc_both(const TcArgs &a, const Layout &L, cudaStream_t s) {
     cudaError_t e = run_tc<MODE, TC_TF32>(a, L, s);
     if (e != cudaSuccess) return e;
-    return run_tc<MODE, TC_BF16>(a, L, s);
+    if ((e = run_tc<MODE, TC_BF16>(a, L, s)) != cudaSuccess) return e;
+    return run_tc<MODE, TC_F16>(a, L, s);
 }
 
 }  // namespace

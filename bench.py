@@ -289,9 +289,10 @@ def run_gb300(args, dist: Dist):
     tc_peak = None
     if info["path"] != "fp32":
         bf16 = (peaks or {}).get("bf16_tflops", BF16_FALLBACK_TFLOPS)
-        tc_peak = bf16 if info["path"] == "bf16" else bf16 * TF32_PER_BF16
+        # f16 and bf16 MMAs share the dense rate; tf32 runs at the nominal ratio
+        tc_peak = bf16 if info["path"] in ("bf16", "f16") else bf16 * TF32_PER_BF16
         tc_source = (("measured bf16 burst (MEASURED_PEAKS.json)" if peaks else "recipe fallback bf16") +
-                     ("" if info["path"] == "bf16" else
+                     ("" if info["path"] in ("bf16", "f16") else
                       f" x {TF32_PER_BF16:.3f} (nominal tf32/bf16 ratio 1.1/2.25)"))
     kname = ("count sweep on CUDA cores (fp32 FFMA, upper triangle)" if info["path"] == "fp32" else
              f"count sweep on tensor cores (tcgen05 {info['path']}, K={info['kpad']}, upper triangle)")
@@ -319,7 +320,7 @@ def run_gb300(args, dist: Dist):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {"fp32": "f32", "tf32": "tf32", "bf16": "bf16"}[info["path"]],
+            "dtype": {"fp32": "f32", "tf32": "tf32", "bf16": "bf16", "f16": "f16"}[info["path"]],
             "data": "synthetic",
             "config": {"workload": w.name if args.n is None else f"{w.name} scaled to n={n}",
                        "n": n, "d": d, "eps": w.eps, "min_pts": w.min_pts,

@@ -230,21 +230,27 @@ def test_device_side_errors_and_bad_pointers():
 PATH_CASES = {
     # name: (points, eps, min_pts, dtype, tensor-core paths the data qualifies for)
     "c4_like_12k_d3": (lambda: synth.scaled("blobs_1m_d3", 12_007, seed=31), 10.0, 8, torch.float32,
-                       {"tf32"}),
+                       {"tf32", "f16"}),
     "c2_like_9k_d2": (lambda: synth.scaled("blobs_100k_d2", 9_001, seed=32), 20.0, 10, torch.float32,
-                      {"tf32"}),
+                      {"tf32", "f16"}),
     "c3_like_3k_d16": (lambda: synth.scaled("blobs_200k_d16", 3_001, seed=33), 120.0, 20,
                        torch.float32, {"tf32"}),
     "c5_like_3k_d64": (lambda: synth.scaled("blobs_500k_d64", 2_999, seed=34), 100.0, 16,
                        torch.bfloat16, {"bf16"}),
     "small_box_d3": (lambda: synth.uniform_ints(4_000, 3, 200, 35), 9.0, 6, torch.float32,
-                     {"tf32", "bf16"}),
+                     {"tf32", "bf16", "f16"}),
     "corners_d3": (lambda: (np.random.default_rng(36).integers(0, 2, size=(700, 3)) * 2047)
-                   .astype(np.float32), 2047.0, 5, torch.float32, {"tf32"}),
+                   .astype(np.float32), 2047.0, 5, torch.float32, {"tf32", "f16"}),
+    # d = 10 with two threshold digits fills the f16 path's single K = 16 MMA
+    "d10_two_digits": (lambda: synth.blob_set(3_000, 10, 511, 12, 20.0, 300, 37), 60.0, 4,
+                       torch.float32, {"tf32", "f16"}),
+    # d = 11 no longer fits one K = 16 MMA: f16 is not eligible
+    "d11_blobs": (lambda: synth.blob_set(2_500, 11, 511, 10, 20.0, 250, 38), 60.0, 5,
+                  torch.float32, {"tf32"}),
 }
 
 
-@pytest.mark.parametrize("path", ["fp32", "tf32", "bf16"])
+@pytest.mark.parametrize("path", ["fp32", "tf32", "bf16", "f16"])
 @pytest.mark.parametrize("name", sorted(PATH_CASES))
 def test_parity_every_path(name, path, monkeypatch):
     # the library picks a path per call from the data; forcing one narrows the
@@ -263,10 +269,13 @@ def test_parity_every_path(name, path, monkeypatch):
 
 
 def test_default_path_choice():
-    # without forcing, integer data in a 2048-wide box goes to tf32 tensor
-    # cores, a 256-wide box to bf16, and a wider box stays on CUDA cores
-    for P, expect in ((synth.uniform_ints(3000, 3, 2047, 1), "tf32"),
-                      (synth.uniform_ints(3000, 3, 255, 2), "bf16"),
+    # without forcing, integer data whose operand rows fit one K = 16 MMA go to
+    # f16, other data in a 256-wide box to bf16, in a 2048-wide box to tf32,
+    # and wider or fractional data stays on CUDA cores
+    for P, expect in ((synth.uniform_ints(3000, 3, 2047, 1), "f16"),
+                      (synth.uniform_ints(3000, 3, 255, 2), "f16"),
+                      (synth.uniform_ints(3000, 16, 255, 5), "bf16"),
+                      (synth.uniform_ints(3000, 12, 511, 6), "tf32"),
                       (synth.uniform_ints(3000, 2, 3000, 3), "fp32"),
                       (synth.uniform_ints(3000, 2, 100, 4) + np.float32(0.5), "fp32")):
         info = {}
