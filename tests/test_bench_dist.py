@@ -41,11 +41,12 @@ def test_dist_max_and_barrier_over_two_ranks(tmp_path):
         "d.barrier()\n"
         "v = d.max(10.0 + d.rank)\n"
         "d.barrier()\n"
-        "print(json.dumps({'rank': d.rank, 'max': v}), flush=True)\n"
+        f"open({str(tmp_path)!r} + f'/rank{{d.rank}}.json', 'w').write(json.dumps({{'rank': d.rank, 'max': v}}))\n"
         "d.close()\n")
     r = _torchrun([str(script)])
     assert r.returncode == 0, r.stderr[-2000:]
-    got = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    # each rank writes its own file (two processes share one stdout pipe)
+    got = [json.loads((tmp_path / f"rank{k}.json").read_text()) for k in range(2)]
     assert sorted(g["rank"] for g in got) == [0, 1]
     assert all(g["max"] == 11.0 for g in got)
 
