@@ -184,9 +184,9 @@ static void keep_pool(void) {
 // CUDA-core kernel and one kernel per tensor-core path the shape allows
 // (ntc); all but the path chosen on the device return at once.
 //   prep 4 + 5 locality order (+1 operand staging), count 1 + ntc,
-//   compact 4 (+1 operand staging), union 1 tile-local + 2 waves x
-//   (1 + ntc) + 1 compression, flatten 2, border (+1 operand staging)
-//   1 + ntc, finalize 1.
+//   compact 4 (+1 operand staging), union 1 tile-local + 2 CUDA-core waves
+//   + 1 compression + 6 tensor-core bands x ntc + 5 compressions, flatten 2,
+//   border (+1 operand staging) 1 + ntc, finalize 1.
 static int stage_launches(int d, float eps2, int stage) {
     int ntc = 0;
     for (int kind = TC_TF32; kind <= TC_F16; ++kind)
@@ -196,7 +196,7 @@ static int stage_launches(int d, float eps2, int stage) {
     case 0: return 9 + umma;
     case 1: return 1 + ntc;
     case 2: return 4 + umma;
-    case 3: return 1 + 2 * (1 + ntc) + 1;
+    case 3: return 1 + 2 + 1 + 6 * ntc + 5;
     case 4: return 2;
     case 5: return umma + 1 + ntc;
     default: return 1;

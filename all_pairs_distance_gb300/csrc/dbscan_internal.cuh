@@ -42,7 +42,8 @@ struct Ctrl {
     int tc_nt;          // digits of the threshold constant in the operands
     float ord_lo[3];    // locality order: lower bound of each key axis
     float ord_scale[3]; // locality order: quantisation scale of each key axis
-    int pad1[37];
+    unsigned band_ctr[8];   // work-unit counters of the tensor-core union bands
+    int pad1[29];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl must be 256 bytes");
 
@@ -159,7 +160,9 @@ cudaError_t launch_border(const Work &w, const Layout &L, int32_t *labels, cudaS
 cudaError_t launch_finalize(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
 
 cudaError_t launch_count_tc(const Work &w, const Layout &L, cudaStream_t s);
-cudaError_t launch_union_tc_wave(const Work &w, const Layout &L, int wave, int ulo, int uhi,
+// Tensor-core union over the tile pairs (rb, t) of the upper triangle with
+// blo <= t - rb < bhi (bhi < 0: no upper limit), one work unit per row block.
+cudaError_t launch_union_tc_band(const Work &w, const Layout &L, int band, int blo, int bhi,
                                  cudaStream_t s);
 cudaError_t launch_border_tc(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
 

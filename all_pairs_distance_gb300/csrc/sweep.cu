@@ -45,6 +45,9 @@ constexpr int UNION_WAVES = 2;
 // between waves so that later waves mostly find equal parents in the staged
 // snapshot and never touch global memory.
 static const int kUnionWaveEdges[UNION_WAVES + 1] = {0, 2, -1};
+// Tensor-core union bands: tile distances [edge_b, edge_{b+1}) from the diagonal.
+constexpr int UNION_BANDS = 6;
+static const int kUnionBandEdges[UNION_BANDS + 1] = {0, 2, 4, 8, 16, 32, -1};
 
 struct SweepArgs {
     const float *rows;     // staged row points
@@ -451,8 +454,16 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
 // position of its tile-local component, so that the sweep's staged parent
 // snapshots already carry those roots and the sweep skips such pairs without
 // touching global memory.  Same hit test as the sweep (v_ij < T_i).
+// Find with path halving: parents only ever move towards the root, so a
+// racing write of a grandparent is always a valid ancestor.
 __device__ __forceinline__ int sm_find(volatile int *sp, int x) {
-    for (int it = 0; it < BT && sp[x] != x; ++it) x = sp[x];
+    for (int it = 0; it < BT; ++it) {
+        const int p = sp[x];
+        if (p == x) break;
+        const int gp = sp[p];
+        if (gp != p) sp[x] = gp;
+        x = gp;
+    }
     return x;
 }
 
@@ -498,8 +509,10 @@ __global__ void k_local_union(const Ctrl *ctrl, const float *staged, const float
     }
 }
 
-// Point every core position straight at its root (between union waves).
-__global__ void k_compress(Ctrl *ctrl, int *parent) {
+// Point every core position straight at its root (between union waves);
+// tc = 1 runs only on the tensor-core path, tc = 0 only on the CUDA-core path.
+__global__ void k_compress(Ctrl *ctrl, int *parent, int tc) {
+    if ((ctrl->tc_kind != TC_NONE) != (tc != 0)) return;
     const int n_core = ctrl->n_core;
     for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < n_core; p += gridDim.x * blockDim.x) {
         int r = uf_find(parent, p, ctrl);
@@ -596,16 +609,27 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
     if (lgrid > L.ntiles) lgrid = L.ntiles;
     if (lgrid < 1) lgrid = 1;
     k_local_union<<<(unsigned)lgrid, BT, lsmem, s>>>(w.ctrl, w.staged_core, w.T_core, L.d, w.parent);
+    // CUDA-core path (its kernels return at once when a tensor-core path was chosen)
     for (int wv = 0; wv < UNION_WAVES; ++wv) {
         a.ulo = kUnionWaveEdges[wv];
         a.uhi = kUnionWaveEdges[wv + 1];
         a.ctr = &w.ctrl->unit_ctr[CTR_UNION0 + wv];
         cudaError_t e = dispatch<SWEEP_UNION>(a, L.d, s);
         if (e != cudaSuccess) return e;
-        e = launch_union_tc_wave(w, L, wv, a.ulo, a.uhi, s);
-        if (e != cudaSuccess) return e;
         if (wv + 1 < UNION_WAVES) {
-            k_compress<<<grid, 256, 0, s>>>(w.ctrl, w.parent);
+            k_compress<<<grid, 256, 0, s>>>(w.ctrl, w.parent, 0);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+    }
+    // Tensor-core path by bands of tile distance from the diagonal, nearest
+    // first, compressed between bands: in locality order most neighbour pairs
+    // lie near the diagonal, so the far bands find merged roots in their
+    // staged parent snapshots and skip their pairs without a global access.
+    for (int bd = 0; bd < UNION_BANDS; ++bd) {
+        cudaError_t e = launch_union_tc_band(w, L, bd, kUnionBandEdges[bd], kUnionBandEdges[bd + 1], s);
+        if (e != cudaSuccess) return e;
+        if (bd + 1 < UNION_BANDS) {
+            k_compress<<<grid, 256, 0, s>>>(w.ctrl, w.parent, 1);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
     }

@@ -61,6 +61,7 @@ struct TcArgs {
     const int *n_rows, *n_cols;
     const int *aux;           // per-column int staged with the tiles (parent or label), or null
     int tri, ulo, uhi;
+    int band, blo, bhi;       // band != 0: one unit per row block, tiles rb+blo .. rb+bhi-1
     unsigned *ctr;
     Ctrl *ctrl;
     int *cnt, *parent;
@@ -363,7 +364,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const TcSched sc = tc_sched(n_rows, n_cols, a.tri, a.ulo, a.uhi);
+    TcSched sc = tc_sched(n_rows, n_cols, a.tri, a.ulo, a.uhi);
+    if (a.band) {   // one unit per row block
+        sc.ubegin = 0;
+        sc.uend = (unsigned)sc.nrt;
+    }
 
     if (warp == PRODUCER_WARP) {
         // The whole warp walks the schedule; the copies of consecutive stages
@@ -376,11 +381,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             if (lane == 0) u = sc.ubegin + atomicAdd(a.ctr, 1u);
             u = __shfl_sync(FULL, u, 0);
             if (u >= sc.uend) break;
-            const int rb = (int)(u / sc.kc);
-            const int c = (int)(u % sc.kc);
-            const int t0 = a.tri ? rb + c * sc.uc : c * sc.uc;
-            if (t0 >= sc.nct) continue;
-            const int t1 = min(t0 + sc.uc, sc.nct);
+            int rb, t0, t1;
+            if (a.band) {
+                rb = (int)u;
+                t0 = rb + a.blo;
+                t1 = a.bhi < 0 ? sc.nct : min(sc.nct, rb + a.bhi);
+                if (t0 >= t1) continue;
+            } else {
+                rb = (int)(u / sc.kc);
+                const int c = (int)(u % sc.kc);
+                t0 = a.tri ? rb + c * sc.uc : c * sc.uc;
+                if (t0 >= sc.nct) continue;
+                t1 = min(t0 + sc.uc, sc.nct);
+            }
             const int ab = ua & 1;
             ok = __all_sync(FULL, mbar_spin(smem_addr(&a_empty[ab]), ((ua >> 1) & 1) ^ 1, s_abort, ctrl));
             if (!ok) break;
@@ -687,13 +700,14 @@ cudaError_t launch_count_tc(const Work &w, const Layout &L, cudaStream_t s) {
     return run_tc_both<SWEEP_COUNT>(a, L, s);
 }
 
-cudaError_t launch_union_tc_wave(const Work &w, const Layout &L, int wave, int ulo, int uhi,
+cudaError_t launch_union_tc_band(const Work &w, const Layout &L, int band, int blo, int bhi,
                                  cudaStream_t s) {
     TcArgs a{};
     a.ua = w.ua_core; a.ub = w.ub_core;
     a.n_rows = &w.ctrl->n_core; a.n_cols = &w.ctrl->n_core; a.aux = w.parent;
-    a.tri = 1; a.ulo = ulo; a.uhi = uhi;
-    a.ctr = &w.ctrl->unit_ctr[1 + wave]; a.ctrl = w.ctrl; a.parent = w.parent;
+    a.tri = 1; a.ulo = 0; a.uhi = -1;
+    a.band = 1; a.blo = blo; a.bhi = bhi;
+    a.ctr = &w.ctrl->band_ctr[band]; a.ctrl = w.ctrl; a.parent = w.parent;
     return run_tc_both<SWEEP_UNION>(a, L, s);
 }
 
