@@ -60,6 +60,8 @@ def load():
         lib.dbscan_fit.restype = ctypes.c_int
         lib.dbscan_fit_ex.argtypes = [P, i32, i64, i32, f32, i32, P, P, P, sz, P]
         lib.dbscan_fit_ex.restype = ctypes.c_int
+        lib.dbscan_fit_culled.argtypes = [P, i32, i64, i32, f32, i32, P, P, P, sz, P]
+        lib.dbscan_fit_culled.restype = ctypes.c_int
         lib.dbscan_fit_host.argtypes = [P, i32, i64, i32, f32, i32, P, P, P]
         lib.dbscan_fit_host.restype = ctypes.c_int
         lib.dbscan_neighbor_counts.argtypes = [P, i32, i64, i32, f32, P, P, sz, P]
@@ -143,6 +145,24 @@ def dbscan_fit_ex(points: torch.Tensor, eps: float, min_pts: int, *, labels=None
                                 workspace.numel(), _stream_handle(stream)), "dbscan_fit_ex")
     return labels, is_core
 
+
+
+def dbscan_fit_culled(points: torch.Tensor, eps: float, min_pts: int, *, labels=None,
+                  is_core=None, workspace=None, stream=None):
+    """dbscan_fit_ex with tile culling (tile pairs whose bounding boxes are eps
+    or more apart are skipped; identical results for exact data, d <= 8)."""
+    p = _points(points)
+    n, d = p.shape
+    if labels is None:
+        labels = torch.empty(n, dtype=torch.int32, device=p.device)
+    if is_core is None:
+        is_core = torch.empty(n, dtype=torch.uint8, device=p.device)
+    if workspace is None:
+        workspace = workspace_for(p)
+    _check(load().dbscan_fit_culled(p.data_ptr(), DTYPES[p.dtype], n, d, float(eps), int(min_pts),
+                                labels.data_ptr(), is_core.data_ptr(), workspace.data_ptr(),
+                                workspace.numel(), _stream_handle(stream)), "dbscan_fit_culled")
+    return labels, is_core
 
 def dbscan_neighbor_counts(points: torch.Tensor, eps: float, *, out=None, workspace=None,
                            stream=None):

@@ -77,6 +77,11 @@ Layout make_layout(int64_t n, int32_t d) {
     L.off_bstart = off;      off += align256(nbins * sizeof(int));
     L.off_btot = off;        off += align256((nbins / 1024 + 1) * sizeof(int));
     L.off_rootmin = off;     off += align256(per_pt);
+    // tile bounding boxes for culling (three arrays: all, core, candidates)
+    L.box_floats = d <= CULL_MAX_D ? (size_t)L.ntiles * 2 * d : 0;
+    L.off_box_all = off;     off += align256(L.box_floats * sizeof(float));
+    L.off_box_core = off;    off += align256(L.box_floats * sizeof(float));
+    L.off_box_cand = off;    off += align256(L.box_floats * sizeof(float));
     L.total = off;
     return L;
 }
@@ -129,6 +134,9 @@ Work carve(void *base, const Layout &L) {
     w.bstart = reinterpret_cast<int *>(b + L.off_bstart);
     w.btot = reinterpret_cast<int *>(b + L.off_btot);
     w.rootmin = reinterpret_cast<int *>(b + L.off_rootmin);
+    w.box_all = reinterpret_cast<float *>(b + L.off_box_all);
+    w.box_core = reinterpret_cast<float *>(b + L.off_box_core);
+    w.box_cand = reinterpret_cast<float *>(b + L.off_box_cand);
     return w;
 }
 
@@ -208,6 +216,7 @@ struct ProfCall {
     int stages;   // number of stages the call ran
     int d;        // dimension of the call (sets the kernels per stage)
     float eps2;   // eps^2 of the call (sets the tensor-core kinds launched)
+    int cull;     // tile culling on (adds the box kernels)
 };
 struct ProfState {
     bool on = false;
@@ -220,9 +229,10 @@ struct StageMarks {
     ProfCall call{};
     bool on = false;
     int next = 0;
-    StageMarks(cudaStream_t s, int d, float eps2) {
+    StageMarks(cudaStream_t s, int d, float eps2, int cull) {
         call.d = d;
         call.eps2 = eps2;
+        call.cull = cull;
         if (!g_prof.on) return;
         for (int i = 0; i <= DBSCAN_NUM_STAGES; ++i) {
             if (cudaEventCreate(&call.ev[i]) != cudaSuccess) {
@@ -252,11 +262,12 @@ static int run(const void *points, int dtype, int64_t n, int d, float eps, int m
                int32_t *labels, uint8_t *is_core, int32_t *cnt_out, void *ws, const Layout &L,
                cudaStream_t s) {
     Work w = carve(ws, L);
-    StageMarks marks(s, d, L.eps2);
+    StageMarks marks(s, d, L.eps2, L.cull);
     if (cudaMemsetAsync(w.ctrl, 0, sizeof(Ctrl), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     if (cudaMemsetAsync(w.cnt, 0, (size_t)n * sizeof(int), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     if (launch_prep(points, dtype, n, d, eps, allowed_tc(d, L.eps2), w, L, s) != cudaSuccess)
         return DBSCAN_ERR_CUDA;
+    if (L.cull && launch_tile_boxes(w, L, 0, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     marks.mark(s);
     if (launch_count(w, L, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     marks.mark(s);
@@ -265,6 +276,9 @@ static int run(const void *points, int dtype, int64_t n, int d, float eps, int m
         return DBSCAN_OK;
     }
     if (launch_compact(w, L, min_pts, labels, is_core, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+    if (L.cull && (launch_tile_boxes(w, L, 1, s) != cudaSuccess ||
+                   launch_tile_boxes(w, L, 2, s) != cudaSuccess))
+        return DBSCAN_ERR_CUDA;
     marks.mark(s);
     if (launch_union(w, L, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     marks.mark(s);
@@ -290,7 +304,7 @@ static int read_status(const void *ws, cudaStream_t s) {
 // Shared body of dbscan_fit_ex and dbscan_neighbor_counts.
 static int fit_common(const void *points, int32_t dtype, int64_t n, int32_t d, float eps,
                       int32_t min_pts, int32_t *labels, uint8_t *is_core, int32_t *cnt_out,
-                      void *workspace, size_t workspace_bytes, void *stream) {
+                      void *workspace, size_t workspace_bytes, void *stream, int cull = 0) {
     int st = check_shape(n, d, dtype);
     if (st != DBSCAN_OK) return st;
     if ((st = check_scalars(eps, min_pts)) != DBSCAN_OK) return st;
@@ -299,6 +313,7 @@ static int fit_common(const void *points, int32_t dtype, int64_t n, int32_t d, f
     if (!cnt_out && (!labels || !is_core)) return DBSCAN_ERR_INVALID_ARG;
     Layout L = make_layout(n, d);
     L.eps2 = eps * eps;
+    L.cull = cull && L.box_floats > 0 && L.umma_tile_bytes > 0;
     if (workspace) {
         if (workspace_bytes < L.total) return DBSCAN_ERR_INVALID_ARG;
         if (reinterpret_cast<uintptr_t>(workspace) & 255) return DBSCAN_ERR_INVALID_ARG;
@@ -360,6 +375,13 @@ int dbscan_fit_ex(const void *points, int32_t dtype, int64_t n, int32_t d, float
                       workspace, workspace_bytes, stream);
 }
 
+int dbscan_fit_culled(const void *points, int32_t dtype, int64_t n, int32_t d, float eps,
+                      int32_t min_pts, int32_t *labels_out, uint8_t *is_core_out, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    return fit_common(points, dtype, n, d, eps, min_pts, labels_out, is_core_out, nullptr,
+                      workspace, workspace_bytes, stream, 1);
+}
+
 int dbscan_fit(const float *points, int64_t n, int32_t d, float eps, int32_t min_pts,
                int32_t *labels_out, uint8_t *is_core_out) {
     return fit_common(points, DBSCAN_F32, n, d, eps, min_pts, labels_out, is_core_out, nullptr,
@@ -405,7 +427,7 @@ int dbscan_profile_end(float *stage_ms, int32_t max_stages, int64_t *calls,
                 cudaEventElapsedTime(&ms, c.ev[i], c.ev[i + 1]) != cudaSuccess)
                 st = DBSCAN_ERR_CUDA;
             acc[i] += ms;
-            launches += stage_launches(c.d, c.eps2, i);
+            launches += stage_launches(c.d, c.eps2, i) + (c.cull ? (i == 0 ? 1 : (i == 2 ? 2 : 0)) : 0);
         }
         for (int i = 0; i <= c.stages; ++i) cudaEventDestroy(c.ev[i]);
     }

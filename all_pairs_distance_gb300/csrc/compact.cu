@@ -13,6 +13,8 @@
 // position p maps to the caller's numbering through perm[p].
 #include "dbscan_internal.cuh"
 
+#include <math.h>
+
 namespace dbscan {
 
 constexpr int CT_THREADS = 256;
@@ -147,6 +149,46 @@ __global__ void k_scatter(const int *cnt, const int *perm, int64_t n, int d, int
         off_cand += td;
         __syncthreads();
     }
+}
+
+// Bounding box of every tile of a staged array (min and max of each centred
+// coordinate over the tile's valid points): one block of BT threads per tile.
+__global__ void k_tile_boxes(const float *staged, const int *count, int d, float *box) {
+    __shared__ float red[2][BT / 32];
+    const int t = blockIdx.x, lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int cnt = *count;
+    if ((int64_t)t * BT >= cnt) return;
+    const bool valid = (int64_t)t * BT + threadIdx.x < cnt;
+    const float *src = staged + (size_t)t * (size_t)(d + 1) * BT + threadIdx.x;
+    for (int k = 0; k < d; ++k) {
+        const float v = src[(size_t)k * BT];
+        float lo = valid ? v : INFINITY, hi = valid ? v : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        if (lane == 0) { red[0][wid] = lo; red[1][wid] = hi; }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int w2 = 1; w2 < BT / 32; ++w2) {
+                lo = fminf(lo, red[0][w2]);
+                hi = fmaxf(hi, red[1][w2]);
+            }
+            box[((size_t)t * d + k) * 2] = lo;
+            box[((size_t)t * d + k) * 2 + 1] = hi;
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_tile_boxes(const Work &w, const Layout &L, int which, cudaStream_t s) {
+    if (L.box_floats == 0) return cudaSuccess;
+    const float *st = which == 0 ? w.staged_all : (which == 1 ? w.staged_core : w.staged_cand);
+    const int *cnt = which == 0 ? &w.ctrl->n_all : (which == 1 ? &w.ctrl->n_core : &w.ctrl->n_cand);
+    float *box = which == 0 ? w.box_all : (which == 1 ? w.box_core : w.box_cand);
+    k_tile_boxes<<<(unsigned)L.ntiles, BT, 0, s>>>(st, cnt, L.d, box);
+    return cudaGetLastError();
 }
 
 // Padding slots of the last tile of the core and candidate arrays.

@@ -17,6 +17,9 @@ namespace dbscan {
 // the BT squared norms: (d + 1) * BT floats, 512-byte aligned rows.
 constexpr int BT = 128;
 constexpr int SCAN_BLOCK = 1024;   // elements per block of the compaction scan
+// Tile culling (dbscan_fit_culled) keeps per-tile bounding boxes for d up to
+// this dimension; beyond it the boxes prune little and the call runs unculled.
+constexpr int CULL_MAX_D = 8;
 
 // Sentinels for the padding slots of the last tile: a padding column has a
 // huge norm and never tests as a neighbour; a padding row has a hugely
@@ -61,6 +64,9 @@ struct Layout {
     size_t off_ua_all, off_ub_all, off_ua_core, off_ub_core, off_ua_cand;
     int order_bits;       // bins of the locality order: 2^order_bits
     size_t off_bin, off_perm, off_hist, off_bstart, off_btot, off_rootmin;
+    int cull;             // 1: this call skips tile pairs whose boxes are eps apart
+    size_t box_floats;    // floats of one box array (ntiles x 2d), 0 when d > CULL_MAX_D
+    size_t off_box_all, off_box_core, off_box_cand;
     int64_t nscan_blocks;
     size_t total;
 };
@@ -87,6 +93,7 @@ struct Work {
     int *hist, *bstart;   // [2^order_bits] bin counts and bin starts
     int *btot;            // [2^order_bits / 1024] bin-block offsets
     int *rootmin;         // [n] smallest input index of each union-find root's component
+    float *box_all, *box_core, *box_cand;   // [ntiles][d][min, max] tile bounding boxes
 };
 
 Work carve(void *base, const Layout &L);
@@ -148,6 +155,7 @@ cudaError_t launch_order(const void *points, int dtype, int64_t n, int d, const 
                          const Layout &L, cudaStream_t s);
 cudaError_t launch_unpermute_counts(const Work &w, const Layout &L, int32_t *cnt_out,
                                     cudaStream_t s);
+cudaError_t launch_tile_boxes(const Work &w, const Layout &L, int which, cudaStream_t s);
 cudaError_t launch_prep(const void *points, int dtype, int64_t n, int d, float eps, int allow_tc,
                         const Work &w, const Layout &L, cudaStream_t s);
 cudaError_t launch_stage_umma(const Work &w, const Layout &L, int which, cudaStream_t s);

@@ -54,7 +54,7 @@ constexpr int ISSUE_LANES = 8;          // producer lanes that take turns issuin
 constexpr long long WAIT_LIMIT = 8000000000LL;   // clock cycles (about 4 s)
 constexpr int UF_CAP = 1 << 22;
 
-constexpr int F_FIRST = 1, F_LAST = 2, F_DIAG = 4, F_TERM = 8;
+constexpr int F_FIRST = 1, F_TERM = 8;
 
 struct TcArgs {
     const uint8_t *ua, *ub;   // row / column operand tiles, packed 128 x kbytes each
@@ -62,6 +62,8 @@ struct TcArgs {
     const int *aux;           // per-column int staged with the tiles (parent or label), or null
     int tri, ulo, uhi;
     int band, blo, bhi;       // band != 0: one unit per row block, tiles rb+blo .. rb+bhi-1
+    const float *rbox, *cbox; // per-tile bounding boxes of rows / columns (d x (min, max))
+    int cull, d;              // cull != 0: skip column tiles whose box is eps or more away
     unsigned *ctr;
     Ctrl *ctrl;
     int *cnt, *parent;
@@ -376,6 +378,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         // complete one after another.
         int k = 0, ua = 0, a_issued = 0;
         bool ok = true;
+        // Culling by tile boxes is exact for integer data within the exactness
+        // bound: box gaps are integers, their squared sum is exact, and every
+        // pair of a culled tile pair has d^2 >= that sum >= thrx (not a neighbour).
+        const bool cull = a.cull && ctrl->exact && a.rbox && a.cbox;
+        const float cthr = ctrl->thrx;
         for (;;) {
             unsigned u = 0;
             if (lane == 0) u = sc.ubegin + atomicAdd(a.ctr, 1u);
@@ -395,42 +402,83 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                 t1 = min(t0 + sc.uc, sc.nct);
             }
             const int ab = ua & 1;
-            ok = __all_sync(FULL, mbar_spin(smem_addr(&a_empty[ab]), ((ua >> 1) & 1) ^ 1, s_abort, ctrl));
-            if (!ok) break;
-            if (lane == ISSUE_LANES + (ua % ISSUE_LANES)) {
-                mbar_expect_tx(smem_addr(&a_full[ab]), tile_bytes);
-                bulk_g2s(smem_addr(sA + (size_t)ab * a.tile_bytes_max),
-                         a.ua + (size_t)rb * tile_bytes, tile_bytes, smem_addr(&a_full[ab]));
-            }
-            a_issued = ua + 1;
-            for (int tf = t0; tf < t1; tf += G) {
-                const int s = k % S;
-                const int nt = min(G, t1 - tf);
-                ok = __all_sync(FULL, mbar_spin(smem_addr(&b_empty[s]), ((k / S) & 1) ^ 1, s_abort, ctrl));
-                if (!ok) break;
-                if (lane == 0) {
-                    Meta m;
-                    m.rb = rb;
-                    m.t_first = tf;
-                    m.ntiles = nt;
-                    m.flags = (tf == t0 ? F_FIRST : 0) | (tf + nt == t1 ? F_LAST : 0);
-                    m.abuf = ab;
-                    meta[s] = m;
+            bool started = false;   // this unit's row tile has been loaded
+            // Stages of up to G consecutive tiles over [ts, te); the unit's row
+            // tile is loaded before its first stage, so a unit whose column
+            // tiles are all culled costs nothing.
+            auto emit = [&](int ts, int te) -> bool {
+                for (int tf = ts; tf < te; tf += G) {
+                    bool first = false;
+                    if (!started) {
+                        if (!__all_sync(FULL, mbar_spin(smem_addr(&a_empty[ab]), ((ua >> 1) & 1) ^ 1,
+                                                        s_abort, ctrl)))
+                            return false;
+                        if (lane == ISSUE_LANES + (ua % ISSUE_LANES)) {
+                            mbar_expect_tx(smem_addr(&a_full[ab]), tile_bytes);
+                            bulk_g2s(smem_addr(sA + (size_t)ab * a.tile_bytes_max),
+                                     a.ua + (size_t)rb * tile_bytes, tile_bytes, smem_addr(&a_full[ab]));
+                        }
+                        a_issued = ua + 1;
+                        started = first = true;
+                    }
+                    const int s = k % S;
+                    const int nt = min(G, te - tf);
+                    if (!__all_sync(FULL, mbar_spin(smem_addr(&b_empty[s]), ((k / S) & 1) ^ 1, s_abort, ctrl)))
+                        return false;
+                    if (lane == 0) {
+                        Meta m;
+                        m.rb = rb;
+                        m.t_first = tf;
+                        m.ntiles = nt;
+                        m.flags = first ? F_FIRST : 0;
+                        m.abuf = ab;
+                        meta[s] = m;
+                    }
+                    __syncwarp();
+                    if (lane == k % ISSUE_LANES) {
+                        uint8_t *dst = sStage + (size_t)s * a.stage_bytes;
+                        mbar_expect_tx(smem_addr(&b_full[s]),
+                                       (uint32_t)nt * tile_bytes + (AUX ? (uint32_t)nt * BT * 4u : 0u));
+                        bulk_g2s(smem_addr(dst), a.ub + (size_t)tf * tile_bytes, (uint32_t)nt * tile_bytes,
+                                 smem_addr(&b_full[s]));
+                        if (AUX)
+                            bulk_g2s(smem_addr(dst + (size_t)G * a.tile_bytes_max), a.aux + (size_t)tf * BT,
+                                     (uint32_t)nt * BT * 4u, smem_addr(&b_full[s]));
+                    }
+                    ++k;
                 }
-                __syncwarp();
-                if (lane == k % ISSUE_LANES) {
-                    uint8_t *dst = sStage + (size_t)s * a.stage_bytes;
-                    mbar_expect_tx(smem_addr(&b_full[s]),
-                                   (uint32_t)nt * tile_bytes + (AUX ? (uint32_t)nt * BT * 4u : 0u));
-                    bulk_g2s(smem_addr(dst), a.ub + (size_t)tf * tile_bytes, (uint32_t)nt * tile_bytes,
-                             smem_addr(&b_full[s]));
-                    if (AUX)
-                        bulk_g2s(smem_addr(dst + (size_t)G * a.tile_bytes_max), a.aux + (size_t)tf * BT,
-                                 (uint32_t)nt * BT * 4u, smem_addr(&b_full[s]));
+                return true;
+            };
+            if (!cull) {
+                ok = emit(t0, t1);
+            } else {
+                // each lane tests one column tile of a 32-tile window against the
+                // row tile's box; runs of kept tiles become stages
+                const float *rbx = a.rbox + (size_t)rb * 2 * a.d;
+                for (int w0 = t0; w0 < t1 && ok; w0 += 32) {
+                    const int tt = w0 + lane;
+                    bool keep = false;
+                    if (tt < t1) {
+                        const float *cbx = a.cbox + (size_t)tt * 2 * a.d;
+                        float g2 = 0.f;
+                        for (int kk = 0; kk < a.d; ++kk) {
+                            const float g = fmaxf(0.f, fmaxf(cbx[2 * kk] - rbx[2 * kk + 1],
+                                                             rbx[2 * kk] - cbx[2 * kk + 1]));
+                            g2 = fmaf(g, g, g2);
+                        }
+                        keep = g2 < cthr;   // some pair could be a neighbour
+                    }
+                    unsigned km = __ballot_sync(FULL, keep);
+                    while (km && ok) {
+                        const int s0 = __ffs(km) - 1;
+                        const unsigned gaps = ~(km >> s0);
+                        const int len = gaps ? __ffs(gaps) - 1 : 32 - s0;
+                        km = (s0 + len >= 32) ? 0u : (km & (0xffffffffu << (s0 + len)));
+                        ok = emit(w0 + s0, w0 + s0 + len);
+                    }
                 }
-                ++k;
             }
-            ++ua;
+            if (started) ++ua;
             if (!ok) break;
         }
         if (ok) {   // terminate marker (every consumer reads every stage)
@@ -458,8 +506,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                 if (!mbar_spin(smem_addr(&b_full[s]), (k / S) & 1, s_abort, ctrl)) break;
                 const Meta m = meta[s];
                 if (m.flags & F_TERM) break;
-                if (m.flags & F_FIRST)
+                if (m.flags & F_FIRST) {
+                    // the previous unit's row tile has been read by every MMA issued so far
+                    if (ua > 0) umma_commit(smem_addr(&a_empty[(ua - 1) & 1]));
                     if (!mbar_spin(smem_addr(&a_full[m.abuf]), (ua >> 1) & 1, s_abort, ctrl)) break;
+                    ++ua;
+                }
                 const uint32_t abase = smem_addr(sA + (size_t)m.abuf * a.tile_bytes_max);
                 const uint32_t sbase = smem_addr(sStage + (size_t)s * a.stage_bytes);
                 for (int i = 0; 2 * i < m.ntiles; ++i, ++it) {
@@ -477,10 +529,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                     umma_commit(smem_addr(&acc_full[b]));
                 }
                 if (!ok) break;
-                if (m.flags & F_LAST) {
-                    umma_commit(smem_addr(&a_empty[m.abuf]));
-                    ++ua;
-                }
+
                 ++k;
             }
             if (issued) {   // no MMA may be in flight when TMEM is freed
@@ -697,6 +746,7 @@ cudaError_t launch_count_tc(const Work &w, const Layout &L, cudaStream_t s) {
     a.n_rows = &w.ctrl->n_all; a.n_cols = &w.ctrl->n_all;
     a.tri = 1; a.ulo = 0; a.uhi = -1;
     a.ctr = &w.ctrl->unit_ctr[0]; a.ctrl = w.ctrl; a.cnt = w.cnt;
+    a.rbox = w.box_all; a.cbox = w.box_all; a.cull = L.cull; a.d = L.d;
     return run_tc_both<SWEEP_COUNT>(a, L, s);
 }
 
@@ -708,6 +758,7 @@ cudaError_t launch_union_tc_band(const Work &w, const Layout &L, int band, int b
     a.tri = 1; a.ulo = 0; a.uhi = -1;
     a.band = 1; a.blo = blo; a.bhi = bhi;
     a.ctr = &w.ctrl->band_ctr[band]; a.ctrl = w.ctrl; a.parent = w.parent;
+    a.rbox = w.box_core; a.cbox = w.box_core; a.cull = L.cull; a.d = L.d;
     return run_tc_both<SWEEP_UNION>(a, L, s);
 }
 
@@ -718,6 +769,7 @@ cudaError_t launch_border_tc(const Work &w, const Layout &L, int32_t *labels, cu
     a.tri = 0; a.ulo = 0; a.uhi = -1;
     a.ctr = &w.ctrl->unit_ctr[5]; a.ctrl = w.ctrl;
     a.candidx = w.candidx; a.labels = labels;
+    a.rbox = w.box_cand; a.cbox = w.box_core; a.cull = L.cull; a.d = L.d;
     return run_tc_both<SWEEP_BORDER>(a, L, s);
 }
 

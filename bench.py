@@ -50,6 +50,7 @@ def parse():
                     help="run a smaller set drawn like the workload (profiling cases only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-culled", action="store_true")
     return ap.parse_args()
 
 
@@ -331,6 +332,37 @@ def run_gb300(args, dist: Dist):
             "exact": info["exact"],
             "count_pair_evals_per_s": float(n) * n / (count_ms * 1e-3),
             "roofline": roofline, "gpu_launches": launches, "clocks": clk}
+
+    # Tile culling (dbscan_fit_culled), reported beside the headline: same
+    # results, but pairs in tiles whose boxes are eps apart are never
+    # evaluated, so its time is not an all-pairs figure.
+    if not args.no_culled:
+        def step_culled():
+            binding.dbscan_fit_culled(x, w.eps, w.min_pts, labels=labels, is_core=is_core,
+                                      workspace=ws, stream=stream)
+        for _ in range(args.warmup):
+            flush.zero_()
+            step_culled()
+        cs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ce = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        dist.barrier()
+        for k in range(args.steps):
+            flush.zero_()
+            cs[k].record(stream)
+            step_culled()
+            ce[k].record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        st = binding.dbscan_workspace_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {binding.dbscan_strerror(st)}")
+        c_ms = dist.max(sum(a.elapsed_time(b) for a, b in zip(cs, ce)) / args.steps)
+        line["culled"] = {"ms_per_step": c_ms, "speedup_vs_all_pairs": mean_ms / c_ms,
+                          "api": "dbscan_fit_culled",
+                          "note": "tile pairs whose bounding boxes are eps apart are skipped "
+                                  "(identical labels); not an all-pairs evaluation, so no "
+                                  "pair-evals/s figure"}
 
     if not args.no_e2e:
         ph = torch.from_numpy(P).to(dtype).pin_memory()

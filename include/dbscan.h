@@ -108,6 +108,24 @@ int dbscan_fit_ex(const void *points, int32_t dtype, int64_t n, int32_t d,
                   size_t workspace_bytes, void *stream);
 
 /*
+ * dbscan_fit_ex with tile culling: the same arguments, workspace and error
+ * behaviour, and the same labels and core flags.  The sweeps skip every pair
+ * of 128-point tiles whose bounding boxes (of the points in the library's
+ * locality order) are eps or more apart: no pair in such tiles can be a
+ * neighbour, so for integer data within the exactness bound the result is
+ * identical to dbscan_fit_ex.  This is not an all-pairs evaluation (pairs in
+ * skipped tiles are never evaluated), which is why it is a separate entry
+ * point.  Culling applies on the tensor-core paths for d <= 8 and exact data;
+ * otherwise the call runs exactly as dbscan_fit_ex.  The pages evaluate all
+ * pairs ("Design and optimization of DBSCAN Algorithm based on CUDA", §IV-A);
+ * pruning by spatial bounds is not on them.
+ */
+int dbscan_fit_culled(const void *points, int32_t dtype, int64_t n, int32_t d,
+                      float eps, int32_t min_pts, int32_t *labels_out,
+                      uint8_t *is_core_out, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/*
  * Full DBSCAN on HOST buffers: copies points in, runs, copies the results
  * out and synchronises `stream`.  Device memory is allocated stream-ordered
  * for the call and freed before returning.  Host buffers may be pageable or

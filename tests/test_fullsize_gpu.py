@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from all_pairs_distance_gb300 import synth
+from all_pairs_distance_gb300 import binding, synth
 from gpu_util import assert_same, check_sampled, gpu_run, kdtree_dbscan
 
 pytestmark = pytest.mark.gpu
@@ -66,3 +66,15 @@ def test_full_exact_1m_d3_against_kdtree_dbscan():
     assert_same(cnt, cnt_ref, "counts")
     assert_same(core, core_ref, "core")
     assert_same(label, label_ref, "labels")
+
+
+def test_culled_equals_all_pairs_at_1m_d3():
+    # the bench workload: tile culling must not change a single label or flag
+    P = synth.generate("blobs_1m_d3")
+    x = torch.from_numpy(P).cuda()
+    ws = binding.workspace_for(x)
+    lab_a, core_a = binding.dbscan_fit_ex(x, 10.0, 8, workspace=ws)
+    assert binding.dbscan_workspace_status(ws) == 0
+    lab_c, core_c = binding.dbscan_fit_culled(x, 10.0, 8, workspace=ws)
+    assert binding.dbscan_workspace_status(ws) == 0
+    assert torch.equal(lab_a, lab_c) and torch.equal(core_a, core_c)

@@ -281,3 +281,42 @@ def test_default_path_choice():
         info = {}
         gpu_run(P, 4.0, 3, info=info, counts=False)
         assert info["path"] == expect, (expect, info)
+
+
+def gpu_run_culled(P, eps, min_pts, dtype=torch.float32):
+    x = torch.from_numpy(np.ascontiguousarray(P)).to("cuda").to(dtype)
+    ws = binding.workspace_for(x)
+    labels, core = binding.dbscan_fit_culled(x, eps, min_pts, workspace=ws)
+    st = binding.dbscan_workspace_status(ws)
+    assert st == 0, binding.dbscan_strerror(st)
+    return core.cpu().numpy(), labels.cpu().numpy()
+
+
+CULL_CASES = {
+    # tile culling engages (integer data, d <= 8) or must leave results untouched
+    "c1_full_2k_d2": (lambda: synth.generate("blobs_2k_d2"), 30.0, 5, torch.float32),
+    "c2_like_20k_d2": (lambda: synth.scaled("blobs_100k_d2", 20_000, seed=41), 20.0, 10, torch.float32),
+    "c4_like_20k_d3": (lambda: synth.scaled("blobs_1m_d3", 20_011, seed=42), 10.0, 8, torch.float32),
+    "d8_blobs": (lambda: _blobs(6_000, 8, 255, 12, 6.0, 600, 43), 14.0, 5, torch.float32),
+    "d1_blobs": (lambda: _blobs(4_100, 1, 4095, 6, 30.0, 400, 44), 2.0, 4, torch.float32),
+    "corners_d3": (lambda: (np.random.default_rng(45).integers(0, 2, size=(700, 3)) * 2047)
+                   .astype(np.float32), 2047.0, 5, torch.float32),
+    "d16_no_cull": (lambda: synth.scaled("blobs_200k_d16", 4_001, seed=46), 120.0, 20, torch.float32),
+    "fractional_no_cull": (lambda: synth.scaled("blobs_1m_d3", 5_003, seed=47) * np.float32(0.5),
+                           5.0, 8, torch.float32),
+}
+
+
+@pytest.mark.parametrize("path", ["default", "tf32", "bf16", "fp32"])
+@pytest.mark.parametrize("name", sorted(CULL_CASES))
+def test_culled_matches_oracle(name, path, monkeypatch):
+    if path == "default":
+        monkeypatch.delenv("DBSCAN_FORCE_PATH", raising=False)
+    else:
+        monkeypatch.setenv("DBSCAN_FORCE_PATH", path)
+    make, eps, min_pts, dtype = CULL_CASES[name]
+    P = make()
+    _, core_ref, label_ref = oracle.dbscan(P, eps, min_pts)
+    core, label = gpu_run_culled(P, eps, min_pts, dtype)
+    assert_same(core, core_ref, f"{name} [{path}] culled core flags")
+    assert_same(label, label_ref, f"{name} [{path}] culled labels")
