@@ -19,7 +19,8 @@
 // page's form overflows 2^24 already at d = 3 over [0, 2047].
 //
 // Tensor-core operands.  When every centred coordinate is an integer small
-// enough for the MMA input type (|2c| <= 2048 for tf32 and f16, <= 256 for bf16), the
+// enough for the MMA input type (|2c| <= 2048 for tf32 and f16, <= 256 for
+// bf16), the
 // pair quantity w_ij = |c_i - c_j|^2 - thrx is written as one dot product
 //     A_i = [-2 c_i,  1, B, ..,   n0_i, n1_i, ..,  -h0, -h1, ..]
 //     B_j = [   c_j,  n0_j, n1_j, .., 1, B, ..,     1,   B, ..]
@@ -27,7 +28,10 @@
 // every element exactly representable.  The positive terms sum to at most
 // 4 S and the negative ones to at most 2 S + thrx (S = sum_k M_k^2); when both
 // are below 2^24 every partial sum the tensor core forms, in any order, is an
-// exact integer, and w_ij < 0 <=> neighbour.
+// exact integer, and w_ij < 0 <=> neighbour.  The f16 kind is used only when
+// the whole row fits one K = 16 MMA: its f16 accumulator then rounds the exact
+// sum once, which keeps the sign (the smallest nonzero |w| is 1; overflow gives
+// +-inf; an exact zero is stored as +0).
 #include "dbscan_internal.cuh"
 
 #include <math.h>

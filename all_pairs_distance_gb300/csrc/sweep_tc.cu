@@ -3,22 +3,26 @@
 //
 // The squared distance is a dense contraction once the point-only terms are
 // hoisted ("Design and optimization of DBSCAN Algorithm based on CUDA",
-// §IV-B2).  prep.cu writes each point as a tf32 or bf16 operand row whose dot
-// product with another point's row is exactly w_ij = |c_i - c_j|^2 - thrx, so
-// one 128 x 128 x K MMA evaluates a whole tile and a pair is a neighbour iff
+// §IV-B2).  prep.cu writes each point as a tf32, bf16 or f16 operand row whose
+// dot product with another point's row is exactly w_ij = |c_i - c_j|^2 - thrx,
+// so one 128 x 256 x K MMA evaluates two tiles and a pair is a neighbour iff
 // w_ij < 0.  The CUDA cores only read the accumulator and test signs.
 //
 // CTA = 18 warps, one per SM (the CTA owns all 512 TMEM columns):
-//   warp 16     producer: pulls work units and bulk-copies (cp.async.bulk) the
-//               row operand tile of a unit and groups of up to 32 consecutive
-//               column tiles (plus their aux ints) into a ring of shared-memory
-//               stages; lanes take turns issuing, since the bulk copies of one
-//               thread complete one after another;
+//   warp 16     producer: pulls work units (a row block and a run of column
+//               tiles; for the union, one row block per band of tile distances)
+//               and bulk-copies (cp.async.bulk) the unit's row operand tile and
+//               groups of up to 32 consecutive column tiles (plus their aux
+//               ints) into a ring of shared-memory stages; lanes take turns
+//               issuing, since the bulk copies of one thread complete one after
+//               another.  With tile culling it streams only the column tiles
+//               whose bounding boxes are within eps of the row tile's;
 //   warp 17     MMA: one thread issues a 128 x 256 x K MMA per pair of column
 //               tiles into one of two 256-column TMEM accumulators and commits
 //               completion to mbarriers;
 //   warps 0-15  epilogue: every warp reads every tile pair, 32 rows x 64
-//               columns (two tcgen05.ld), and frees the accumulator before it
+//               columns (two tcgen05.ld, or one packed load of an f16
+//               accumulator), and frees the accumulator before it
 //               tests anything -- the accumulator round trip is bound by how
 //               fast TMEM is drained, and TMEM read bandwidth grows with the
 //               number of warps loading.  A warp ORs the sign bits of its 64
@@ -529,7 +533,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                     umma_commit(smem_addr(&acc_full[b]));
                 }
                 if (!ok) break;
-
                 ++k;
             }
             if (issued) {   // no MMA may be in flight when TMEM is freed

@@ -32,10 +32,11 @@
  * clusters joins; the answers above are the readings this library takes.
  *
  * Exactness: when every coordinate is an integer and sum_k (max_k - min_k)^2
- * over the data's per-dimension ranges is below 2^24, every quantity the
- * kernels form is an integer below 2^24 and the results are exact (identical
- * to a double-precision evaluation).  Otherwise pairs within float32 rounding
- * of the eps boundary may be classified either way.
+ * over the data's per-dimension ranges is below 2^24, every sum the kernels
+ * form is an integer below 2^24 (the f16 tensor-core path rounds its final
+ * sum once, which keeps its sign, the only thing read) and the results are
+ * exact (identical to a double-precision evaluation).  Otherwise pairs within
+ * float32 rounding of the eps boundary may be classified either way.
  *
  * Memory: every pointer argument is a DEVICE pointer unless the entry point's
  * name ends in _host.  The caller owns all buffers; the library never frees
@@ -192,7 +193,7 @@ int dbscan_workspace_status(const void *workspace, void *stream);
  * Facts about the last call that used `workspace` (synchronises `stream`
  * first).  Fills up to n of, in this order:
  *   0  arithmetic path of the sweeps: 0 CUDA-core fp32, 1 tf32 tensor cores,
- *      2 bf16 tensor cores
+ *      2 bf16 tensor cores, 3 f16 tensor cores (f16 accumulator)
  *   1  number of core points
  *   2  number of border candidates (non-core points with a neighbour
  *      besides themselves)
