@@ -79,9 +79,12 @@ Layout make_layout(int64_t n, int32_t d) {
     L.off_rootmin = off;     off += align256(per_pt);
     // tile bounding boxes for culling (three arrays: all, core, candidates)
     L.box_floats = d <= CULL_MAX_D ? (size_t)L.ntiles * 2 * d : 0;
+    L.gbox_floats = d <= CULL_MAX_D ? (size_t)((L.ntiles + 31) / 32) * 2 * d : 0;
     L.off_box_all = off;     off += align256(L.box_floats * sizeof(float));
     L.off_box_core = off;    off += align256(L.box_floats * sizeof(float));
     L.off_box_cand = off;    off += align256(L.box_floats * sizeof(float));
+    L.off_gbox_all = off;    off += align256(L.gbox_floats * sizeof(float));
+    L.off_gbox_core = off;   off += align256(L.gbox_floats * sizeof(float));
     L.total = off;
     return L;
 }
@@ -137,6 +140,8 @@ Work carve(void *base, const Layout &L) {
     w.box_all = reinterpret_cast<float *>(b + L.off_box_all);
     w.box_core = reinterpret_cast<float *>(b + L.off_box_core);
     w.box_cand = reinterpret_cast<float *>(b + L.off_box_cand);
+    w.gbox_all = reinterpret_cast<float *>(b + L.off_gbox_all);
+    w.gbox_core = reinterpret_cast<float *>(b + L.off_gbox_core);
     return w;
 }
 
@@ -427,7 +432,7 @@ int dbscan_profile_end(float *stage_ms, int32_t max_stages, int64_t *calls,
                 cudaEventElapsedTime(&ms, c.ev[i], c.ev[i + 1]) != cudaSuccess)
                 st = DBSCAN_ERR_CUDA;
             acc[i] += ms;
-            launches += stage_launches(c.d, c.eps2, i) + (c.cull ? (i == 0 ? 1 : (i == 2 ? 2 : 0)) : 0);
+            launches += stage_launches(c.d, c.eps2, i) + (c.cull ? (i == 0 ? 2 : (i == 2 ? 3 : 0)) : 0);
         }
         for (int i = 0; i <= c.stages; ++i) cudaEventDestroy(c.ev[i]);
     }

@@ -182,12 +182,36 @@ __global__ void k_tile_boxes(const float *staged, const int *count, int d, float
     }
 }
 
+// Box of every group of 32 consecutive tiles (over its valid tiles), so that
+// the sweeps can skip a whole group with one test: one thread per group and
+// dimension.
+__global__ void k_group_boxes(const float *box, const int *count, int d, int64_t ngroups,
+                              float *gbox) {
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= ngroups * d) return;
+    const int64_t g = e / d;
+    const int k = (int)(e % d);
+    const int64_t ntv = ((int64_t)*count + BT - 1) / BT;   // valid tiles
+    float lo = INFINITY, hi = -INFINITY;
+    for (int64_t t = g * 32; t < g * 32 + 32 && t < ntv; ++t) {
+        lo = fminf(lo, box[(t * d + k) * 2]);
+        hi = fmaxf(hi, box[(t * d + k) * 2 + 1]);
+    }
+    gbox[(g * d + k) * 2] = lo;
+    gbox[(g * d + k) * 2 + 1] = hi;
+}
+
 cudaError_t launch_tile_boxes(const Work &w, const Layout &L, int which, cudaStream_t s) {
     if (L.box_floats == 0) return cudaSuccess;
     const float *st = which == 0 ? w.staged_all : (which == 1 ? w.staged_core : w.staged_cand);
     const int *cnt = which == 0 ? &w.ctrl->n_all : (which == 1 ? &w.ctrl->n_core : &w.ctrl->n_cand);
     float *box = which == 0 ? w.box_all : (which == 1 ? w.box_core : w.box_cand);
     k_tile_boxes<<<(unsigned)L.ntiles, BT, 0, s>>>(st, cnt, L.d, box);
+    if (which != 2) {   // column arrays (all points, core points) also get group boxes
+        const int64_t ngroups = (L.ntiles + 31) / 32;
+        k_group_boxes<<<(unsigned)((ngroups * L.d + 255) / 256), 256, 0, s>>>(
+            box, cnt, L.d, ngroups, which == 0 ? w.gbox_all : w.gbox_core);
+    }
     return cudaGetLastError();
 }
 

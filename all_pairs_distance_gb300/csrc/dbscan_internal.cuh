@@ -66,7 +66,9 @@ struct Layout {
     size_t off_bin, off_perm, off_hist, off_bstart, off_btot, off_rootmin;
     int cull;             // 1: this call skips tile pairs whose boxes are eps apart
     size_t box_floats;    // floats of one box array (ntiles x 2d), 0 when d > CULL_MAX_D
+    size_t gbox_floats;   // floats of one group-box array (ceil(ntiles / 32) x 2d)
     size_t off_box_all, off_box_core, off_box_cand;
+    size_t off_gbox_all, off_gbox_core;
     int64_t nscan_blocks;
     size_t total;
 };
@@ -94,6 +96,7 @@ struct Work {
     int *btot;            // [2^order_bits / 1024] bin-block offsets
     int *rootmin;         // [n] smallest input index of each union-find root's component
     float *box_all, *box_core, *box_cand;   // [ntiles][d][min, max] tile bounding boxes
+    float *gbox_all, *gbox_core;            // [ntiles / 32][d][min, max] boxes of 32-tile groups
 };
 
 Work carve(void *base, const Layout &L);

@@ -67,6 +67,7 @@ struct TcArgs {
     int tri, ulo, uhi;
     int band, blo, bhi;       // band != 0: one unit per row block, tiles rb+blo .. rb+bhi-1
     const float *rbox, *cbox; // per-tile bounding boxes of rows / columns (d x (min, max))
+    const float *cgbox;       // boxes of groups of 32 column tiles
     int cull, d;              // cull != 0: skip column tiles whose box is eps or more away
     unsigned *ctr;
     Ctrl *ctrl;
@@ -385,7 +386,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         // Culling by tile boxes is exact for integer data within the exactness
         // bound: box gaps are integers, their squared sum is exact, and every
         // pair of a culled tile pair has d^2 >= that sum >= thrx (not a neighbour).
-        const bool cull = a.cull && ctrl->exact && a.rbox && a.cbox;
+        const bool cull = a.cull && ctrl->exact && a.rbox && a.cbox && a.cgbox;
         const float cthr = ctrl->thrx;
         for (;;) {
             unsigned u = 0;
@@ -456,13 +457,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             if (!cull) {
                 ok = emit(t0, t1);
             } else {
-                // each lane tests one column tile of a 32-tile window against the
-                // row tile's box; runs of kept tiles become stages
+                // Column tiles go by groups of 32: a group whose box is eps or
+                // more from the row tile's box is skipped with one test;
+                // otherwise each lane tests one tile of the group, and runs of
+                // kept tiles become stages.
                 const float *rbx = a.rbox + (size_t)rb * 2 * a.d;
-                for (int w0 = t0; w0 < t1 && ok; w0 += 32) {
+                for (int g = t0 / 32; g * 32 < t1 && ok; ++g) {
+                    {
+                        const float *gbx = a.cgbox + (size_t)g * 2 * a.d;
+                        float g2 = 0.f;
+                        for (int kk = 0; kk < a.d; ++kk) {
+                            const float gap = fmaxf(0.f, fmaxf(gbx[2 * kk] - rbx[2 * kk + 1],
+                                                               rbx[2 * kk] - gbx[2 * kk + 1]));
+                            g2 = fmaf(gap, gap, g2);
+                        }
+                        if (!(g2 < cthr)) continue;   // same value in every lane
+                    }
+                    const int w0 = g * 32;
                     const int tt = w0 + lane;
                     bool keep = false;
-                    if (tt < t1) {
+                    if (tt >= t0 && tt < t1) {
                         const float *cbx = a.cbox + (size_t)tt * 2 * a.d;
                         float g2 = 0.f;
                         for (int kk = 0; kk < a.d; ++kk) {
@@ -749,7 +763,7 @@ cudaError_t launch_count_tc(const Work &w, const Layout &L, cudaStream_t s) {
     a.n_rows = &w.ctrl->n_all; a.n_cols = &w.ctrl->n_all;
     a.tri = 1; a.ulo = 0; a.uhi = -1;
     a.ctr = &w.ctrl->unit_ctr[0]; a.ctrl = w.ctrl; a.cnt = w.cnt;
-    a.rbox = w.box_all; a.cbox = w.box_all; a.cull = L.cull; a.d = L.d;
+    a.rbox = w.box_all; a.cbox = w.box_all; a.cgbox = w.gbox_all; a.cull = L.cull; a.d = L.d;
     return run_tc_both<SWEEP_COUNT>(a, L, s);
 }
 
@@ -761,7 +775,7 @@ cudaError_t launch_union_tc_band(const Work &w, const Layout &L, int band, int b
     a.tri = 1; a.ulo = 0; a.uhi = -1;
     a.band = 1; a.blo = blo; a.bhi = bhi;
     a.ctr = &w.ctrl->band_ctr[band]; a.ctrl = w.ctrl; a.parent = w.parent;
-    a.rbox = w.box_core; a.cbox = w.box_core; a.cull = L.cull; a.d = L.d;
+    a.rbox = w.box_core; a.cbox = w.box_core; a.cgbox = w.gbox_core; a.cull = L.cull; a.d = L.d;
     return run_tc_both<SWEEP_UNION>(a, L, s);
 }
 
@@ -772,7 +786,7 @@ cudaError_t launch_border_tc(const Work &w, const Layout &L, int32_t *labels, cu
     a.tri = 0; a.ulo = 0; a.uhi = -1;
     a.ctr = &w.ctrl->unit_ctr[5]; a.ctrl = w.ctrl;
     a.candidx = w.candidx; a.labels = labels;
-    a.rbox = w.box_cand; a.cbox = w.box_core; a.cull = L.cull; a.d = L.d;
+    a.rbox = w.box_cand; a.cbox = w.box_core; a.cgbox = w.gbox_core; a.cull = L.cull; a.d = L.d;
     return run_tc_both<SWEEP_BORDER>(a, L, s);
 }
 

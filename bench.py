@@ -347,6 +347,7 @@ def run_gb300(args, dist: Dist):
         ce = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         torch.cuda.synchronize()
         dist.barrier()
+        binding.dbscan_profile_begin()
         for k in range(args.steps):
             flush.zero_()
             cs[k].record(stream)
@@ -354,11 +355,13 @@ def run_gb300(args, dist: Dist):
             ce[k].record(stream)
         torch.cuda.synchronize()
         dist.barrier()
+        c_stage_ms, c_calls, _ = binding.dbscan_profile_end()
         st = binding.dbscan_workspace_status(ws)
         if st != 0:
             raise RuntimeError(f"device status {binding.dbscan_strerror(st)}")
         c_ms = dist.max(sum(a.elapsed_time(b) for a, b in zip(cs, ce)) / args.steps)
         line["culled"] = {"ms_per_step": c_ms, "speedup_vs_all_pairs": mean_ms / c_ms,
+                          "stages_ms": {k: v / max(c_calls, 1) for k, v in c_stage_ms.items()},
                           "api": "dbscan_fit_culled",
                           "note": "tile pairs whose bounding boxes are eps apart are skipped "
                                   "(identical labels); not an all-pairs evaluation, so no "
