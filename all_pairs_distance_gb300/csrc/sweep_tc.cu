@@ -122,9 +122,9 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 // Bounded wait that polls without suspending; false on timeout or when
-// another role aborted.
-__device__ __noinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                       Ctrl *ctrl) {
+// another role aborted.  Out of line: only the slow path of mbar_spin.
+__device__ __noinline__ bool mbar_spin_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                            Ctrl *ctrl) {
     long long start = 0;
     for (unsigned it = 0;; ++it) {
         if (mbar_test(bar, parity)) return true;
@@ -139,6 +139,13 @@ __device__ __noinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile i
             }
         }
     }
+}
+// A phase that has already completed is the common case on the critical
+// path; testing it inline avoids a call (which saves and restores the live
+// registers of the caller) on every tile pair.
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          Ctrl *ctrl) {
+    return mbar_test(bar, parity) || mbar_spin_slow(bar, parity, abort_flag, ctrl);
 }
 // Bounded wait that ignores the abort flag (draining copies in flight).
 __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
