@@ -64,7 +64,7 @@ struct TcArgs {
     const uint8_t *ua, *ub;   // row / column operand tiles, packed 128 x kbytes each
     const int *n_rows, *n_cols;
     const int *aux;           // per-column int staged with the tiles (parent or label), or null
-    int tri, ulo, uhi;
+    int tri;
     int band, blo, bhi;       // band != 0: one unit per row block, tiles rb+blo .. rb+bhi-1
     const float *rbox, *cbox; // per-tile bounding boxes of rows / columns (d x (min, max))
     const float *cgbox;       // boxes of groups of 32 column tiles
@@ -291,27 +291,51 @@ __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
     return x;
 }
 
-// ---- unit schedule (as in the CUDA-core sweep) ---------------------------------
+// ---- unit schedule ---------------------------------------------------------------
+// Units go column chunk by column chunk (CHUNK tiles each), and within a chunk
+// by row block: the CTAs working at the same time stream the same chunk of
+// column tiles, which stays in L2 even when the operand arrays do not.  A unit
+// is row block rb against the chunk's tiles t with t - rb in [lo, hi) (the
+// whole triangle for the count, a distance band for the union, every tile for
+// the border's rectangle).
+constexpr int CHUNK = 512;
 struct TcSched {
-    int nrt, nct, uc, kc;
-    unsigned units, ubegin, uend;
+    int nrt, nct, nchunks;
+    unsigned units;
 };
-__device__ __forceinline__ TcSched tc_sched(int n_rows, int n_cols, int tri, int ulo, int uhi) {
+// The row blocks [first, first + count) of chunk c that have at least one tile
+// in it: rb + lo < (c + 1) * CHUNK and, with an upper distance, rb + hi > c * CHUNK.
+__device__ __forceinline__ int chunk_first_row(int c, int tri, int hi) {
+    return (tri && hi >= 0) ? max(0, c * CHUNK - hi + 1) : 0;
+}
+__device__ __forceinline__ int chunk_rows(const TcSched &s, int c, int tri, int lo, int hi) {
+    if (!tri) return s.nrt;
+    const int end = min(s.nrt, (c + 1) * CHUNK - lo);
+    return max(0, end - chunk_first_row(c, tri, hi));
+}
+__device__ __forceinline__ TcSched tc_sched(int n_rows, int n_cols, int tri, int lo, int hi) {
     TcSched s;
     s.nrt = (n_rows + BT - 1) / BT;
     s.nct = (n_cols + BT - 1) / BT;
-    long long total = tri ? (long long)s.nrt * (s.nrt + 1) / 2 : (long long)s.nrt * s.nct;
-    long long target = 8LL * gridDim.x;
-    long long uc = (total + target - 1) / target;
-    if (uc < 1) uc = 1;
-    if (uc > s.nct) uc = s.nct;
-    s.uc = (int)uc;
-    s.kc = (s.nct + s.uc - 1) / s.uc;
-    s.units = (unsigned)((long long)s.nrt * s.kc);
-    const long long g = gridDim.x;
-    s.ubegin = (unsigned)min((long long)s.units, ulo * g);
-    s.uend = uhi < 0 ? s.units : (unsigned)min((long long)s.units, uhi * g);
+    s.nchunks = (s.nct + CHUNK - 1) / CHUNK;
+    long long u = 0;
+    for (int c = 0; c < s.nchunks; ++c) u += chunk_rows(s, c, tri, lo, hi);
+    s.units = (unsigned)u;
     return s;
+}
+// Unit u -> row block and column tiles [t0, t1); false when it holds none.
+__device__ __forceinline__ bool tc_unit(const TcSched &s, unsigned u, int tri, int lo, int hi,
+                                        int &rb, int &t0, int &t1) {
+    int c = 0;
+    for (; c < s.nchunks; ++c) {
+        const unsigned r = (unsigned)chunk_rows(s, c, tri, lo, hi);
+        if (u < r) break;
+        u -= r;
+    }
+    rb = chunk_first_row(c, tri, hi) + (int)u;
+    t0 = max(c * CHUNK, tri ? rb + lo : 0);
+    t1 = min(min((c + 1) * CHUNK, s.nct), (tri && hi >= 0) ? rb + hi : s.nct);
+    return t0 < t1;
 }
 
 // ---- the kernel --------------------------------------------------------------------
@@ -378,11 +402,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    TcSched sc = tc_sched(n_rows, n_cols, a.tri, a.ulo, a.uhi);
-    if (a.band) {   // one unit per row block
-        sc.ubegin = 0;
-        sc.uend = (unsigned)sc.nrt;
-    }
+    const int lo = a.band ? a.blo : 0, hi = a.band ? a.bhi : -1;
+    const TcSched sc = tc_sched(n_rows, n_cols, a.tri, lo, hi);
 
     if (warp == PRODUCER_WARP) {
         // The whole warp walks the schedule; the copies of consecutive stages
@@ -397,22 +418,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         const float cthr = ctrl->thrx;
         for (;;) {
             unsigned u = 0;
-            if (lane == 0) u = sc.ubegin + atomicAdd(a.ctr, 1u);
+            if (lane == 0) u = atomicAdd(a.ctr, 1u);
             u = __shfl_sync(FULL, u, 0);
-            if (u >= sc.uend) break;
+            if (u >= sc.units) break;
             int rb, t0, t1;
-            if (a.band) {
-                rb = (int)u;
-                t0 = rb + a.blo;
-                t1 = a.bhi < 0 ? sc.nct : min(sc.nct, rb + a.bhi);
-                if (t0 >= t1) continue;
-            } else {
-                rb = (int)(u / sc.kc);
-                const int c = (int)(u % sc.kc);
-                t0 = a.tri ? rb + c * sc.uc : c * sc.uc;
-                if (t0 >= sc.nct) continue;
-                t1 = min(t0 + sc.uc, sc.nct);
-            }
+            if (!tc_unit(sc, u, a.tri, lo, hi, rb, t0, t1)) continue;
             const int ab = ua & 1;
             bool started = false;   // this unit's row tile has been loaded
             // Stages of up to G consecutive tiles over [ts, te); the unit's row
@@ -537,19 +547,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                     if (!mbar_spin(smem_addr(&a_full[m.abuf]), (ua >> 1) & 1, s_abort, ctrl)) break;
                     ++ua;
                 }
-                const uint32_t abase = smem_addr(sA + (size_t)m.abuf * a.tile_bytes_max);
-                const uint32_t sbase = smem_addr(sStage + (size_t)s * a.stage_bytes);
+                // descriptors of the row tile and of the stage's first tile; a
+                // K step is 256 bytes further, 16 in the descriptor's address field
+                const uint64_t da0 = umma_desc(smem_addr(sA + (size_t)m.abuf * a.tile_bytes_max), sbo);
+                const uint64_t ds0 = umma_desc(smem_addr(sStage + (size_t)s * a.stage_bytes), sbo);
                 for (int i = 0; 2 * i < m.ntiles; ++i, ++it) {
                     const int b = it % NACC;
                     if (!(ok = mbar_spin(smem_addr(&acc_empty[b]), ((it / NACC) & 1) ^ 1, s_abort, ctrl)))
                         break;
                     tc_fence_after();
                     // a pair of consecutive column tiles is one 256-row B operand
-                    const uint32_t bbase = sbase + (uint32_t)(2 * i) * tile_bytes;
+                    const uint64_t db0 = ds0 + (uint64_t)(((uint32_t)(2 * i) * tile_bytes) >> 4);
                     const uint32_t idesc = 2 * i + 1 < m.ntiles ? idesc256 : idesc128;
                     for (int ks = 0; ks < ksteps; ++ks)
-                        umma<KIND>(tmem + (uint32_t)(b * ACC_COLS), umma_desc(abase + ks * 256, sbo),
-                                   umma_desc(bbase + ks * 256, sbo), idesc, ks > 0 ? 1u : 0u);
+                        umma<KIND>(tmem + (uint32_t)(b * ACC_COLS), da0 + (uint64_t)(16 * ks),
+                                   db0 + (uint64_t)(16 * ks), idesc, ks > 0 ? 1u : 0u);
                     issued = true;
                     umma_commit(smem_addr(&acc_full[b]));
                 }
@@ -768,7 +780,7 @@ cudaError_t launch_count_tc(const Work &w, const Layout &L, cudaStream_t s) {
     TcArgs a{};
     a.ua = w.ua_all; a.ub = w.ub_all;
     a.n_rows = &w.ctrl->n_all; a.n_cols = &w.ctrl->n_all;
-    a.tri = 1; a.ulo = 0; a.uhi = -1;
+    a.tri = 1;
     a.ctr = &w.ctrl->unit_ctr[0]; a.ctrl = w.ctrl; a.cnt = w.cnt;
     a.rbox = w.box_all; a.cbox = w.box_all; a.cgbox = w.gbox_all; a.cull = L.cull; a.d = L.d;
     return run_tc_both<SWEEP_COUNT>(a, L, s);
@@ -779,7 +791,7 @@ cudaError_t launch_union_tc_band(const Work &w, const Layout &L, int band, int b
     TcArgs a{};
     a.ua = w.ua_core; a.ub = w.ub_core;
     a.n_rows = &w.ctrl->n_core; a.n_cols = &w.ctrl->n_core; a.aux = w.parent;
-    a.tri = 1; a.ulo = 0; a.uhi = -1;
+    a.tri = 1;
     a.band = 1; a.blo = blo; a.bhi = bhi;
     a.ctr = &w.ctrl->band_ctr[band]; a.ctrl = w.ctrl; a.parent = w.parent;
     a.rbox = w.box_core; a.cbox = w.box_core; a.cgbox = w.gbox_core; a.cull = L.cull; a.d = L.d;
@@ -790,7 +802,7 @@ cudaError_t launch_border_tc(const Work &w, const Layout &L, int32_t *labels, cu
     TcArgs a{};
     a.ua = w.ua_cand; a.ub = w.ub_core;
     a.n_rows = &w.ctrl->n_cand; a.n_cols = &w.ctrl->n_core; a.aux = w.clabel;
-    a.tri = 0; a.ulo = 0; a.uhi = -1;
+    a.tri = 0;
     a.ctr = &w.ctrl->unit_ctr[5]; a.ctrl = w.ctrl;
     a.candidx = w.candidx; a.labels = labels;
     a.rbox = w.box_cand; a.cbox = w.box_core; a.cgbox = w.gbox_core; a.cull = L.cull; a.d = L.d;
