@@ -221,7 +221,7 @@ struct ProfCall {
     int stages;   // number of stages the call ran
     int d;        // dimension of the call (sets the kernels per stage)
     float eps2;   // eps^2 of the call (sets the tensor-core kinds launched)
-    int cull;     // tile culling on (adds the box kernels)
+    int cull;     // 1: culled count, 2: culled union and border (box kernels)
 };
 struct ProfState {
     bool on = false;
@@ -267,7 +267,7 @@ static int run(const void *points, int dtype, int64_t n, int d, float eps, int m
                int32_t *labels, uint8_t *is_core, int32_t *cnt_out, void *ws, const Layout &L,
                cudaStream_t s) {
     Work w = carve(ws, L);
-    StageMarks marks(s, d, L.eps2, L.cull);
+    StageMarks marks(s, d, L.eps2, L.cull + 2 * L.cull_nbr);
     if (cudaMemsetAsync(w.ctrl, 0, sizeof(Ctrl), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     if (cudaMemsetAsync(w.cnt, 0, (size_t)n * sizeof(int), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     if (launch_prep(points, dtype, n, d, eps, allowed_tc(d, L.eps2), w, L, s) != cudaSuccess)
@@ -281,8 +281,8 @@ static int run(const void *points, int dtype, int64_t n, int d, float eps, int m
         return DBSCAN_OK;
     }
     if (launch_compact(w, L, min_pts, labels, is_core, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
-    if (L.cull && (launch_tile_boxes(w, L, 1, s) != cudaSuccess ||
-                   launch_tile_boxes(w, L, 2, s) != cudaSuccess))
+    if (L.cull_nbr && (launch_tile_boxes(w, L, 1, s) != cudaSuccess ||
+                       launch_tile_boxes(w, L, 2, s) != cudaSuccess))
         return DBSCAN_ERR_CUDA;
     marks.mark(s);
     if (launch_union(w, L, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
@@ -318,7 +318,12 @@ static int fit_common(const void *points, int32_t dtype, int64_t n, int32_t d, f
     if (!cnt_out && (!labels || !is_core)) return DBSCAN_ERR_INVALID_ARG;
     Layout L = make_layout(n, d);
     L.eps2 = eps * eps;
-    L.cull = cull && L.box_floats > 0 && L.umma_tile_bytes > 0;
+    // Union and border act only on neighbour pairs, all of which the count
+    // sweep has evaluated; they skip tile pairs that the box test proves hold
+    // none (exact data only, checked on the device).  The count sweep itself
+    // evaluates every pair unless the caller asked for culling.
+    L.cull_nbr = L.box_floats > 0 && L.umma_tile_bytes > 0;
+    L.cull = cull && L.cull_nbr;
     if (workspace) {
         if (workspace_bytes < L.total) return DBSCAN_ERR_INVALID_ARG;
         if (reinterpret_cast<uintptr_t>(workspace) & 255) return DBSCAN_ERR_INVALID_ARG;
@@ -432,7 +437,10 @@ int dbscan_profile_end(float *stage_ms, int32_t max_stages, int64_t *calls,
                 cudaEventElapsedTime(&ms, c.ev[i], c.ev[i + 1]) != cudaSuccess)
                 st = DBSCAN_ERR_CUDA;
             acc[i] += ms;
-            launches += stage_launches(c.d, c.eps2, i) + (c.cull ? (i == 0 ? 2 : (i == 2 ? 3 : 0)) : 0);
+            // box kernels: all points in prep (culled count), core and
+            // candidate arrays after compaction (union and border)
+            launches += stage_launches(c.d, c.eps2, i) + ((c.cull & 1) && i == 0 ? 2 : 0) +
+                        ((c.cull & 2) && i == 2 ? 3 : 0);
         }
         for (int i = 0; i <= c.stages; ++i) cudaEventDestroy(c.ev[i]);
     }

@@ -17,9 +17,10 @@ namespace dbscan {
 // the BT squared norms: (d + 1) * BT floats, 512-byte aligned rows.
 constexpr int BT = 128;
 constexpr int SCAN_BLOCK = 1024;   // elements per block of the compaction scan
-// Tile culling (dbscan_fit_culled) keeps per-tile bounding boxes for d up to
-// this dimension; beyond it the boxes prune little and the call runs unculled.
-constexpr int CULL_MAX_D = 8;
+// Tile culling keeps per-tile bounding boxes for d up to this dimension;
+// beyond it 128-point tiles in the locality order span most of every
+// dimension's range and the boxes prune little.
+constexpr int CULL_MAX_D = 16;
 
 // Sentinels for the padding slots of the last tile: a padding column has a
 // huge norm and never tests as a neighbour; a padding row has a hugely
@@ -64,7 +65,8 @@ struct Layout {
     size_t off_ua_all, off_ub_all, off_ua_core, off_ub_core, off_ua_cand;
     int order_bits;       // bins of the locality order: 2^order_bits
     size_t off_bin, off_perm, off_hist, off_bstart, off_btot, off_rootmin;
-    int cull;             // 1: this call skips tile pairs whose boxes are eps apart
+    int cull;             // 1: the count sweep also skips tile pairs whose boxes are eps apart
+    int cull_nbr;         // 1: union and border skip tile pairs whose boxes are eps apart
     size_t box_floats;    // floats of one box array (ntiles x 2d), 0 when d > CULL_MAX_D
     size_t gbox_floats;   // floats of one group-box array (ceil(ntiles / 32) x 2d)
     size_t off_box_all, off_box_core, off_box_cand;

@@ -481,6 +481,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                 const float *rbx = a.rbox + (size_t)rb * 2 * a.d;
                 for (int g = t0 / 32; g * 32 < t1 && ok; ++g) {
                     {
+                        // every lane computes the same sum (at most 16 dimensions)
                         const float *gbx = a.cgbox + (size_t)g * 2 * a.d;
                         float g2 = 0.f;
                         for (int kk = 0; kk < a.d; ++kk) {
@@ -488,7 +489,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                                                                rbx[2 * kk] - gbx[2 * kk + 1]));
                             g2 = fmaf(gap, gap, g2);
                         }
-                        if (!(g2 < cthr)) continue;   // same value in every lane
+                        if (!(g2 < cthr)) continue;
                     }
                     const int w0 = g * 32;
                     const int tt = w0 + lane;
@@ -794,7 +795,7 @@ cudaError_t launch_union_tc_band(const Work &w, const Layout &L, int band, int b
     a.tri = 1;
     a.band = 1; a.blo = blo; a.bhi = bhi;
     a.ctr = &w.ctrl->band_ctr[band]; a.ctrl = w.ctrl; a.parent = w.parent;
-    a.rbox = w.box_core; a.cbox = w.box_core; a.cgbox = w.gbox_core; a.cull = L.cull; a.d = L.d;
+    a.rbox = w.box_core; a.cbox = w.box_core; a.cgbox = w.gbox_core; a.cull = L.cull_nbr; a.d = L.d;
     return run_tc_both<SWEEP_UNION>(a, L, s);
 }
 
@@ -805,7 +806,7 @@ cudaError_t launch_border_tc(const Work &w, const Layout &L, int32_t *labels, cu
     a.tri = 0;
     a.ctr = &w.ctrl->unit_ctr[5]; a.ctrl = w.ctrl;
     a.candidx = w.candidx; a.labels = labels;
-    a.rbox = w.box_cand; a.cbox = w.box_core; a.cgbox = w.gbox_core; a.cull = L.cull; a.d = L.d;
+    a.rbox = w.box_cand; a.cbox = w.box_core; a.cgbox = w.gbox_core; a.cull = L.cull_nbr; a.d = L.d;
     return run_tc_both<SWEEP_BORDER>(a, L, s);
 }
 

@@ -116,8 +116,10 @@ int dbscan_fit_ex(const void *points, int32_t dtype, int64_t n, int32_t d,
  * neighbour, so for integer data within the exactness bound the result is
  * identical to dbscan_fit_ex.  This is not an all-pairs evaluation (pairs in
  * skipped tiles are never evaluated), which is why it is a separate entry
- * point.  Culling applies on the tensor-core paths for d <= 8 and exact data;
- * otherwise the call runs exactly as dbscan_fit_ex.  The pages evaluate all
+ * point.  Culling applies on the tensor-core paths for d <= 16 and exact data;
+ * otherwise the call runs exactly as dbscan_fit_ex.  (dbscan_fit_ex itself
+ * applies the same exact test in its union and border passes, which act only
+ * on neighbour pairs; its count pass evaluates every pair.)  The pages evaluate all
  * pairs ("Design and optimization of DBSCAN Algorithm based on CUDA", §IV-A);
  * pruning by spatial bounds is not on them.
  */

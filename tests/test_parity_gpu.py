@@ -301,7 +301,8 @@ CULL_CASES = {
     "d1_blobs": (lambda: _blobs(4_100, 1, 4095, 6, 30.0, 400, 44), 2.0, 4, torch.float32),
     "corners_d3": (lambda: (np.random.default_rng(45).integers(0, 2, size=(700, 3)) * 2047)
                    .astype(np.float32), 2047.0, 5, torch.float32),
-    "d16_no_cull": (lambda: synth.scaled("blobs_200k_d16", 4_001, seed=46), 120.0, 20, torch.float32),
+    "d16_blobs": (lambda: synth.scaled("blobs_200k_d16", 4_001, seed=46), 120.0, 20, torch.float32),
+    "d33_no_cull": (lambda: _blobs(2_500, 33, 127, 8, 4.0, 250, 48), 30.0, 5, torch.float32),
     "fractional_no_cull": (lambda: synth.scaled("blobs_1m_d3", 5_003, seed=47) * np.float32(0.5),
                            5.0, 8, torch.float32),
 }
