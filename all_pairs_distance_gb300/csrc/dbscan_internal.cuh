@@ -17,10 +17,9 @@ namespace dbscan {
 // the BT squared norms: (d + 1) * BT floats, 512-byte aligned rows.
 constexpr int BT = 128;
 constexpr int SCAN_BLOCK = 1024;   // elements per block of the compaction scan
-// Tile culling keeps per-tile bounding boxes for d up to this dimension;
-// beyond it 128-point tiles in the locality order span most of every
-// dimension's range and the boxes prune little.
-constexpr int CULL_MAX_D = 16;
+// Tile culling keeps per-tile bounding boxes for d up to this dimension (the
+// locality order's nearest-pivot key covers d <= 64 and keeps tiles tight).
+constexpr int CULL_MAX_D = 64;
 
 // Sentinels for the padding slots of the last tile: a padding column has a
 // huge norm and never tests as a neighbour; a padding row has a hugely

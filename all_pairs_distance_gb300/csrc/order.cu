@@ -14,8 +14,12 @@
 //
 // Key: d <= 3 interleaves the quantised coordinates themselves (30 bits for
 // d = 1, 15 per axis for d = 2, 10 per axis for d = 3); d > 3 interleaves three
-// fixed +-1 projections sum_k s_mk x_k, 10 bits each.  The top `bits` bits of
-// the 30-bit key name a bin (bits = ceil(log2 n) clamped to [8, 20]); a counting
+// fixed +-1 projections sum_k s_mk x_k, 10 bits each.  For 16 < d <= 64 three
+// projections mix clusters (in 64-D, 200 clusters projected to 3-D overlap),
+// so the key leads with the nearest of 512 pivots -- input points spread
+// evenly over the input order -- followed by the projection key: a cluster's
+// points share a pivot and land next to each other.  The top `bits` bits of the
+// 30-bit key name a bin (bits = ceil(log2 n) clamped to [8, 20]); a counting
 // sort over the bins gives the permutation (order within a bin is unspecified).
 #include "dbscan_internal.cuh"
 
@@ -57,6 +61,61 @@ __device__ __forceinline__ uint32_t spread2(uint32_t x) {   // 15 bits -> every 
     x = (x | (x << 2)) & 0x33333333u;
     x = (x | (x << 1)) & 0x55555555u;
     return x;
+}
+
+constexpr int PIVOT_MIN_D = 16;   // 16 < d <= PIVOT_MAX_D orders by nearest pivot first
+constexpr int PIVOT_MAX_D = 64;   // the point's coordinates sit in registers
+constexpr int PIVOT_BITS = 9;     // 512 pivots
+
+__host__ __device__ inline bool use_pivots(int d) { return d > PIVOT_MIN_D && d <= PIVOT_MAX_D; }
+
+// Nearest pivot of every point, into pid[i] (ties to the lower pivot).  Pivots
+// are the input points floor(j n / P).  |x - p|^2 = |x|^2 + |p|^2 - 2 x.p, and
+// |x|^2 is the same for every pivot, so each thread minimises |p|^2 - 2 x.p
+// with its point in registers, four pivots at a time (one 16-byte load of
+// -2p feeds four independent FMA chains).  Float rounding only perturbs the
+// order, never a result.
+__global__ void __launch_bounds__(256) k_pivot_assign(const void *pts, int dtype, int64_t n, int d,
+                                                      int *pid) {
+    constexpr int P = 1 << PIVOT_BITS;
+    extern __shared__ float s_piv[];   // [d][P]: -2 p_jk at k * P + j
+    __shared__ float s_pn[P];          // |p_j|^2
+    for (int e = threadIdx.x; e < P * d; e += blockDim.x) {
+        const int j = e % P, k = e / P;
+        const int64_t src = (int64_t)j * n / P;
+        s_piv[e] = -2.f * load_point(pts, dtype, (size_t)src * d + k);
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < P; j += blockDim.x) {
+        float q = 0.f;
+        for (int k = 0; k < d; ++k) q = fmaf(s_piv[k * P + j], s_piv[k * P + j], q);
+        s_pn[j] = 0.25f * q;
+    }
+    __syncthreads();
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float x[PIVOT_MAX_D];
+#pragma unroll
+    for (int k = 0; k < PIVOT_MAX_D; ++k) x[k] = k < d ? load_point(pts, dtype, (size_t)i * d + k) : 0.f;
+    float best = INFINITY;
+    int bj = 0;
+    for (int j0 = 0; j0 < P; j0 += 4) {
+        float a0 = s_pn[j0], a1 = s_pn[j0 + 1], a2 = s_pn[j0 + 2], a3 = s_pn[j0 + 3];
+#pragma unroll
+        for (int k = 0; k < PIVOT_MAX_D; ++k)
+            if (k < d) {
+                const float4 pv = *reinterpret_cast<const float4 *>(s_piv + k * P + j0);
+                a0 = fmaf(x[k], pv.x, a0);
+                a1 = fmaf(x[k], pv.y, a1);
+                a2 = fmaf(x[k], pv.z, a2);
+                a3 = fmaf(x[k], pv.w, a3);
+            }
+        if (a0 < best) { best = a0; bj = j0; }
+        if (a1 < best) { best = a1; bj = j0 + 1; }
+        if (a2 < best) { best = a2; bj = j0 + 2; }
+        if (a3 < best) { best = a3; bj = j0 + 3; }
+    }
+    pid[i] = bj;
 }
 
 // One thread: the axes' lower bounds and quantisation scales into Ctrl.
@@ -123,6 +182,8 @@ __global__ void k_order_key(const void *pts, int dtype, int64_t n, int d, const 
         key = 0;
         for (int m = 0; m < 3; ++m)
             key |= spread3(quantise(v[m], ctrl->ord_lo[m], ctrl->ord_scale[m], 1023.f)) << m;
+        if (use_pivots(d))   // nearest pivot first (bin[i] holds it on entry)
+            key = ((uint32_t)bin[i] << (30 - PIVOT_BITS)) | (key >> PIVOT_BITS);
     }
     const int b = (int)(key >> shift);
     bin[i] = b;
@@ -197,6 +258,13 @@ cudaError_t launch_order(const void *points, int dtype, int64_t n, int d, const 
     if (cudaMemsetAsync(w.hist, 0, (size_t)nbins * sizeof(int), s) != cudaSuccess) return cudaGetLastError();
     k_order_setup<<<1, 32, 0, s>>>(w.ctrl, w.stat_min, w.stat_max, d);
     const int blocks = (int)((n + 255) / 256);
+    if (use_pivots(d)) {
+        const size_t smem = (size_t)(1 << PIVOT_BITS) * d * sizeof(float);
+        if (cudaFuncSetAttribute((const void *)k_pivot_assign,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return cudaGetLastError();
+        k_pivot_assign<<<blocks, 256, smem, s>>>(points, dtype, n, d, w.bin);
+    }
     k_order_key<<<blocks, 256, 0, s>>>(points, dtype, n, d, w.ctrl, 30 - L.order_bits, w.bin,
                                        w.hist);
     k_bin_scan<<<nblk, BIN_SCAN_THREADS, 0, s>>>(w.hist, nbins, w.bstart, w.btot);

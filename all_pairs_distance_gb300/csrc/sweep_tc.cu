@@ -481,13 +481,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                 const float *rbx = a.rbox + (size_t)rb * 2 * a.d;
                 for (int g = t0 / 32; g * 32 < t1 && ok; ++g) {
                     {
-                        // every lane computes the same sum (at most 16 dimensions)
+                        // every lane gets the same sum: up to 16 dimensions each
+                        // lane adds them all; beyond, lanes split the dimensions
+                        // (integer gaps: the sum is exact in any order)
                         const float *gbx = a.cgbox + (size_t)g * 2 * a.d;
                         float g2 = 0.f;
-                        for (int kk = 0; kk < a.d; ++kk) {
+                        const bool split = a.d > 16;
+                        for (int kk = split ? lane : 0; kk < a.d; kk += split ? 32 : 1) {
                             const float gap = fmaxf(0.f, fmaxf(gbx[2 * kk] - rbx[2 * kk + 1],
                                                                rbx[2 * kk] - gbx[2 * kk + 1]));
                             g2 = fmaf(gap, gap, g2);
+                        }
+                        if (split) {
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) g2 += __shfl_xor_sync(FULL, g2, o);
                         }
                         if (!(g2 < cthr)) continue;
                     }
