@@ -64,13 +64,18 @@ __device__ __forceinline__ uint32_t spread2(uint32_t x) {   // 15 bits -> every 
 }
 
 constexpr int PIVOT_MIN_D = 16;   // 16 < d <= PIVOT_MAX_D orders by nearest pivot first
-constexpr int PIVOT_MAX_D = 64;   // the point's coordinates sit in registers
+constexpr int PIVOT_MAX_D = 64;   // beyond, tiles stay too wide for the box test
 constexpr int PIVOT_BITS = 9;     // 512 pivots
+constexpr int PIVOT_DIMS = 16;    // distances to the pivots over 16 evenly spread coordinates
+
+// Coordinate m (< PIVOT_DIMS) of the pivot distance.
+__host__ __device__ inline int pivot_dim(int m, int d) { return (int)((int64_t)m * d / PIVOT_DIMS); }
 
 __host__ __device__ inline bool use_pivots(int d) { return d > PIVOT_MIN_D && d <= PIVOT_MAX_D; }
 
-// Nearest pivot of every point, into pid[i] (ties to the lower pivot).  Pivots
-// are the input points floor(j n / P).  |x - p|^2 = |x|^2 + |p|^2 - 2 x.p, and
+// Nearest pivot of every point, into pid[i] (ties to the lower pivot), over 16
+// coordinates spread evenly across the d (enough to tell clusters apart).
+// Pivots are the input points floor(j n / P).  |x - p|^2 = |x|^2 + |p|^2 - 2 x.p, and
 // |x|^2 is the same for every pivot, so each thread minimises |p|^2 - 2 x.p
 // with its point in registers, four pivots at a time (one 16-byte load of
 // -2p feeds four independent FMA chains).  Float rounding only perturbs the
@@ -78,38 +83,37 @@ __host__ __device__ inline bool use_pivots(int d) { return d > PIVOT_MIN_D && d 
 __global__ void __launch_bounds__(256) k_pivot_assign(const void *pts, int dtype, int64_t n, int d,
                                                       int *pid) {
     constexpr int P = 1 << PIVOT_BITS;
-    extern __shared__ float s_piv[];   // [d][P]: -2 p_jk at k * P + j
-    __shared__ float s_pn[P];          // |p_j|^2
-    for (int e = threadIdx.x; e < P * d; e += blockDim.x) {
-        const int j = e % P, k = e / P;
+    __shared__ __align__(16) float s_piv[PIVOT_DIMS * P];   // -2 p_jm at m * P + j
+    __shared__ float s_pn[P];                                // |p_j|^2 over the 16 coordinates
+    for (int e = threadIdx.x; e < P * PIVOT_DIMS; e += blockDim.x) {
+        const int j = e % P, m = e / P;
         const int64_t src = (int64_t)j * n / P;
-        s_piv[e] = -2.f * load_point(pts, dtype, (size_t)src * d + k);
+        s_piv[e] = -2.f * load_point(pts, dtype, (size_t)src * d + pivot_dim(m, d));
     }
     __syncthreads();
     for (int j = threadIdx.x; j < P; j += blockDim.x) {
         float q = 0.f;
-        for (int k = 0; k < d; ++k) q = fmaf(s_piv[k * P + j], s_piv[k * P + j], q);
+        for (int m = 0; m < PIVOT_DIMS; ++m) q = fmaf(s_piv[m * P + j], s_piv[m * P + j], q);
         s_pn[j] = 0.25f * q;
     }
     __syncthreads();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
-    float x[PIVOT_MAX_D];
+    float x[PIVOT_DIMS];
 #pragma unroll
-    for (int k = 0; k < PIVOT_MAX_D; ++k) x[k] = k < d ? load_point(pts, dtype, (size_t)i * d + k) : 0.f;
+    for (int m = 0; m < PIVOT_DIMS; ++m) x[m] = load_point(pts, dtype, (size_t)i * d + pivot_dim(m, d));
     float best = INFINITY;
     int bj = 0;
     for (int j0 = 0; j0 < P; j0 += 4) {
         float a0 = s_pn[j0], a1 = s_pn[j0 + 1], a2 = s_pn[j0 + 2], a3 = s_pn[j0 + 3];
 #pragma unroll
-        for (int k = 0; k < PIVOT_MAX_D; ++k)
-            if (k < d) {
-                const float4 pv = *reinterpret_cast<const float4 *>(s_piv + k * P + j0);
-                a0 = fmaf(x[k], pv.x, a0);
-                a1 = fmaf(x[k], pv.y, a1);
-                a2 = fmaf(x[k], pv.z, a2);
-                a3 = fmaf(x[k], pv.w, a3);
-            }
+        for (int m = 0; m < PIVOT_DIMS; ++m) {
+            const float4 pv = *reinterpret_cast<const float4 *>(s_piv + m * P + j0);
+            a0 = fmaf(x[m], pv.x, a0);
+            a1 = fmaf(x[m], pv.y, a1);
+            a2 = fmaf(x[m], pv.z, a2);
+            a3 = fmaf(x[m], pv.w, a3);
+        }
         if (a0 < best) { best = a0; bj = j0; }
         if (a1 < best) { best = a1; bj = j0 + 1; }
         if (a2 < best) { best = a2; bj = j0 + 2; }
@@ -258,13 +262,7 @@ cudaError_t launch_order(const void *points, int dtype, int64_t n, int d, const 
     if (cudaMemsetAsync(w.hist, 0, (size_t)nbins * sizeof(int), s) != cudaSuccess) return cudaGetLastError();
     k_order_setup<<<1, 32, 0, s>>>(w.ctrl, w.stat_min, w.stat_max, d);
     const int blocks = (int)((n + 255) / 256);
-    if (use_pivots(d)) {
-        const size_t smem = (size_t)(1 << PIVOT_BITS) * d * sizeof(float);
-        if (cudaFuncSetAttribute((const void *)k_pivot_assign,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return cudaGetLastError();
-        k_pivot_assign<<<blocks, 256, smem, s>>>(points, dtype, n, d, w.bin);
-    }
+    if (use_pivots(d)) k_pivot_assign<<<blocks, 256, 0, s>>>(points, dtype, n, d, w.bin);
     k_order_key<<<blocks, 256, 0, s>>>(points, dtype, n, d, w.ctrl, 30 - L.order_bits, w.bin,
                                        w.hist);
     k_bin_scan<<<nblk, BIN_SCAN_THREADS, 0, s>>>(w.hist, nbins, w.bstart, w.btot);

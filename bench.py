@@ -310,9 +310,16 @@ def run_gb300(args, dist: Dist):
                                        "note": "the same algorithmic FLOP against the tensor peak of "
                                                "the MMA kind the sweep runs on"}
     else:
+        sust = (peaks or {}).get("bf16_tflops_sustained")
         roofline = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                     "frac": achieved / tc_peak, "traffic": traffic, "kernel": kname,
                     "peak_source": tc_source + " -- of measured",
+                    # the count sweep is timed inside a long multi-kernel step; the
+                    # measured sustained peak (a seconds-long GEMM loop at the power
+                    # cap) is the other denominator for that case
+                    "frac_vs_sustained": (achieved / (sust * (1.0 if info["path"] in ("bf16", "f16")
+                                                              else TF32_PER_BF16))
+                                          if sust else None),
                     "fp32_equivalent": {"achieved": achieved, "peak": fp32_peak,
                                         "frac": achieved / fp32_peak,
                                         "note": "same algorithmic FLOP (2d per unordered pair) "
