@@ -147,28 +147,72 @@ __global__ void k_setup(Ctrl *ctrl, const int *smin, const int *smax, float *cen
     }
 }
 
-// Write element k of an operand row: float bits for tf32, f16 or bf16 otherwise.
-__device__ __forceinline__ void put_elem(uint8_t *tile, int row, int k, int kbytes, int kind,
-                                         float v) {
-    if (kind == TC_TF32) {
-        *reinterpret_cast<float *>(tile + umma_offset(row, 4 * k, kbytes)) = v;
-    } else if (kind == TC_F16) {
-        *reinterpret_cast<__half *>(tile + umma_offset(row, 2 * k, kbytes)) = __float2half_rn(v);
-    } else {
-        *reinterpret_cast<__nv_bfloat16 *>(tile + umma_offset(row, 2 * k, kbytes)) =
-            __float2bfloat16_rn(v);
+// Element k of a point's operand row (see the header comment):
+//   A (row form)    [-2 c,  base powers,  norm digits,  -threshold digits, 0..]
+//   B (column form) [   c,  norm digits,  base powers,   base powers,      0..]
+struct OperandRow {
+    const float *src;   // the point's staged coordinates (stride BT), then its norm
+    int d, nd, nt, base, nrm, th;
+    __device__ __forceinline__ float elem(int k, bool col) const {
+        if (k < d) {
+            const float c = src[(size_t)k * BT];
+            return col ? c : -2.f * c;
+        }
+        k -= d;
+        if (k < 2 * nd + nt) {
+            const int j = k < nd ? k : (k < 2 * nd ? k - nd : k - 2 * nd);
+            int pw = 1;
+            for (int t = 0; t < j; ++t) pw *= base;
+            if (k < nd) return col ? (float)((nrm / pw) % base) : (float)pw;        // column norm
+            if (k < 2 * nd) return col ? (float)pw : (float)((nrm / pw) % base);    // row norm
+            return col ? (float)pw : (float)(-((th / pw) % base));                  // threshold
+        }
+        return 0.f;
     }
+};
+
+__device__ __forceinline__ uint32_t pack_pair(int kind, float lo, float hi) {
+    uint16_t a, b;
+    if (kind == TC_F16) {
+        const __half x = __float2half_rn(lo), y = __float2half_rn(hi);
+        a = *reinterpret_cast<const uint16_t *>(&x);
+        b = *reinterpret_cast<const uint16_t *>(&y);
+    } else {
+        const __nv_bfloat16 x = __float2bfloat16_rn(lo), y = __float2bfloat16_rn(hi);
+        a = *reinterpret_cast<const uint16_t *>(&x);
+        b = *reinterpret_cast<const uint16_t *>(&y);
+    }
+    return (uint32_t)a | ((uint32_t)b << 16);
+}
+
+// 16 bytes of an operand row: 4 tf32 or 8 f16/bf16 elements from element k0.
+__device__ __forceinline__ uint4 row_chunk(const OperandRow &r, int kind, int k0, bool col) {
+    uint4 v;
+    if (kind == TC_TF32) {
+        v.x = __float_as_uint(r.elem(k0, col));
+        v.y = __float_as_uint(r.elem(k0 + 1, col));
+        v.z = __float_as_uint(r.elem(k0 + 2, col));
+        v.w = __float_as_uint(r.elem(k0 + 3, col));
+    } else {
+        v.x = pack_pair(kind, r.elem(k0, col), r.elem(k0 + 1, col));
+        v.y = pack_pair(kind, r.elem(k0 + 2, col), r.elem(k0 + 3, col));
+        v.z = pack_pair(kind, r.elem(k0 + 4, col), r.elem(k0 + 5, col));
+        v.w = pack_pair(kind, r.elem(k0 + 6, col), r.elem(k0 + 7, col));
+    }
+    return v;
 }
 
 // Tensor-core operand tiles from the staged points: A (row form) and,
 // optionally, B (column form).  Tiles are packed back to back (128 x kbytes
 // each) so that consecutive tiles can be copied in one piece.  Slots at or
-// beyond *count are zero; the sweep masks them out by index.
+// beyond *count are zero; the sweep masks them out by index.  Each thread
+// writes its row 16 bytes at a time: in the K-major layout 16 bytes of a row
+// are contiguous and 8 consecutive rows fill 128 contiguous bytes.
 __global__ void k_stage_umma(const Ctrl *ctrl, const int *count, const float *staged, int d,
                              int64_t npad, uint8_t *ua, uint8_t *ub) {
     const int kind = ctrl->tc_kind;
     if (kind == TC_NONE) return;
-    const int kpad = ctrl->tc_kpad, kbytes = ctrl->tc_kbytes, nt = ctrl->tc_nt;
+    const int kbytes = ctrl->tc_kbytes;
     const size_t tile_stride = (size_t)BT * kbytes;
     const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (p >= npad) return;
@@ -176,45 +220,26 @@ __global__ void k_stage_umma(const Ctrl *ctrl, const int *count, const float *st
     const int row = (int)(p % BT);
     uint8_t *ta = ua + (size_t)tile * tile_stride;
     uint8_t *tb = ub ? ub + (size_t)tile * tile_stride : nullptr;
+    const int per = kind == TC_TF32 ? 4 : 8;   // elements per 16 bytes
     if (p >= *count) {
-        for (int k = 0; k < kpad; ++k) {
-            put_elem(ta, row, k, kbytes, kind, 0.f);
-            if (tb) put_elem(tb, row, k, kbytes, kind, 0.f);
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        for (int q = 0; q < kbytes / 16; ++q) {
+            *reinterpret_cast<uint4 *>(ta + umma_offset(row, 16 * q, kbytes)) = z;
+            if (tb) *reinterpret_cast<uint4 *>(tb + umma_offset(row, 16 * q, kbytes)) = z;
         }
         return;
     }
-    const int base = kind == TC_BF16 ? 256 : 2048;
-    const int nd = tc_norm_digits(kind);
-    const float *src = staged + (size_t)tile * (size_t)(d + 1) * BT + row;
-    int k = 0;
-    for (; k < d; ++k) {
-        const float c = src[(size_t)k * BT];
-        put_elem(ta, row, k, kbytes, kind, -2.f * c);
-        if (tb) put_elem(tb, row, k, kbytes, kind, c);
-    }
-    const int nrm = (int)src[(size_t)d * BT];
-    // column norm: B holds its digits, A the powers of the base
-    int pw = 1, nr = nrm;
-    for (int j = 0; j < nd; ++j, ++k, pw *= base, nr /= base) {
-        put_elem(ta, row, k, kbytes, kind, (float)pw);
-        if (tb) put_elem(tb, row, k, kbytes, kind, (float)(nr % base));
-    }
-    // row norm: A holds its digits, B the powers of the base
-    pw = 1, nr = nrm;
-    for (int j = 0; j < nd; ++j, ++k, pw *= base, nr /= base) {
-        put_elem(ta, row, k, kbytes, kind, (float)(nr % base));
-        if (tb) put_elem(tb, row, k, kbytes, kind, (float)pw);
-    }
-    // threshold constant: -digits in A, powers in B
-    pw = 1;
-    int th = (int)ctrl->thrx;
-    for (int j = 0; j < nt; ++j, ++k, pw *= base, th /= base) {
-        put_elem(ta, row, k, kbytes, kind, (float)(-(th % base)));
-        if (tb) put_elem(tb, row, k, kbytes, kind, (float)pw);
-    }
-    for (; k < kpad; ++k) {
-        put_elem(ta, row, k, kbytes, kind, 0.f);
-        if (tb) put_elem(tb, row, k, kbytes, kind, 0.f);
+    OperandRow r;
+    r.src = staged + (size_t)tile * (size_t)(d + 1) * BT + row;
+    r.d = d;
+    r.nd = tc_norm_digits(kind);
+    r.nt = ctrl->tc_nt;
+    r.base = kind == TC_BF16 ? 256 : 2048;
+    r.nrm = (int)r.src[(size_t)d * BT];
+    r.th = (int)ctrl->thrx;
+    for (int q = 0; q < kbytes / 16; ++q) {
+        *reinterpret_cast<uint4 *>(ta + umma_offset(row, 16 * q, kbytes)) = row_chunk(r, kind, q * per, false);
+        if (tb) *reinterpret_cast<uint4 *>(tb + umma_offset(row, 16 * q, kbytes)) = row_chunk(r, kind, q * per, true);
     }
 }
 
