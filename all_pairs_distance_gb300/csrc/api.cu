@@ -89,6 +89,19 @@ Layout make_layout(int64_t n, int32_t d) {
     return L;
 }
 
+// The layout of one call: sizes plus eps and the culling switches.  Union and
+// border act only on neighbour pairs, all of which the count sweep has
+// evaluated; they skip tile pairs that the box test proves hold none (exact
+// data only, checked on the device).  The count sweep itself evaluates every
+// pair unless the caller asked for culling.
+static Layout call_layout(int64_t n, int32_t d, float eps, int cull) {
+    Layout L = make_layout(n, d);
+    L.eps2 = eps * eps;
+    L.cull_nbr = L.box_floats > 0 && L.umma_tile_bytes > 0;
+    L.cull = cull && L.cull_nbr;
+    return L;
+}
+
 // Tensor-core paths this call may use (operand rows that fit the kind for the
 // threshold digits eps allows), narrowed by DBSCAN_FORCE_PATH ("fp32", "tf32",
 // "bf16" or "f16") when it is set.
@@ -316,14 +329,7 @@ static int fit_common(const void *points, int32_t dtype, int64_t n, int32_t d, f
     if (n == 0) return DBSCAN_OK;
     if (!points) return DBSCAN_ERR_INVALID_ARG;
     if (!cnt_out && (!labels || !is_core)) return DBSCAN_ERR_INVALID_ARG;
-    Layout L = make_layout(n, d);
-    L.eps2 = eps * eps;
-    // Union and border act only on neighbour pairs, all of which the count
-    // sweep has evaluated; they skip tile pairs that the box test proves hold
-    // none (exact data only, checked on the device).  The count sweep itself
-    // evaluates every pair unless the caller asked for culling.
-    L.cull_nbr = L.box_floats > 0 && L.umma_tile_bytes > 0;
-    L.cull = cull && L.cull_nbr;
+    const Layout L = call_layout(n, d, eps, cull);
     if (workspace) {
         if (workspace_bytes < L.total) return DBSCAN_ERR_INVALID_ARG;
         if (reinterpret_cast<uintptr_t>(workspace) & 255) return DBSCAN_ERR_INVALID_ARG;
@@ -466,8 +472,7 @@ int dbscan_fit_host(const void *points_host, int32_t dtype, int64_t n, int32_t d
     if (n == 0) return DBSCAN_OK;
     if (!points_host || !labels_host || !is_core_host) return DBSCAN_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    Layout L = make_layout(n, d);
-    L.eps2 = eps * eps;
+    const Layout L = call_layout(n, d, eps, 0);
     const size_t esz = dtype == DBSCAN_BF16 ? 2 : 4;
     const size_t pbytes = align256((size_t)n * d * esz);
     const size_t lbytes = align256((size_t)n * sizeof(int32_t));
