@@ -18,7 +18,7 @@ namespace dbscan {
 constexpr int BT = 128;
 constexpr int SCAN_BLOCK = 1024;   // elements per block of the compaction scan
 // Tile culling keeps per-tile bounding boxes for d up to this dimension (the
-// locality order's nearest-pivot key covers d <= 64 and keeps tiles tight).
+// locality order's nearest-pivot key covers 3 < d <= 64 and keeps tiles tight).
 constexpr int CULL_MAX_D = 64;
 
 // Sentinels for the padding slots of the last tile: a padding column has a

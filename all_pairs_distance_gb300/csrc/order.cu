@@ -14,11 +14,12 @@
 //
 // Key: d <= 3 interleaves the quantised coordinates themselves (30 bits for
 // d = 1, 15 per axis for d = 2, 10 per axis for d = 3); d > 3 interleaves three
-// fixed +-1 projections sum_k s_mk x_k, 10 bits each.  For 16 < d <= 64 three
-// projections mix clusters (in 64-D, 200 clusters projected to 3-D overlap),
-// so the key leads with the nearest of 512 pivots -- input points spread
-// evenly over the input order -- followed by the projection key: a cluster's
-// points share a pivot and land next to each other.  The top `bits` bits of the
+// fixed +-1 projections sum_k s_mk x_k, 10 bits each.  Three projections mix
+// clusters once d > 3 (in 64-D, 200 clusters projected to 3-D overlap; in
+// 16-D the union's tile boxes stay wide), so for 3 < d <= 64 the key leads
+// with the nearest of 512 pivots -- input points spread evenly over the input
+// order -- followed by the projection key: a cluster's points share a pivot
+// and land next to each other.  The top `bits` bits of the
 // 30-bit key name a bin (bits = ceil(log2 n) clamped to [8, 20]); a counting
 // sort over the bins gives the permutation (order within a bin is unspecified).
 #include "dbscan_internal.cuh"
@@ -63,18 +64,25 @@ __device__ __forceinline__ uint32_t spread2(uint32_t x) {   // 15 bits -> every 
     return x;
 }
 
-constexpr int PIVOT_MIN_D = 16;   // 16 < d <= PIVOT_MAX_D orders by nearest pivot first
+constexpr int PIVOT_MIN_D = 3;    // PIVOT_MIN_D < d <= PIVOT_MAX_D orders by nearest pivot first
 constexpr int PIVOT_MAX_D = 64;   // beyond, tiles stay too wide for the box test
 constexpr int PIVOT_BITS = 9;     // 512 pivots
-constexpr int PIVOT_DIMS = 16;    // distances to the pivots over 16 evenly spread coordinates
+constexpr int PIVOT_DIMS = 16;    // distances to the pivots over at most 16 coordinates
 
-// Coordinate m (< PIVOT_DIMS) of the pivot distance.
-__host__ __device__ inline int pivot_dim(int m, int d) { return (int)((int64_t)m * d / PIVOT_DIMS); }
+// Coordinate m (< PIVOT_DIMS) of the pivot distance: all d coordinates when
+// d <= 16 (slots m >= d hold 0 in points and pivots alike), else 16 spread
+// evenly across the d.
+__host__ __device__ inline int pivot_dim(int m, int d) {
+    return d <= PIVOT_DIMS ? m : (int)((int64_t)m * d / PIVOT_DIMS);
+}
+__device__ __forceinline__ float pivot_coord(const void *pts, int dtype, int64_t row, int m, int d) {
+    return m < d ? load_point(pts, dtype, (size_t)row * d + pivot_dim(m, d)) : 0.f;
+}
 
 __host__ __device__ inline bool use_pivots(int d) { return d > PIVOT_MIN_D && d <= PIVOT_MAX_D; }
 
-// Nearest pivot of every point, into pid[i] (ties to the lower pivot), over 16
-// coordinates spread evenly across the d (enough to tell clusters apart).
+// Nearest pivot of every point, into pid[i] (ties to the lower pivot), over the
+// coordinates pivot_dim picks (at most 16: enough to tell clusters apart).
 // Pivots are the input points floor(j n / P).  |x - p|^2 = |x|^2 + |p|^2 - 2 x.p, and
 // |x|^2 is the same for every pivot, so each thread minimises |p|^2 - 2 x.p
 // with its point in registers, four pivots at a time (one 16-byte load of
@@ -84,11 +92,11 @@ __global__ void __launch_bounds__(256) k_pivot_assign(const void *pts, int dtype
                                                       int *pid) {
     constexpr int P = 1 << PIVOT_BITS;
     __shared__ __align__(16) float s_piv[PIVOT_DIMS * P];   // -2 p_jm at m * P + j
-    __shared__ float s_pn[P];                                // |p_j|^2 over the 16 coordinates
+    __shared__ float s_pn[P];                                // |p_j|^2 over those coordinates
     for (int e = threadIdx.x; e < P * PIVOT_DIMS; e += blockDim.x) {
         const int j = e % P, m = e / P;
         const int64_t src = (int64_t)j * n / P;
-        s_piv[e] = -2.f * load_point(pts, dtype, (size_t)src * d + pivot_dim(m, d));
+        s_piv[e] = -2.f * pivot_coord(pts, dtype, src, m, d);
     }
     __syncthreads();
     for (int j = threadIdx.x; j < P; j += blockDim.x) {
@@ -101,7 +109,7 @@ __global__ void __launch_bounds__(256) k_pivot_assign(const void *pts, int dtype
     if (i >= n) return;
     float x[PIVOT_DIMS];
 #pragma unroll
-    for (int m = 0; m < PIVOT_DIMS; ++m) x[m] = load_point(pts, dtype, (size_t)i * d + pivot_dim(m, d));
+    for (int m = 0; m < PIVOT_DIMS; ++m) x[m] = pivot_coord(pts, dtype, i, m, d);
     float best = INFINITY;
     int bj = 0;
     for (int j0 = 0; j0 < P; j0 += 4) {

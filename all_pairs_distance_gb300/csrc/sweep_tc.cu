@@ -40,6 +40,9 @@
 // and MMAs in flight, frees its TMEM and returns.
 #include "dbscan_internal.cuh"
 
+#include <stdlib.h>
+#include <string.h>
+
 #include <map>
 #include <mutex>
 
@@ -54,7 +57,12 @@ constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int TC_MAX_STAGES = 8;
 constexpr int TC_MAX_GROUP = 32;        // column tiles per stage (one bulk copy)
-constexpr int ISSUE_LANES = 8;          // producer lanes that take turns issuing copies
+// Producer lanes: the bulk copies of one thread complete one after another,
+// each taking some 600 cycles up to about 48 KB, so a stage is copied in parts
+// of about PART_BYTES issued by different lanes (B_LANES of them, in turn) and
+// the row tiles by the other A_LANES.
+constexpr int B_LANES = 24, A_LANES = 8;
+constexpr int PART_BYTES = 16384;
 constexpr long long WAIT_LIMIT = 8000000000LL;   // clock cycles (about 4 s)
 constexpr int UF_CAP = 1 << 22;
 
@@ -81,7 +89,7 @@ struct TcArgs {
 };
 
 struct Meta {
-    int rb, t_first, ntiles, flags, abuf;
+    int rb, nrow, t_first, ntiles, flags, abuf;
 };
 
 // ---- PTX wrappers ------------------------------------------------------------
@@ -293,53 +301,65 @@ __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
 
 // ---- unit schedule ---------------------------------------------------------------
 // Units go column chunk by column chunk (CHUNK tiles each), and within a chunk
-// by row block: the CTAs working at the same time stream the same chunk of
-// column tiles, which stays in L2 even when the operand arrays do not.  A unit
-// is row block rb against the chunk's tiles t with t - rb in [lo, hi) (the
-// whole triangle for the count, a distance band for the union, every tile for
-// the border's rectangle).
+// by row unit: the CTAs working at the same time stream the same chunk of
+// column tiles, which stays in L2 even when the operand arrays do not.  A row
+// unit is rt consecutive row blocks rb .. rb + rt - 1 (rb = rt x its index);
+// every column tile staged for it meets all of them, so a column tile is
+// copied from L2 once per rt row blocks.  A unit is a row unit against the
+// chunk's tiles t with t - rb in [lo, hi) (the whole triangle for the count,
+// a distance band for the union, every tile for the border's rectangle).  In
+// the triangle the pairs (rb + r, t) with t < rb + r are skipped; every pair
+// (r, t) with t >= r still lies in exactly one unit and one band, since bands
+// split t - rb.
 constexpr int CHUNK = 512;
 struct TcSched {
-    int nrt, nct, nchunks;
+    int nrt, nct, nchunks, rt, nru;
     unsigned units;
 };
-// The row blocks [first, first + count) of chunk c that have at least one tile
+// The row units [first, first + count) of chunk c that have at least one tile
 // in it: rb + lo < (c + 1) * CHUNK and, with an upper distance, rb + hi > c * CHUNK.
-__device__ __forceinline__ int chunk_first_row(int c, int tri, int hi) {
-    return (tri && hi >= 0) ? max(0, c * CHUNK - hi + 1) : 0;
+__device__ __forceinline__ int chunk_first_row(const TcSched &s, int c, int tri, int hi) {
+    if (!(tri && hi >= 0)) return 0;
+    const int x = c * CHUNK - hi;          // first rb with rb > x
+    return x < 0 ? 0 : x / s.rt + 1;
 }
 __device__ __forceinline__ int chunk_rows(const TcSched &s, int c, int tri, int lo, int hi) {
-    if (!tri) return s.nrt;
-    const int end = min(s.nrt, (c + 1) * CHUNK - lo);
-    return max(0, end - chunk_first_row(c, tri, hi));
+    if (!tri) return s.nru;
+    const int lim = (c + 1) * CHUNK - lo;  // rb < lim
+    const int end = lim <= 0 ? 0 : min(s.nru, (lim + s.rt - 1) / s.rt);
+    return max(0, end - chunk_first_row(s, c, tri, hi));
 }
-__device__ __forceinline__ TcSched tc_sched(int n_rows, int n_cols, int tri, int lo, int hi) {
+__device__ __forceinline__ TcSched tc_sched(int n_rows, int n_cols, int tri, int lo, int hi, int rt) {
     TcSched s;
     s.nrt = (n_rows + BT - 1) / BT;
     s.nct = (n_cols + BT - 1) / BT;
     s.nchunks = (s.nct + CHUNK - 1) / CHUNK;
+    s.rt = rt;
+    s.nru = (s.nrt + rt - 1) / rt;
     long long u = 0;
     for (int c = 0; c < s.nchunks; ++c) u += chunk_rows(s, c, tri, lo, hi);
     s.units = (unsigned)u;
     return s;
 }
-// Unit u -> row block and column tiles [t0, t1); false when it holds none.
+// Unit u -> first row block, row blocks in the unit and column tiles [t0, t1);
+// false when it holds none.
 __device__ __forceinline__ bool tc_unit(const TcSched &s, unsigned u, int tri, int lo, int hi,
-                                        int &rb, int &t0, int &t1) {
+                                        int &rb, int &nrow, int &t0, int &t1) {
     int c = 0;
     for (; c < s.nchunks; ++c) {
         const unsigned r = (unsigned)chunk_rows(s, c, tri, lo, hi);
         if (u < r) break;
         u -= r;
     }
-    rb = chunk_first_row(c, tri, hi) + (int)u;
+    rb = (chunk_first_row(s, c, tri, hi) + (int)u) * s.rt;
+    nrow = min(s.rt, s.nrt - rb);
     t0 = max(c * CHUNK, tri ? rb + lo : 0);
     t1 = min(min((c + 1) * CHUNK, s.nct), (tri && hi >= 0) ? rb + hi : s.nct);
     return t0 < t1;
 }
 
 // ---- the kernel --------------------------------------------------------------------
-template <int MODE, int KIND>
+template <int MODE, int KIND, int RT>
 __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
     Ctrl *ctrl = a.ctrl;
     if (ctrl->tc_kind != KIND) return;     // another path was selected for this data
@@ -350,10 +370,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
 
     extern __shared__ __align__(1024) uint8_t smem[];
     const int S = a.stages, G = a.group;
-    // layout: [A0 | A1 | stage 0 .. stage S-1 | barriers | meta | misc]; a stage
-    // holds up to G column tiles back to back, then G x BT ints of aux data
+    // layout: [A0 | A1 | stage 0 .. stage S-1 | barriers | meta | misc]; an A
+    // buffer holds the RT row tiles of a unit, a stage up to G column tiles back
+    // to back, then G x BT ints of aux data
+    const size_t abuf_bytes = (size_t)RT * a.tile_bytes_max;
     uint8_t *sA = smem;
-    uint8_t *sStage = smem + 2 * (size_t)a.tile_bytes_max;
+    uint8_t *sStage = smem + 2 * abuf_bytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + (size_t)S * a.stage_bytes);
     uint64_t *b_full = bars, *b_empty = bars + TC_MAX_STAGES;
     uint64_t *a_full = bars + 2 * TC_MAX_STAGES, *a_empty = a_full + 2;
@@ -403,13 +425,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const int lo = a.band ? a.blo : 0, hi = a.band ? a.bhi : -1;
-    const TcSched sc = tc_sched(n_rows, n_cols, a.tri, lo, hi);
+    const TcSched sc = tc_sched(n_rows, n_cols, a.tri, lo, hi, RT);
 
     if (warp == PRODUCER_WARP) {
         // The whole warp walks the schedule; the copies of consecutive stages
         // are issued by different lanes, since one thread's bulk copies
         // complete one after another.
         int k = 0, ua = 0, a_issued = 0;
+        unsigned lane_turn = 0;   // next lane to issue a stage part
+        // column tiles per copy: about PART_BYTES, and at most B_LANES copies a
+        // stage, the aux ints included
+        const int maxp = B_LANES - (AUX ? 1 : 0);
+        const int tpp = max(max(1, PART_BYTES / (int)tile_bytes), (G + maxp - 1) / maxp);
         bool ok = true;
         // Culling by tile boxes is exact for integer data within the exactness
         // bound: box gaps are integers, their squared sum is exact, and every
@@ -421,8 +448,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             if (lane == 0) u = atomicAdd(a.ctr, 1u);
             u = __shfl_sync(FULL, u, 0);
             if (u >= sc.units) break;
-            int rb, t0, t1;
-            if (!tc_unit(sc, u, a.tri, lo, hi, rb, t0, t1)) continue;
+            int rb, nrow, t0, t1;
+            if (!tc_unit(sc, u, a.tri, lo, hi, rb, nrow, t0, t1)) continue;
             const int ab = ua & 1;
             bool started = false;   // this unit's row tile has been loaded
             // Stages of up to G consecutive tiles over [ts, te); the unit's row
@@ -435,10 +462,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                         if (!__all_sync(FULL, mbar_spin(smem_addr(&a_empty[ab]), ((ua >> 1) & 1) ^ 1,
                                                         s_abort, ctrl)))
                             return false;
-                        if (lane == ISSUE_LANES + (ua % ISSUE_LANES)) {
-                            mbar_expect_tx(smem_addr(&a_full[ab]), tile_bytes);
-                            bulk_g2s(smem_addr(sA + (size_t)ab * a.tile_bytes_max),
-                                     a.ua + (size_t)rb * tile_bytes, tile_bytes, smem_addr(&a_full[ab]));
+                        if (lane == B_LANES + (ua % A_LANES)) {
+                            // the unit's row tiles are consecutive in the operand array
+                            mbar_expect_tx(smem_addr(&a_full[ab]), (uint32_t)nrow * tile_bytes);
+                            bulk_g2s(smem_addr(sA + (size_t)ab * abuf_bytes), a.ua + (size_t)rb * tile_bytes,
+                                     (uint32_t)nrow * tile_bytes, smem_addr(&a_full[ab]));
                         }
                         a_issued = ua + 1;
                         started = first = true;
@@ -450,23 +478,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                     if (lane == 0) {
                         Meta m;
                         m.rb = rb;
+                        m.nrow = nrow;
                         m.t_first = tf;
                         m.ntiles = nt;
                         m.flags = first ? F_FIRST : 0;
                         m.abuf = ab;
                         meta[s] = m;
                     }
-                    __syncwarp();
-                    if (lane == k % ISSUE_LANES) {
-                        uint8_t *dst = sStage + (size_t)s * a.stage_bytes;
+                    // one arrival with the stage's bytes, then the parts from
+                    // consecutive lanes (the arrival is ordered before them)
+                    if (lane == 0)
                         mbar_expect_tx(smem_addr(&b_full[s]),
                                        (uint32_t)nt * tile_bytes + (AUX ? (uint32_t)nt * BT * 4u : 0u));
-                        bulk_g2s(smem_addr(dst), a.ub + (size_t)tf * tile_bytes, (uint32_t)nt * tile_bytes,
-                                 smem_addr(&b_full[s]));
-                        if (AUX)
+                    __syncwarp();
+                    const int parts = (nt + tpp - 1) / tpp + (AUX ? 1 : 0);
+                    const int j = (lane - (int)(lane_turn % B_LANES) + B_LANES) % B_LANES;
+                    if (lane < B_LANES && j < parts) {
+                        uint8_t *dst = sStage + (size_t)s * a.stage_bytes;
+                        const int ntp = (nt + tpp - 1) / tpp;
+                        if (j < ntp) {
+                            const int t_lo = j * tpp, t_n = min(tpp, nt - t_lo);
+                            bulk_g2s(smem_addr(dst + (size_t)t_lo * tile_bytes),
+                                     a.ub + (size_t)(tf + t_lo) * tile_bytes, (uint32_t)t_n * tile_bytes,
+                                     smem_addr(&b_full[s]));
+                        } else {
                             bulk_g2s(smem_addr(dst + (size_t)G * a.tile_bytes_max), a.aux + (size_t)tf * BT,
                                      (uint32_t)nt * BT * 4u, smem_addr(&b_full[s]));
+                        }
                     }
+                    lane_turn += (unsigned)parts;
                     ++k;
                 }
                 return true;
@@ -478,7 +518,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                 // more from the row tile's box is skipped with one test;
                 // otherwise each lane tests one tile of the group, and runs of
                 // kept tiles become stages.
-                const float *rbx = a.rbox + (size_t)rb * 2 * a.d;
+                // box of the unit's row tiles: the union of theirs
+                const float *rbx0 = a.rbox + (size_t)rb * 2 * a.d;
+                const float *rbx1 = a.rbox + (size_t)(rb + nrow - 1) * 2 * a.d;
+                auto rlo = [&](int kk) { return fminf(rbx0[2 * kk], rbx1[2 * kk]); };
+                auto rhi = [&](int kk) { return fmaxf(rbx0[2 * kk + 1], rbx1[2 * kk + 1]); };
                 for (int g = t0 / 32; g * 32 < t1 && ok; ++g) {
                     {
                         // every lane gets the same sum: up to 16 dimensions each
@@ -488,8 +532,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                         float g2 = 0.f;
                         const bool split = a.d > 16;
                         for (int kk = split ? lane : 0; kk < a.d; kk += split ? 32 : 1) {
-                            const float gap = fmaxf(0.f, fmaxf(gbx[2 * kk] - rbx[2 * kk + 1],
-                                                               rbx[2 * kk] - gbx[2 * kk + 1]));
+                            const float gap = fmaxf(0.f, fmaxf(gbx[2 * kk] - rhi(kk), rlo(kk) - gbx[2 * kk + 1]));
                             g2 = fmaf(gap, gap, g2);
                         }
                         if (split) {
@@ -505,8 +548,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                         const float *cbx = a.cbox + (size_t)tt * 2 * a.d;
                         float g2 = 0.f;
                         for (int kk = 0; kk < a.d; ++kk) {
-                            const float g = fmaxf(0.f, fmaxf(cbx[2 * kk] - rbx[2 * kk + 1],
-                                                             rbx[2 * kk] - cbx[2 * kk + 1]));
+                            const float g = fmaxf(0.f, fmaxf(cbx[2 * kk] - rhi(kk), rlo(kk) - cbx[2 * kk + 1]));
                             g2 = fmaf(g, g, g2);
                         }
                         keep = g2 < cthr;   // some pair could be a neighbour
@@ -557,21 +599,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                 }
                 // descriptors of the row tile and of the stage's first tile; a
                 // K step is 256 bytes further, 16 in the descriptor's address field
-                const uint64_t da0 = umma_desc(smem_addr(sA + (size_t)m.abuf * a.tile_bytes_max), sbo);
+                const uint64_t da0 = umma_desc(smem_addr(sA + (size_t)m.abuf * abuf_bytes), sbo);
                 const uint64_t ds0 = umma_desc(smem_addr(sStage + (size_t)s * a.stage_bytes), sbo);
-                for (int i = 0; 2 * i < m.ntiles; ++i, ++it) {
-                    const int b = it % NACC;
-                    if (!(ok = mbar_spin(smem_addr(&acc_empty[b]), ((it / NACC) & 1) ^ 1, s_abort, ctrl)))
-                        break;
-                    tc_fence_after();
+                // item (i, r): row tile r of the unit against column tiles 2i, 2i + 1
+                for (int i = 0; 2 * i < m.ntiles && ok; ++i) {
                     // a pair of consecutive column tiles is one 256-row B operand
                     const uint64_t db0 = ds0 + (uint64_t)(((uint32_t)(2 * i) * tile_bytes) >> 4);
                     const uint32_t idesc = 2 * i + 1 < m.ntiles ? idesc256 : idesc128;
-                    for (int ks = 0; ks < ksteps; ++ks)
-                        umma<KIND>(tmem + (uint32_t)(b * ACC_COLS), da0 + (uint64_t)(16 * ks),
-                                   db0 + (uint64_t)(16 * ks), idesc, ks > 0 ? 1u : 0u);
-                    issued = true;
-                    umma_commit(smem_addr(&acc_full[b]));
+                    for (int r = 0; r < (RT == 1 ? 1 : m.nrow); ++r, ++it) {
+                        const int b = it % NACC;
+                        if (!(ok = mbar_spin(smem_addr(&acc_empty[b]), ((it / NACC) & 1) ^ 1, s_abort, ctrl)))
+                            break;
+                        tc_fence_after();
+                        const uint64_t da = da0 + (uint64_t)(((uint32_t)r * tile_bytes) >> 4);
+                        for (int ks = 0; ks < ksteps; ++ks)
+                            umma<KIND>(tmem + (uint32_t)(b * ACC_COLS), da + (uint64_t)(16 * ks),
+                                       db0 + (uint64_t)(16 * ks), idesc, ks > 0 ? 1u : 0u);
+                        issued = true;
+                        umma_commit(smem_addr(&acc_full[b]));
+                    }
                 }
                 if (!ok) break;
                 ++k;
@@ -590,8 +636,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         // trip is bounded by how fast TMEM is drained, which takes every warp.
         const int wq = warp & 3, cq = warp >> 2;
         const int row = wq * 32 + lane;
-        int last_rb = -1, acc = -1;             // UNION: a known ancestor of this row's point
-        int lastq = -1;                         // UNION: last staged parent joined to this row
+        // per row tile r of the unit (at most two): UNION keeps a known ancestor
+        // of this row's point and the last staged parent joined to it
+        int last_rb = -1, acc0 = -1, acc1 = -1, lastq0 = -1, lastq1 = -1;
         int k = 0, it = 0;
         for (;;) {
             const int s = k % S;
@@ -599,126 +646,153 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             if (!__all_sync(FULL, mbar_spin(smem_addr(&b_full[s]), (k / S) & 1, s_abort, ctrl))) break;
             const Meta m = meta[s];
             if (m.flags & F_TERM) break;
-            const int p = m.rb * BT + row;
-            const bool rowvalid = p < n_rows;
+            const int p0 = m.rb * BT + row, p1 = p0 + BT;
+            const bool valid0 = p0 < n_rows, valid1 = RT > 1 && m.nrow > 1 && p1 < n_rows;
             if (MODE == SWEEP_UNION && m.rb != last_rb) {
-                acc = rowvalid ? tc_find(a.parent, p, ctrl) : -1;
+                acc0 = valid0 ? tc_find(a.parent, p0, ctrl) : -1;
+                if (RT > 1) acc1 = valid1 ? tc_find(a.parent, p1, ctrl) : -1;
                 last_rb = m.rb;
-                lastq = -1;
+                lastq0 = lastq1 = -1;
             }
             const int *saux = reinterpret_cast<const int *>(sStage + (size_t)s * a.stage_bytes +
                                                             (size_t)G * a.tile_bytes_max);
-            int rowadd = 0, rowmin = 0x7fffffff;
+            int rowadd0 = 0, rowadd1 = 0, rowmin0 = 0x7fffffff, rowmin1 = 0x7fffffff;
             bool ok = true;
-            for (int i = 0; 2 * i < m.ntiles; ++i, ++it) {
-                const int b = it % NACC;
-                if (!(ok = __all_sync(FULL, mbar_spin(smem_addr(&acc_full[b]), (it / NACC) & 1, s_abort, ctrl))))
-                    break;
-                tc_fence_after();
-                const int ti = 2 * i + (cq >> 1);     // tile within the stage
-                const bool have = ti < m.ntiles;      // warp-uniform
-                const int tile = m.t_first + ti;
-                const bool diag = a.tri && tile == m.rb;
-                // f32 accumulator: v0, v1 = columns 0-31, 32-63 of the warp's 64;
-                // f16 accumulator: v0 = all 64 columns, two per register
-                uint32_t v0[32], v1[32];
-                if (have) {
-                    const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) +
-                                           (uint32_t)(b * ACC_COLS + cq * 64);
-                    if (KIND == TC_F16) {
-                        tmem_ld32p(taddr, v0);
-                    } else {
-                        tmem_ld32(taddr, v0);
-                        tmem_ld32(taddr + 32, v1);
+            for (int i = 0; 2 * i < m.ntiles && ok; ++i) {
+                for (int r = 0; r < (RT == 1 ? 1 : m.nrow); ++r, ++it) {
+                    const int b = it % NACC;
+                    if (!(ok = __all_sync(FULL, mbar_spin(smem_addr(&acc_full[b]), (it / NACC) & 1, s_abort, ctrl))))
+                        break;
+                    tc_fence_after();
+                    const int ti = 2 * i + (cq >> 1);     // tile within the stage
+                    const int tile = m.t_first + ti;
+                    const int rt = m.rb + r;              // row tile of this item
+                    // warp-uniform: the tile exists and, in the triangle, is not
+                    // below this row tile (that pair belongs to the other order)
+                    const bool have = ti < m.ntiles && !(RT > 1 && a.tri && tile < rt);
+                    const bool diag = a.tri && tile == rt;
+                    // f32 accumulator: v0, v1 = columns 0-31, 32-63 of the warp's 64;
+                    // f16 accumulator: v0 = all 64 columns, two per register
+                    uint32_t v0[32], v1[32];
+                    if (have) {
+                        const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) +
+                                               (uint32_t)(b * ACC_COLS + cq * 64);
+                        if (KIND == TC_F16) {
+                            tmem_ld32p(taddr, v0);
+                        } else {
+                            tmem_ld32(taddr, v0);
+                            tmem_ld32(taddr + 32, v1);
+                        }
+                        tmem_ld_wait();
                     }
-                    tmem_ld_wait();
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&acc_empty[b]));
-                if (!have) continue;
-                const uint32_t neg = KIND == TC_F16 ? (or32(v0) & 0x80008000u) : (or64(v0, v1) >> 31);
-                if (!__any_sync(FULL, rowvalid && neg)) continue;
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_addr(&acc_empty[b]));
+                    if (!have) continue;
+                    const int p = r ? p1 : p0;
+                    const bool rowvalid = r ? valid1 : valid0;
+                    const uint32_t neg = KIND == TC_F16 ? (or32(v0) & 0x80008000u) : (or64(v0, v1) >> 31);
+                    if (!__any_sync(FULL, rowvalid && neg)) continue;
+                    int rowadd = 0, rowmin = 0x7fffffff;
+                    int acc = r ? acc1 : acc0, lastq = r ? lastq1 : lastq0;
 #pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
-                    const int cb = (cq & 1) * 64 + blk * 32;   // column offset in the tile
-                    const int qbase = tile * BT + cb;
-                    // bit c of mask = (w_c < 0) for the block's 32 columns
-                    uint32_t mask;
-                    if (KIND == TC_F16) {
-                        uint32_t o = 0;
+                    for (int blk = 0; blk < 2; ++blk) {
+                        const int cb = (cq & 1) * 64 + blk * 32;   // column offset in the tile
+                        const int qbase = tile * BT + cb;
+                        // bit c of mask = (w_c < 0) for the block's 32 columns
+                        uint32_t mask;
+                        if (KIND == TC_F16) {
+                            uint32_t o = 0;
 #pragma unroll
-                        for (int c = 0; c < 16; c += 2) o |= v0[16 * blk + c] | v0[16 * blk + c + 1];
-                        if (!__any_sync(FULL, rowvalid && (o & 0x80008000u))) continue;
-                        // two 16-column chains; register j holds columns 2j (bit 15)
-                        // and 2j + 1 (bit 31)
-                        uint32_t m16[2] = {0u, 0u};
+                            for (int c = 0; c < 16; c += 2) o |= v0[16 * blk + c] | v0[16 * blk + c + 1];
+                            if (!__any_sync(FULL, rowvalid && (o & 0x80008000u))) continue;
+                            // two 16-column chains; register j holds columns 2j (bit 15)
+                            // and 2j + 1 (bit 31)
+                            uint32_t m16[2] = {0u, 0u};
 #pragma unroll
-                        for (int j = 7; j >= 0; --j)
+                            for (int j = 7; j >= 0; --j)
 #pragma unroll
-                            for (int g = 0; g < 2; ++g) {
-                                const uint32_t r = v0[16 * blk + 8 * g + j];
-                                m16[g] = __funnelshift_l(r, m16[g], 1);
-                                m16[g] = __funnelshift_l(r << 16, m16[g], 1);
+                                for (int g = 0; g < 2; ++g) {
+                                    const uint32_t rr = v0[16 * blk + 8 * g + j];
+                                    m16[g] = __funnelshift_l(rr, m16[g], 1);
+                                    m16[g] = __funnelshift_l(rr << 16, m16[g], 1);
+                                }
+                            mask = m16[0] | (m16[1] << 16);
+                        } else {
+                            uint32_t (&v)[32] = blk ? v1 : v0;
+                            uint32_t o = 0;
+#pragma unroll
+                            for (int c = 0; c < 32; c += 2) o |= v[c] | v[c + 1];
+                            if (!__any_sync(FULL, rowvalid && (o >> 31))) continue;
+                            // four independent 8-column chains
+                            uint32_t m8[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                            for (int c = 7; c >= 0; --c)
+#pragma unroll
+                                for (int g = 0; g < 4; ++g) m8[g] = __funnelshift_l(v[8 * g + c], m8[g], 1);
+                            mask = m8[0] | (m8[1] << 8) | (m8[2] << 16) | (m8[3] << 24);
+                        }
+                        const int nv = n_cols - qbase;
+                        mask &= nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
+                        if (!rowvalid) mask = 0;
+                        if (MODE == SWEEP_COUNT) {
+                            const int nh = __popc(mask);
+                            rowadd += nh;
+                            if (!diag) {   // the diagonal tile is counted from both sides already
+                                if (__any_sync(FULL, nh > 2)) {
+                                    // many neighbours: per-column sums through a bit transpose
+                                    const int cc = __popc(warp_transpose32(mask, lane));
+                                    if (cc) atomicAdd(a.cnt + qbase + lane, cc);
+                                } else {
+                                    // few: credit each neighbour's column directly
+                                    while (mask) {
+                                        const int cq2 = __ffs(mask) - 1;
+                                        mask &= mask - 1;
+                                        atomicAdd(a.cnt + qbase + cq2, 1);
+                                    }
+                                }
                             }
-                        mask = m16[0] | (m16[1] << 16);
-                    } else {
-                        uint32_t (&v)[32] = blk ? v1 : v0;
-                        uint32_t o = 0;
-#pragma unroll
-                        for (int c = 0; c < 32; c += 2) o |= v[c] | v[c + 1];
-                        if (!__any_sync(FULL, rowvalid && (o >> 31))) continue;
-                        // four independent 8-column chains
-                        uint32_t m8[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                        for (int c = 7; c >= 0; --c)
-#pragma unroll
-                            for (int g = 0; g < 4; ++g) m8[g] = __funnelshift_l(v[8 * g + c], m8[g], 1);
-                        mask = m8[0] | (m8[1] << 8) | (m8[2] << 16) | (m8[3] << 24);
-                    }
-                    const int nv = n_cols - qbase;
-                    mask &= nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
-                    if (!rowvalid) mask = 0;
-                    if (MODE == SWEEP_COUNT) {
-                        const int nh = __popc(mask);
-                        rowadd += nh;
-                        if (!diag) {   // the diagonal tile is counted from both sides already
-                            if (__any_sync(FULL, nh > 2)) {
-                                // many neighbours: per-column sums through a bit transpose
-                                const int cc = __popc(warp_transpose32(mask, lane));
-                                if (cc) atomicAdd(a.cnt + qbase + lane, cc);
-                            } else {
-                                // few: credit each neighbour's column directly
-                                while (mask) {
-                                    const int cq2 = __ffs(mask) - 1;
-                                    mask &= mask - 1;
-                                    atomicAdd(a.cnt + qbase + cq2, 1);
+                        } else {
+                            while (mask) {
+                                const int cq2 = __ffs(mask) - 1;
+                                mask &= mask - 1;
+                                const int q = qbase + cq2;
+                                const int aq = saux[ti * BT + cb + cq2];
+                                if (MODE == SWEEP_UNION) {
+                                    if (diag && q <= p) continue;
+                                    if (aq == acc || aq == lastq) continue;
+                                    lastq = aq;   // aq joins this row's set for good
+                                    acc = tc_unite(a.parent, acc, aq, ctrl);
+                                } else {
+                                    rowmin = min(rowmin, aq);
                                 }
                             }
                         }
+                    }
+                    if (r) {
+                        rowadd1 += rowadd;
+                        rowmin1 = min(rowmin1, rowmin);
+                        acc1 = acc;
+                        lastq1 = lastq;
                     } else {
-                        while (mask) {
-                            const int cq2 = __ffs(mask) - 1;
-                            mask &= mask - 1;
-                            const int q = qbase + cq2;
-                            const int aq = saux[ti * BT + cb + cq2];
-                            if (MODE == SWEEP_UNION) {
-                                if (diag && q <= p) continue;
-                                if (aq == acc || aq == lastq) continue;
-                                lastq = aq;   // aq joins this row's set for good
-                                acc = tc_unite(a.parent, acc, aq, ctrl);
-                            } else {
-                                rowmin = min(rowmin, aq);
-                            }
-                        }
+                        rowadd0 += rowadd;
+                        rowmin0 = min(rowmin0, rowmin);
+                        acc0 = acc;
+                        lastq0 = lastq;
                     }
                 }
             }
             if (!ok) break;
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&b_empty[s]));
-            if (MODE == SWEEP_COUNT && rowadd) atomicAdd(a.cnt + p, rowadd);
-            if (MODE == SWEEP_BORDER && rowmin != 0x7fffffff) atomicMin(a.labels + a.candidx[p], rowmin);
+            if (MODE == SWEEP_COUNT) {
+                if (rowadd0) atomicAdd(a.cnt + p0, rowadd0);
+                if (RT > 1 && rowadd1) atomicAdd(a.cnt + p1, rowadd1);
+            }
+            if (MODE == SWEEP_BORDER) {
+                if (rowmin0 != 0x7fffffff) atomicMin(a.labels + a.candidx[p0], rowmin0);
+                if (RT > 1 && rowmin1 != 0x7fffffff) atomicMin(a.labels + a.candidx[p1], rowmin1);
+            }
             ++k;
         }
     }
@@ -731,10 +805,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
 }
 
 // Bytes of shared memory the kernel needs.
-size_t tc_smem_bytes(int tile_bytes, int stage_bytes, int stages) {
-    return 2 * (size_t)tile_bytes + (size_t)stages * stage_bytes +
+size_t tc_smem_bytes(int tile_bytes, int rows, int stage_bytes, int stages) {
+    return 2 * (size_t)rows * tile_bytes + (size_t)stages * stage_bytes +
            (2 * TC_MAX_STAGES + 4 + 2 * NACC + 1) * sizeof(uint64_t) + TC_MAX_STAGES * sizeof(Meta) +
            16;
+}
+
+// Row blocks per unit.  A unit costs a row-tile load and the fill of its first
+// stage before its first MMA; when tile culling leaves a unit a few short runs
+// of column tiles, that cost dominates, and two row blocks per unit halve the
+// number of units and copy every kept column tile once for both (the culling
+// box is then the union of the two row tiles' boxes).  A full-length unit gains
+// nothing from it and pays for the second row's bookkeeping in the epilogue.
+// The border sweep keeps one row block: its candidate tiles are sparse.
+// DBSCAN_TC_ROWS overrides: one digit (1 or 2) for every sweep, or three for
+// count, union and border.
+int tc_rows(int mode, int cull) {
+    if (const char *e = getenv("DBSCAN_TC_ROWS")) {
+        const size_t len = strlen(e);
+        const char c = len == 1 ? e[0] : (len == 3 ? e[mode] : '0');
+        if (c == '1') return 1;
+        if (c == '2') return 2;
+    }
+    return cull && mode != SWEEP_BORDER ? 2 : 1;
 }
 
 template <int MODE, int KIND>
@@ -744,21 +837,23 @@ cudaError_t run_tc(TcArgs a, const Layout &L, cudaStream_t s) {
     const int ntb = tc_nt_bound(KIND, L.eps2);
     const int kb = tc_kbytes(KIND, L.d, ntb);
     if (L.umma_tile_bytes == 0 || !tc_fits(KIND, L.d, ntb)) return cudaSuccess;   // never selected
-    auto kernel = k_sweep_tc<MODE, KIND>;
     const int tile = 128 * kb;
     const int aux = MODE != SWEEP_COUNT ? BT * 4 : 0;
     const size_t budget = 224 * 1024;
+    const int rows = tc_rows(MODE, a.cull);
+    auto kernel = rows == 2 ? k_sweep_tc<MODE, KIND, 2> : k_sweep_tc<MODE, KIND, 1>;
+    const size_t abufs = 2 * (size_t)rows * tile;   // two buffers of a unit's row tiles
     // Few, large stages: every stage costs a round of barrier handshakes
     // between the producer, the MMA thread and all epilogue warps, so the
     // group is the largest even number of tiles (<= 32) for which two stages
-    // and the two row tiles fit; deeper rings did not help.
+    // and the row buffers fit; what is left takes further stages.
     int group = TC_MAX_GROUP;
-    while (group > 2 && 2 * (size_t)tile + 2 * (size_t)group * (tile + aux) > budget) group -= 2;
+    while (group > 2 && abufs + 2 * (size_t)group * (tile + aux) > budget) group -= 2;
     const int stage_bytes = group * (tile + aux);
-    int stages = (int)((budget - 2 * (size_t)tile) / stage_bytes);
+    int stages = (int)((budget - abufs) / stage_bytes);
     if (stages > TC_MAX_STAGES) stages = TC_MAX_STAGES;
     if (stages < 2) stages = 2;
-    size_t smem = tc_smem_bytes(tile, stage_bytes, stages);
+    size_t smem = tc_smem_bytes(tile, rows, stage_bytes, stages);
     if (smem < 120 * 1024) smem = 120 * 1024;   // one CTA per SM: it owns all of TMEM
     cudaError_t e = cudaFuncSetAttribute((const void *)kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
