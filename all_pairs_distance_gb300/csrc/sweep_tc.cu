@@ -581,46 +581,62 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         }
     } else if (warp == MMA_WARP) {
         if (lane == 0) {
+            // One thread issues every MMA, and its loop is a dependent chain
+            // on the critical path of the accumulator round trip: everything
+            // it needs is kept in registers -- barrier addresses, descriptors
+            // (a descriptor is a constant plus address >> 4 in bits 0-13, and
+            // every shared-memory address is below 2^18), stage index and
+            // phase -- and nothing is divided.
             const int fmt = KIND == TC_TF32 ? 2 : (KIND == TC_BF16 ? 1 : 0);
             const bool f32acc = KIND != TC_F16;
             const uint32_t idesc256 = umma_idesc(fmt, 256, f32acc), idesc128 = umma_idesc(fmt, 128, f32acc);
-            int k = 0, ua = 0, it = 0;
+            const uint64_t dbase = umma_desc(0, sbo);
+            const uint32_t bar_bf = smem_addr(b_full), bar_af = smem_addr(a_full), bar_ae = smem_addr(a_empty);
+            const uint32_t bar_accf = smem_addr(acc_full), bar_acce = smem_addr(acc_empty);
+            const uint64_t dA0 = dbase + (smem_addr(sA) >> 4), dA1 = dbase + (smem_addr(sA + abuf_bytes) >> 4);
+            const uint64_t dS0 = dbase + (smem_addr(sStage) >> 4);
+            const uint32_t dstage = (uint32_t)a.stage_bytes >> 4, dpair = (2u * tile_bytes) >> 4,
+                           drow = tile_bytes >> 4;
+            int s = 0, ua = 0;
+            uint32_t sph = 0;           // phase of the current use of stage s
+            uint32_t b = 0, eph = 1;    // accumulator of the next item, and the phase of its release
             bool issued = false, ok = true;
             for (;;) {
-                const int s = k % S;
-                if (!mbar_spin(smem_addr(&b_full[s]), (k / S) & 1, s_abort, ctrl)) break;
+                if (!mbar_spin(bar_bf + 8u * s, sph, s_abort, ctrl)) break;
                 const Meta m = meta[s];
                 if (m.flags & F_TERM) break;
                 if (m.flags & F_FIRST) {
-                    // the previous unit's row tile has been read by every MMA issued so far
-                    if (ua > 0) umma_commit(smem_addr(&a_empty[(ua - 1) & 1]));
-                    if (!mbar_spin(smem_addr(&a_full[m.abuf]), (ua >> 1) & 1, s_abort, ctrl)) break;
+                    // the previous unit's row tiles have been read by every MMA issued so far
+                    if (ua > 0) umma_commit(bar_ae + 8u * ((ua - 1) & 1));
+                    if (!mbar_spin(bar_af + 8u * m.abuf, (ua >> 1) & 1, s_abort, ctrl)) break;
                     ++ua;
                 }
-                // descriptors of the row tile and of the stage's first tile; a
-                // K step is 256 bytes further, 16 in the descriptor's address field
-                const uint64_t da0 = umma_desc(smem_addr(sA + (size_t)m.abuf * abuf_bytes), sbo);
-                const uint64_t ds0 = umma_desc(smem_addr(sStage + (size_t)s * a.stage_bytes), sbo);
-                // item (i, r): row tile r of the unit against column tiles 2i, 2i + 1
-                for (int i = 0; 2 * i < m.ntiles && ok; ++i) {
-                    // a pair of consecutive column tiles is one 256-row B operand
-                    const uint64_t db0 = ds0 + (uint64_t)(((uint32_t)(2 * i) * tile_bytes) >> 4);
+                const uint64_t da0 = m.abuf ? dA1 : dA0;
+                // item (i, r): row tile r of the unit against column tiles 2i, 2i + 1;
+                // a pair of consecutive column tiles is one 256-row B operand, and
+                // a K step is 256 bytes further (16 in the address field)
+                uint64_t db = dS0 + (uint64_t)((uint32_t)s * dstage);
+                for (int i = 0; 2 * i < m.ntiles && ok; ++i, db += dpair) {
                     const uint32_t idesc = 2 * i + 1 < m.ntiles ? idesc256 : idesc128;
-                    for (int r = 0; r < (RT == 1 ? 1 : m.nrow); ++r, ++it) {
-                        const int b = it % NACC;
-                        if (!(ok = mbar_spin(smem_addr(&acc_empty[b]), ((it / NACC) & 1) ^ 1, s_abort, ctrl)))
-                            break;
+                    for (int r = 0; r < (RT == 1 ? 1 : m.nrow); ++r) {
+                        if (!(ok = mbar_spin(bar_acce + 8u * b, eph, s_abort, ctrl))) break;
                         tc_fence_after();
-                        const uint64_t da = da0 + (uint64_t)(((uint32_t)r * tile_bytes) >> 4);
+                        const uint64_t da = da0 + (uint64_t)((uint32_t)r * drow);
+                        const uint32_t td = tmem + b * (uint32_t)ACC_COLS;
                         for (int ks = 0; ks < ksteps; ++ks)
-                            umma<KIND>(tmem + (uint32_t)(b * ACC_COLS), da + (uint64_t)(16 * ks),
-                                       db0 + (uint64_t)(16 * ks), idesc, ks > 0 ? 1u : 0u);
+                            umma<KIND>(td, da + (uint64_t)(16 * ks), db + (uint64_t)(16 * ks), idesc,
+                                       ks > 0 ? 1u : 0u);
                         issued = true;
-                        umma_commit(smem_addr(&acc_full[b]));
+                        umma_commit(bar_accf + 8u * b);
+                        eph ^= b;   // accumulator 0 is next released one phase later
+                        b ^= 1u;
                     }
                 }
                 if (!ok) break;
-                ++k;
+                if (++s == S) {
+                    s = 0;
+                    sph ^= 1u;
+                }
             }
             if (issued) {   // no MMA may be in flight when TMEM is freed
                 umma_commit(smem_addr(drain_bar));
@@ -639,11 +655,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         // per row tile r of the unit (at most two): UNION keeps a known ancestor
         // of this row's point and the last staged parent joined to it
         int last_rb = -1, acc0 = -1, acc1 = -1, lastq0 = -1, lastq1 = -1;
-        int k = 0, it = 0;
+        int s = 0, it = 0;
+        uint32_t sph = 0;   // phase of the current use of stage s
         for (;;) {
-            const int s = k % S;
             // every lane waits; the warp goes on only if all lanes saw the phase
-            if (!__all_sync(FULL, mbar_spin(smem_addr(&b_full[s]), (k / S) & 1, s_abort, ctrl))) break;
+            if (!__all_sync(FULL, mbar_spin(smem_addr(&b_full[s]), sph, s_abort, ctrl))) break;
             const Meta m = meta[s];
             if (m.flags & F_TERM) break;
             const int p0 = m.rb * BT + row, p1 = p0 + BT;
@@ -793,7 +809,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                 if (rowmin0 != 0x7fffffff) atomicMin(a.labels + a.candidx[p0], rowmin0);
                 if (RT > 1 && rowmin1 != 0x7fffffff) atomicMin(a.labels + a.candidx[p1], rowmin1);
             }
-            ++k;
+            if (++s == S) {
+                s = 0;
+                sph ^= 1u;
+            }
         }
     }
     tc_fence_before();
