@@ -515,36 +515,83 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                 ok = emit(t0, t1);
             } else {
                 // Column tiles go by groups of 32: a group whose box is eps or
-                // more from the row tile's box is skipped with one test;
-                // otherwise each lane tests one tile of the group, and runs of
-                // kept tiles become stages.
-                // box of the unit's row tiles: the union of theirs
+                // more from the row tiles' box is skipped with one test;
+                // otherwise every tile of the group is tested, and runs of kept
+                // tiles become stages.  Gaps are integers, so every sum below is
+                // exact in any order.
+                // The unit's box is the union of its row tiles' boxes.
                 const float *rbx0 = a.rbox + (size_t)rb * 2 * a.d;
                 const float *rbx1 = a.rbox + (size_t)(rb + nrow - 1) * 2 * a.d;
                 auto rlo = [&](int kk) { return fminf(rbx0[2 * kk], rbx1[2 * kk]); };
                 auto rhi = [&](int kk) { return fmaxf(rbx0[2 * kk + 1], rbx1[2 * kk + 1]); };
+                // d > 4: the lanes split the dimensions (lane and lane + 32), each
+                // keeping its share of the unit's box in registers
+                const bool split = a.d > 4;
+                float rl0 = 0.f, rh0 = 0.f, rl1 = 0.f, rh1 = 0.f;
+                if (split) {
+                    if (lane < a.d) { rl0 = rlo(lane); rh0 = rhi(lane); }
+                    if (lane + 32 < a.d) { rl1 = rlo(lane + 32); rh1 = rhi(lane + 32); }
+                }
+                // this lane's part of the squared gap between the unit's box and box bx
+                auto part = [&](const float *bx) -> float {
+                    float g2 = 0.f;
+                    if (lane < a.d) {
+                        const float2 v = *reinterpret_cast<const float2 *>(bx + 2 * lane);
+                        const float gp = fmaxf(0.f, fmaxf(v.x - rh0, rl0 - v.y));
+                        g2 = gp * gp;
+                    }
+                    if (lane + 32 < a.d) {
+                        const float2 v = *reinterpret_cast<const float2 *>(bx + 2 * (lane + 32));
+                        const float gp = fmaxf(0.f, fmaxf(v.x - rh1, rl1 - v.y));
+                        g2 = fmaf(gp, gp, g2);
+                    }
+                    return g2;
+                };
                 for (int g = t0 / 32; g * 32 < t1 && ok; ++g) {
                     {
-                        // every lane gets the same sum: up to 16 dimensions each
-                        // lane adds them all; beyond, lanes split the dimensions
-                        // (integer gaps: the sum is exact in any order)
+                        // every lane gets the same sum
                         const float *gbx = a.cgbox + (size_t)g * 2 * a.d;
                         float g2 = 0.f;
-                        const bool split = a.d > 16;
-                        for (int kk = split ? lane : 0; kk < a.d; kk += split ? 32 : 1) {
-                            const float gap = fmaxf(0.f, fmaxf(gbx[2 * kk] - rhi(kk), rlo(kk) - gbx[2 * kk + 1]));
-                            g2 = fmaf(gap, gap, g2);
-                        }
                         if (split) {
+                            g2 = part(gbx);
 #pragma unroll
                             for (int o = 16; o > 0; o >>= 1) g2 += __shfl_xor_sync(FULL, g2, o);
+                        } else {
+                            for (int kk = 0; kk < a.d; ++kk) {
+                                const float gap = fmaxf(0.f, fmaxf(gbx[2 * kk] - rhi(kk), rlo(kk) - gbx[2 * kk + 1]));
+                                g2 = fmaf(gap, gap, g2);
+                            }
                         }
                         if (!(g2 < cthr)) continue;
                     }
                     const int w0 = g * 32;
                     const int tt = w0 + lane;
                     bool keep = false;
-                    if (tt >= t0 && tt < t1) {
+                    if (split) {
+                        // every lane's parts for all 32 tiles (tiles outside
+                        // [t0, t1) read an in-range box and are dropped below),
+                        // then a butterfly reduce-scatter: after the round of
+                        // offset o a lane keeps the half of its tiles whose
+                        // index bit o matches its own, so lane t ends with the
+                        // sum for tile t
+                        float pv[32];
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) {
+                            const int tc = min(max(w0 + t, t0), t1 - 1);
+                            pv[t] = part(a.cbox + (size_t)tc * 2 * a.d);
+                        }
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+                            const bool up = (lane & o) != 0;
+#pragma unroll
+                            for (int jj = 0; jj < o; ++jj) {
+                                const float send = up ? pv[jj] : pv[jj + o];
+                                const float mine = up ? pv[jj + o] : pv[jj];
+                                pv[jj] = mine + __shfl_xor_sync(FULL, send, o);
+                            }
+                        }
+                        keep = tt >= t0 && tt < t1 && pv[0] < cthr;
+                    } else if (tt >= t0 && tt < t1) {
                         const float *cbx = a.cbox + (size_t)tt * 2 * a.d;
                         float g2 = 0.f;
                         for (int kk = 0; kk < a.d; ++kk) {
