@@ -168,7 +168,7 @@ int dbscan_neighbor_counts(const void *points, int32_t dtype, int64_t n,
  * Limits and rules:
  *   - problems whose dbscan_workspace_size(n, d, dtype) exceeds
  *     DBSCAN_NOALLOC_SCRATCH_BYTES are rejected with DBSCAN_ERR_UNSUPPORTED
- *     (about 285,000 points at d = 3, 58,000 at d = 64);
+ *     (about 285,000 points at d = 3, 57,000 at d = 64);
  *   - the first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any
  *     stream capture;

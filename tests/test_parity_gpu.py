@@ -321,3 +321,36 @@ def test_culled_matches_oracle(name, path, monkeypatch):
     core, label = gpu_run_culled(P, eps, min_pts, dtype)
     assert_same(core, core_ref, f"{name} [{path}] culled core flags")
     assert_same(label, label_ref, f"{name} [{path}] culled labels")
+
+
+ROW_CASES = {
+    # the tensor-core sweeps take one or two row blocks per unit; DBSCAN_TC_ROWS
+    # forces either for every sweep (one digit) or per sweep (count, union, border)
+    "c4_like_9k_d3": (lambda: synth.scaled("blobs_1m_d3", 9_001, seed=51), 10.0, 8, torch.float32),
+    "c5_like_2k_d64": (lambda: synth.scaled("blobs_500k_d64", 2_177, seed=52), 100.0, 16,
+                       torch.bfloat16),
+    "d16_blobs": (lambda: synth.scaled("blobs_200k_d16", 3_203, seed=53), 120.0, 20, torch.float32),
+    # 9 row tiles: the last unit of two row blocks holds one
+    "odd_tiles_d2": (lambda: synth.scaled("blobs_100k_d2", 1_074, seed=54), 20.0, 4, torch.float32),
+    # fractional data: exact tests off, no tile culling, tensor cores not used
+    "fractional_d3": (lambda: synth.scaled("blobs_1m_d3", 4_001, seed=55) * np.float32(0.5), 5.0, 8,
+                      torch.float32),
+}
+
+
+@pytest.mark.parametrize("rows", ["1", "2", "212", "121"])
+@pytest.mark.parametrize("name", sorted(ROW_CASES))
+def test_row_units_match_oracle(name, rows, monkeypatch):
+    monkeypatch.setenv("DBSCAN_TC_ROWS", rows)
+    make, eps, min_pts, dtype = ROW_CASES[name]
+    P = make()
+    assert len(P) == {"c4_like_9k_d3": 9_001, "c5_like_2k_d64": 2_177, "d16_blobs": 3_203,
+                      "odd_tiles_d2": 1_074, "fractional_d3": 4_001}[name]
+    cnt_ref, core_ref, label_ref = oracle.dbscan(P, eps, min_pts)
+    cnt, core, label = gpu_run(P, eps, min_pts, dtype)
+    assert_same(cnt, cnt_ref, f"{name} [rows {rows}] counts")
+    assert_same(core, core_ref, f"{name} [rows {rows}] core flags")
+    assert_same(label, label_ref, f"{name} [rows {rows}] labels")
+    core_c, label_c = gpu_run_culled(P, eps, min_pts, dtype)
+    assert_same(core_c, core_ref, f"{name} [rows {rows}] culled core flags")
+    assert_same(label_c, label_ref, f"{name} [rows {rows}] culled labels")
