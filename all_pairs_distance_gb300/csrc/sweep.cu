@@ -25,6 +25,7 @@
 //   there.  Only rows with a neighbour take the slow path, which re-tests the
 //   8 pairs one by one and acts on each neighbour pair.
 #include "dbscan_internal.cuh"
+#include "tc_schedule.h"
 
 #include <map>
 #include <mutex>
@@ -45,9 +46,7 @@ constexpr int UNION_WAVES = 2;
 // between waves so that later waves mostly find equal parents in the staged
 // snapshot and never touch global memory.
 static const int kUnionWaveEdges[UNION_WAVES + 1] = {0, 2, -1};
-// Tensor-core union bands: tile distances [edge_b, edge_{b+1}) from the diagonal.
-constexpr int UNION_BANDS = 6;
-static const int kUnionBandEdges[UNION_BANDS + 1] = {0, 2, 4, 8, 16, 32, -1};
+// Tensor-core union bands: UNION_BANDS and kUnionBandEdges in tc_schedule.h.
 
 struct SweepArgs {
     const float *rows;     // staged row points

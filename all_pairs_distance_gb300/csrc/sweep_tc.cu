@@ -39,6 +39,7 @@
 // DBSCAN_ERR_INTERNAL, stops issuing work, waits (bounded) for its own copies
 // and MMAs in flight, frees its TMEM and returns.
 #include "dbscan_internal.cuh"
+#include "tc_schedule.h"
 
 #include <stdlib.h>
 #include <string.h>
@@ -299,64 +300,8 @@ __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
     return x;
 }
 
-// ---- unit schedule ---------------------------------------------------------------
-// Units go column chunk by column chunk (CHUNK tiles each), and within a chunk
-// by row unit: the CTAs working at the same time stream the same chunk of
-// column tiles, which stays in L2 even when the operand arrays do not.  A row
-// unit is rt consecutive row blocks rb .. rb + rt - 1 (rb = rt x its index);
-// every column tile staged for it meets all of them, so a column tile is
-// copied from L2 once per rt row blocks.  A unit is a row unit against the
-// chunk's tiles t with t - rb in [lo, hi) (the whole triangle for the count,
-// a distance band for the union, every tile for the border's rectangle).  In
-// the triangle the pairs (rb + r, t) with t < rb + r are skipped; every pair
-// (r, t) with t >= r still lies in exactly one unit and one band, since bands
-// split t - rb.
-constexpr int CHUNK = 512;
-struct TcSched {
-    int nrt, nct, nchunks, rt, nru;
-    unsigned units;
-};
-// The row units [first, first + count) of chunk c that have at least one tile
-// in it: rb + lo < (c + 1) * CHUNK and, with an upper distance, rb + hi > c * CHUNK.
-__device__ __forceinline__ int chunk_first_row(const TcSched &s, int c, int tri, int hi) {
-    if (!(tri && hi >= 0)) return 0;
-    const int x = c * CHUNK - hi;          // first rb with rb > x
-    return x < 0 ? 0 : x / s.rt + 1;
-}
-__device__ __forceinline__ int chunk_rows(const TcSched &s, int c, int tri, int lo, int hi) {
-    if (!tri) return s.nru;
-    const int lim = (c + 1) * CHUNK - lo;  // rb < lim
-    const int end = lim <= 0 ? 0 : min(s.nru, (lim + s.rt - 1) / s.rt);
-    return max(0, end - chunk_first_row(s, c, tri, hi));
-}
-__device__ __forceinline__ TcSched tc_sched(int n_rows, int n_cols, int tri, int lo, int hi, int rt) {
-    TcSched s;
-    s.nrt = (n_rows + BT - 1) / BT;
-    s.nct = (n_cols + BT - 1) / BT;
-    s.nchunks = (s.nct + CHUNK - 1) / CHUNK;
-    s.rt = rt;
-    s.nru = (s.nrt + rt - 1) / rt;
-    long long u = 0;
-    for (int c = 0; c < s.nchunks; ++c) u += chunk_rows(s, c, tri, lo, hi);
-    s.units = (unsigned)u;
-    return s;
-}
-// Unit u -> first row block, row blocks in the unit and column tiles [t0, t1);
-// false when it holds none.
-__device__ __forceinline__ bool tc_unit(const TcSched &s, unsigned u, int tri, int lo, int hi,
-                                        int &rb, int &nrow, int &t0, int &t1) {
-    int c = 0;
-    for (; c < s.nchunks; ++c) {
-        const unsigned r = (unsigned)chunk_rows(s, c, tri, lo, hi);
-        if (u < r) break;
-        u -= r;
-    }
-    rb = (chunk_first_row(s, c, tri, hi) + (int)u) * s.rt;
-    nrow = min(s.rt, s.nrt - rb);
-    t0 = max(c * CHUNK, tri ? rb + lo : 0);
-    t1 = min(min((c + 1) * CHUNK, s.nct), (tri && hi >= 0) ? rb + hi : s.nct);
-    return t0 < t1;
-}
+// ---- unit schedule: tc_schedule.h ----
+static_assert(TC_TILE == BT, "the schedule counts tiles of BT points");
 
 // ---- the kernel --------------------------------------------------------------------
 template <int MODE, int KIND, int RT>
@@ -731,8 +676,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                     const int tile = m.t_first + ti;
                     const int rt = m.rb + r;              // row tile of this item
                     // warp-uniform: the tile exists and, in the triangle, is not
-                    // below this row tile (that pair belongs to the other order)
-                    const bool have = ti < m.ntiles && !(RT > 1 && a.tri && tile < rt);
+                    // below this row tile (that pair belongs to the other order);
+                    // the union also skips the diagonal tile, whose pairs the
+                    // tile-local union has already joined
+                    const bool have = ti < m.ntiles &&
+                                      !(a.tri && (MODE == SWEEP_UNION ? tile <= rt : (RT > 1 && tile < rt)));
                     const bool diag = a.tri && tile == rt;
                     // f32 accumulator: v0, v1 = columns 0-31, 32-63 of the warp's 64;
                     // f16 accumulator: v0 = all 64 columns, two per register
