@@ -64,6 +64,8 @@ def load():
         lib.dbscan_fit_culled.restype = ctypes.c_int
         lib.dbscan_fit_host.argtypes = [P, i32, i64, i32, f32, i32, P, P, P]
         lib.dbscan_fit_host.restype = ctypes.c_int
+        lib.dbscan_compact_labels.argtypes = [P, i64, P, P, P]
+        lib.dbscan_compact_labels.restype = ctypes.c_int
         lib.dbscan_neighbor_counts.argtypes = [P, i32, i64, i32, f32, P, P, sz, P]
         lib.dbscan_neighbor_counts.restype = ctypes.c_int
         lib.dbscan_workspace_size.argtypes = [i64, i32, i32]
@@ -197,6 +199,20 @@ def dbscan_fit_host(points, eps: float, min_pts: int, *, labels=None, is_core=No
                                   labels.data_ptr(), is_core.data_ptr(),
                                   _stream_handle(stream)), "dbscan_fit_host")
     return labels, is_core
+
+
+def dbscan_compact_labels(labels: torch.Tensor, *, out=None, stream=None):
+    """Labels renumbered 0..k-1 (noise -1) and k; ``out`` may be ``labels``."""
+    if not (labels.is_cuda and labels.dtype == torch.int32 and labels.dim() == 1
+            and labels.is_contiguous()):
+        raise ValueError("labels must be a contiguous 1-D int32 CUDA tensor")
+    if out is None:
+        out = torch.empty_like(labels)
+    k = ctypes.c_int32(0)
+    _check(load().dbscan_compact_labels(labels.data_ptr(), labels.numel(), out.data_ptr(),
+                                        ctypes.byref(k), _stream_handle(stream)),
+           "dbscan_compact_labels")
+    return out, int(k.value)
 
 
 def dbscan_workspace_status(workspace: torch.Tensor, stream=None) -> int:

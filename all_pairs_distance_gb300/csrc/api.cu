@@ -464,6 +464,41 @@ int dbscan_workspace_status(const void *workspace, void *stream) {
     return read_status(workspace, static_cast<cudaStream_t>(stream));
 }
 
+int dbscan_compact_labels(const int32_t *labels, int64_t n, int32_t *labels_out, int32_t *n_clusters,
+                          void *stream) {
+    if (n < 0 || !n_clusters) return DBSCAN_ERR_INVALID_ARG;
+    if (n > (int64_t)INT32_MAX) return DBSCAN_ERR_UNSUPPORTED;
+    if (n == 0) {
+        *n_clusters = 0;
+        return DBSCAN_OK;
+    }
+    if (!labels || !labels_out) return DBSCAN_ERR_INVALID_ARG;
+    if (check_device_ptr(labels) != DBSCAN_OK || check_device_ptr(labels_out) != DBSCAN_OK)
+        return DBSCAN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    keep_pool();
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, compact_labels_scratch(n), s) != cudaSuccess) {
+        cudaGetLastError();
+        return DBSCAN_ERR_ALLOC;
+    }
+    int st = DBSCAN_OK;
+    int *k_err = nullptr;
+    int host[2] = {0, 0};
+    if (launch_compact_labels_rank(labels, n, scratch, &k_err, s) != cudaSuccess ||
+        cudaMemcpyAsync(host, k_err, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        st = DBSCAN_ERR_CUDA;
+    else if (host[1])
+        st = DBSCAN_ERR_INVALID_ARG;   // not labels of dbscan_fit*: nothing is written
+    else if (launch_compact_labels_map(labels, n, scratch, labels_out, s) != cudaSuccess)
+        st = DBSCAN_ERR_CUDA;
+    cudaFreeAsync(scratch, s);
+    if (cudaStreamSynchronize(s) != cudaSuccess && st == DBSCAN_OK) st = DBSCAN_ERR_CUDA;
+    if (st == DBSCAN_OK) *n_clusters = host[0];
+    return st;
+}
+
 int dbscan_fit_host(const void *points_host, int32_t dtype, int64_t n, int32_t d, float eps,
                     int32_t min_pts, int32_t *labels_host, uint8_t *is_core_host, void *stream) {
     int st = check_shape(n, d, dtype);

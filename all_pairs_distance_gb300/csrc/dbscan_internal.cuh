@@ -117,7 +117,11 @@ enum SweepMode { SWEEP_COUNT = 0, SWEEP_UNION = 1, SWEEP_BORDER = 2 };
 enum TcKind { TC_NONE = 0, TC_TF32 = 1, TC_BF16 = 2, TC_F16 = 3 };
 // Allowed-path mask passed from the host (all by default).
 enum { TC_ALLOW_TF32 = 1, TC_ALLOW_BF16 = 2, TC_ALLOW_F16 = 4 };
-constexpr int TC_MAX_KBYTES = 256;   // largest operand row the tensor-core sweep stages
+// Largest operand row the tensor-core sweep stages: two row tiles and two
+// stages of two column tiles (plus their aux ints) must fit 224 KB of shared
+// memory, 768 x kbytes + 2 KB; 288 bytes is 144 bf16 (d <= 137) or 72 tf32
+// (d <= 67) elements.
+constexpr int TC_MAX_KBYTES = 288;
 constexpr int TC_F16_KBYTES = 32;    // the one K = 16 MMA of the F16 path
 
 __host__ __device__ inline int tc_norm_digits(int kind) { return kind == TC_BF16 ? 3 : 2; }
@@ -179,6 +183,15 @@ cudaError_t launch_union_tc_band(const Work &w, const Layout &L, int band, int b
 cudaError_t launch_border_tc(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
 
 int persistent_ctas(const void *kernel, int threads, size_t smem);
+
+// Label compaction (labels.cu): scratch bytes for n labels; the ranking passes
+// (*k_err points at the cluster count and the error flag in the scratch); the
+// mapping pass.
+size_t compact_labels_scratch(int64_t n);
+cudaError_t launch_compact_labels_rank(const int32_t *labels, int64_t n, void *scratch, int **k_err,
+                                       cudaStream_t s);
+cudaError_t launch_compact_labels_map(const int32_t *labels, int64_t n, const void *scratch,
+                                      int32_t *out, cudaStream_t s);
 
 // ---- device helpers --------------------------------------------------------
 __device__ __forceinline__ void set_error(Ctrl *c, int code) {

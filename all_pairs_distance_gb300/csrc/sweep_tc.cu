@@ -854,7 +854,10 @@ cudaError_t run_tc(TcArgs a, const Layout &L, cudaStream_t s) {
     const int tile = 128 * kb;
     const int aux = MODE != SWEEP_COUNT ? BT * 4 : 0;
     const size_t budget = 224 * 1024;
-    const int rows = tc_rows(MODE, a.cull);
+    int rows = tc_rows(MODE, a.cull);
+    // two row blocks need room for four row tiles next to two stages of two
+    // column tiles; wide operand rows keep one
+    if (rows == 2 && 4 * (size_t)tile + 4 * (size_t)(tile + aux) > budget) rows = 1;
     auto kernel = rows == 2 ? k_sweep_tc<MODE, KIND, 2> : k_sweep_tc<MODE, KIND, 1>;
     const size_t abufs = 2 * (size_t)rows * tile;   // two buffers of a unit's row tiles
     // Few, large stages: every stage costs a round of barrier handshakes

@@ -116,7 +116,7 @@ int dbscan_fit_ex(const void *points, int32_t dtype, int64_t n, int32_t d,
  * neighbour, so for integer data within the exactness bound the result is
  * identical to dbscan_fit_ex.  This is not an all-pairs evaluation (pairs in
  * skipped tiles are never evaluated), which is why it is a separate entry
- * point.  Culling applies on the tensor-core paths for d <= 16 and exact data;
+ * point.  Culling applies on the tensor-core paths for d <= 64 and exact data;
  * otherwise the call runs exactly as dbscan_fit_ex.  (dbscan_fit_ex itself
  * applies the same exact test in its union and border passes, which act only
  * on neighbour pairs; its count pass evaluates every pair.)  The pages evaluate all
@@ -141,6 +141,25 @@ int dbscan_fit_host(const void *points_host, int32_t dtype, int64_t n,
                     int32_t d, float eps, int32_t min_pts,
                     int32_t *labels_host, uint8_t *is_core_host,
                     void *stream);
+
+/*
+ * Cluster labels renumbered 0..k-1 in increasing order of label (the order of
+ * each cluster's smallest core index); noise stays -1.  An optional output:
+ * the pages name clusters by the columns of their cluster matrix
+ * ("Design and optimization of DBSCAN Algorithm based on CUDA", §IV-B) and
+ * fix no numbering.
+ *   labels           [n] int32, device: labels as dbscan_fit* writes them --
+ *                    -1, or the index of a point whose own label is that index
+ *   labels_out       [n] int32, device; may equal labels (in place)
+ *   n_clusters       host int32: k, written on success
+ * Synchronises `stream`; scratch memory is allocated stream-ordered for the
+ * call.  Labels that dbscan_fit* cannot have produced (a label that is not -1
+ * and not the index of a point labelled with itself) give
+ * DBSCAN_ERR_INVALID_ARG, and labels_out is then left untouched.  n = 0 sets
+ * k = 0; n > 2^31 - 1 gives DBSCAN_ERR_UNSUPPORTED.
+ */
+int dbscan_compact_labels(const int32_t *labels, int64_t n, int32_t *labels_out,
+                          int32_t *n_clusters, void *stream);
 
 /*
  * Neighbour counts only (the fused distance + count step, §IV-B1/§IV-B2):

@@ -112,3 +112,19 @@ def row_neighbours(points, eps: float, i: int) -> np.ndarray:
         if c <= cap:
             return out[:c]
         cap = int(c)
+
+
+def compact_labels(labels):
+    """Cluster labels renumbered 0..k-1 (noise stays -1) and k.
+
+    The optional compacted output named among the scope's next steps: the
+    distinct non-negative labels, taken in increasing order, become 0, 1, ...
+    (DBSCAN labels are smallest core indices, so clusters keep the order of
+    their first core point).  A plain definition: no page fixes it.
+    """
+    lab = np.asarray(labels, dtype=np.int64)
+    keys = np.unique(lab[lab >= 0])
+    out = np.full(lab.shape, -1, dtype=np.int32)
+    pos = lab >= 0
+    out[pos] = np.searchsorted(keys, lab[pos]).astype(np.int32)
+    return out, int(keys.size)

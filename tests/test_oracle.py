@@ -285,3 +285,29 @@ def test_planted_mistake_is_caught(mutant):
                 caught = True
                 break
         assert caught, f"no golden fixture detects mutant {mutant}"
+
+
+def test_compact_labels_worked_examples():
+    # hand-worked: distinct labels in increasing order become 0, 1, ...
+    out, k = oracle.compact_labels([5, -1, 5, 2, 2, -1, 9])
+    assert k == 3
+    assert out.tolist() == [1, -1, 1, 0, 0, -1, 2]
+    out, k = oracle.compact_labels([-1, -1])
+    assert k == 0 and out.tolist() == [-1, -1]
+    out, k = oracle.compact_labels([])
+    assert k == 0 and out.size == 0
+    out, k = oracle.compact_labels([0, 1, 2, 3])
+    assert k == 4 and out.tolist() == [0, 1, 2, 3]
+
+
+def test_compact_labels_of_a_clustering_keeps_the_partition():
+    # on a real clustering: same partition, noise kept, ids contiguous and in
+    # the order of each cluster's smallest core index (its first point)
+    P = np.array([[0.0], [1.0], [2.0], [10.0], [11.0], [12.0], [30.0], [20.0], [21.0], [22.0]])
+    cnt, core, lab = oracle.dbscan(P, 1.0, 2)
+    out, k = oracle.compact_labels(lab)
+    assert k == 3
+    assert out.tolist() == [0, 0, 0, 1, 1, 1, -1, 2, 2, 2]
+    for i in range(len(lab)):
+        for j in range(len(lab)):
+            assert (lab[i] == lab[j]) == (out[i] == out[j])

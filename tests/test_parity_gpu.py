@@ -169,6 +169,21 @@ def test_extremes_bf16_d64():
             assert_same(g, e, f"eps={eps} {w}")
 
 
+def test_extremes_bf16_d128():
+    # all-0 and all-255 rows at d = 128: the widest operand rows the bf16 path
+    # stages (144 elements); the corner distance is 255 * sqrt(128) = 2884.9
+    rng = np.random.default_rng(4)
+    P = (rng.integers(0, 2, size=(400, 128)) * 255).astype(np.float32)
+    P[:100] = rng.integers(250, 256, size=(100, 128))
+    for eps in (100.0, 2884.0, 2885.0):
+        ref = oracle.dbscan(P, eps, 4)
+        info = {}
+        got = gpu_run(P, eps, 4, torch.bfloat16, info=info)
+        assert info["path"] == "bf16", info
+        for g, e, w in zip(got, ref, ("cnt", "core", "label")):
+            assert_same(g, e, f"eps={eps} {w}")
+
+
 def test_dyadic_fractional_coordinates():
     # quarter-integer coordinates are exact in float32 as well; the
     # non-integer branch of the threshold must still give "<= eps^2"
@@ -236,7 +251,7 @@ PATH_CASES = {
     "c3_like_3k_d16": (lambda: synth.scaled("blobs_200k_d16", 3_001, seed=33), 120.0, 20,
                        torch.float32, {"tf32"}),
     "c5_like_3k_d64": (lambda: synth.scaled("blobs_500k_d64", 2_999, seed=34), 100.0, 16,
-                       torch.bfloat16, {"bf16"}),
+                       torch.bfloat16, {"bf16", "tf32"}),
     "small_box_d3": (lambda: synth.uniform_ints(4_000, 3, 200, 35), 9.0, 6, torch.float32,
                      {"tf32", "bf16", "f16"}),
     "corners_d3": (lambda: (np.random.default_rng(36).integers(0, 2, size=(700, 3)) * 2047)
@@ -247,6 +262,12 @@ PATH_CASES = {
     # d = 11 no longer fits one K = 16 MMA: f16 is not eligible
     "d11_blobs": (lambda: synth.blob_set(2_500, 11, 511, 10, 20.0, 250, 38), 60.0, 5,
                   torch.float32, {"tf32"}),
+    # the widest rows: 144 bf16 elements at d = 128, 72 tf32 elements at d = 64
+    # (a range of 400 is too wide for bf16 and narrow enough for exact tf32)
+    "d128_bf16": (lambda: synth.blob_set(2_500, 128, 255, 8, 6.0, 250, 39), 110.0, 5,
+                  torch.bfloat16, {"bf16"}),
+    "d64_tf32_wide": (lambda: synth.blob_set(2_000, 64, 400, 8, 12.0, 200, 40), 150.0, 5,
+                      torch.float32, {"tf32"}),
 }
 
 
@@ -276,6 +297,8 @@ def test_default_path_choice():
                       (synth.uniform_ints(3000, 3, 255, 2), "f16"),
                       (synth.uniform_ints(3000, 16, 255, 5), "bf16"),
                       (synth.uniform_ints(3000, 12, 511, 6), "tf32"),
+                      (synth.uniform_ints(3000, 128, 255, 7), "bf16"),
+                      (synth.uniform_ints(3000, 64, 400, 8), "tf32"),
                       (synth.uniform_ints(3000, 2, 3000, 3), "fp32"),
                       (synth.uniform_ints(3000, 2, 100, 4) + np.float32(0.5), "fp32")):
         info = {}
