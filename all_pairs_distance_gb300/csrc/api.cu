@@ -79,7 +79,7 @@ Layout make_layout(int64_t n, int32_t d) {
     L.off_rootmin = off;     off += align256(per_pt);
     // tile bounding boxes for culling (three arrays: all, core, candidates)
     L.box_floats = d <= CULL_MAX_D ? (size_t)L.ntiles * 2 * d : 0;
-    L.gbox_floats = d <= CULL_MAX_D ? (size_t)((L.ntiles + 31) / 32) * 2 * d : 0;
+    L.gbox_floats = d <= CULL_MAX_D ? (size_t)((L.ntiles + CULL_GROUP - 1) / CULL_GROUP) * 2 * d : 0;
     L.off_box_all = off;     off += align256(L.box_floats * sizeof(float));
     L.off_box_core = off;    off += align256(L.box_floats * sizeof(float));
     L.off_box_cand = off;    off += align256(L.box_floats * sizeof(float));

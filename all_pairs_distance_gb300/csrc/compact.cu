@@ -193,7 +193,7 @@ __global__ void k_group_boxes(const float *box, const int *count, int d, int64_t
     const int k = (int)(e % d);
     const int64_t ntv = ((int64_t)*count + BT - 1) / BT;   // valid tiles
     float lo = INFINITY, hi = -INFINITY;
-    for (int64_t t = g * 32; t < g * 32 + 32 && t < ntv; ++t) {
+    for (int64_t t = g * CULL_GROUP; t < (g + 1) * CULL_GROUP && t < ntv; ++t) {
         lo = fminf(lo, box[(t * d + k) * 2]);
         hi = fmaxf(hi, box[(t * d + k) * 2 + 1]);
     }
@@ -208,7 +208,7 @@ cudaError_t launch_tile_boxes(const Work &w, const Layout &L, int which, cudaStr
     float *box = which == 0 ? w.box_all : (which == 1 ? w.box_core : w.box_cand);
     k_tile_boxes<<<(unsigned)L.ntiles, BT, 0, s>>>(st, cnt, L.d, box);
     if (which != 2) {   // column arrays (all points, core points) also get group boxes
-        const int64_t ngroups = (L.ntiles + 31) / 32;
+        const int64_t ngroups = (L.ntiles + CULL_GROUP - 1) / CULL_GROUP;
         k_group_boxes<<<(unsigned)((ngroups * L.d + 255) / 256), 256, 0, s>>>(
             box, cnt, L.d, ngroups, which == 0 ? w.gbox_all : w.gbox_core);
     }

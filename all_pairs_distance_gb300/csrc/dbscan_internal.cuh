@@ -20,6 +20,8 @@ constexpr int SCAN_BLOCK = 1024;   // elements per block of the compaction scan
 // Tile culling keeps per-tile bounding boxes for d up to this dimension (the
 // locality order's nearest-pivot key covers 3 < d <= 64 and keeps tiles tight).
 constexpr int CULL_MAX_D = 64;
+// Tiles per group of the group boxes (the coarse level of the test).
+constexpr int CULL_GROUP = 8;
 
 // Sentinels for the padding slots of the last tile: a padding column has a
 // huge norm and never tests as a neighbour; a padding row has a hugely
@@ -67,7 +69,7 @@ struct Layout {
     int cull;             // 1: the count sweep also skips tile pairs whose boxes are eps apart
     int cull_nbr;         // 1: union and border skip tile pairs whose boxes are eps apart
     size_t box_floats;    // floats of one box array (ntiles x 2d), 0 when d > CULL_MAX_D
-    size_t gbox_floats;   // floats of one group-box array (ceil(ntiles / 32) x 2d)
+    size_t gbox_floats;   // floats of one group-box array (ceil(ntiles / CULL_GROUP) x 2d)
     size_t off_box_all, off_box_core, off_box_cand;
     size_t off_gbox_all, off_gbox_core;
     int64_t nscan_blocks;
@@ -97,7 +99,7 @@ struct Work {
     int *btot;            // [2^order_bits / 1024] bin-block offsets
     int *rootmin;         // [n] smallest input index of each union-find root's component
     float *box_all, *box_core, *box_cand;   // [ntiles][d][min, max] tile bounding boxes
-    float *gbox_all, *gbox_core;            // [ntiles / 32][d][min, max] boxes of 32-tile groups
+    float *gbox_all, *gbox_core;            // [ntiles / CULL_GROUP][d][min, max] group boxes
 };
 
 Work carve(void *base, const Layout &L);

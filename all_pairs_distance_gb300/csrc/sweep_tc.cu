@@ -76,7 +76,7 @@ struct TcArgs {
     int tri;
     int band, blo, bhi;       // band != 0: one unit per row block, tiles rb+blo .. rb+bhi-1
     const float *rbox, *cbox; // per-tile bounding boxes of rows / columns (d x (min, max))
-    const float *cgbox;       // boxes of groups of 32 column tiles
+    const float *cgbox;       // boxes of groups of CULL_GROUP column tiles
     int cull, d;              // cull != 0: skip column tiles whose box is eps or more away
     unsigned *ctr;
     Ctrl *ctrl;
@@ -459,23 +459,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             if (!cull) {
                 ok = emit(t0, t1);
             } else {
-                // Column tiles go by groups of 32: a group whose box is eps or
-                // more from the row tiles' box is skipped with one test;
-                // otherwise every tile of the group is tested, and runs of kept
-                // tiles become stages.  Gaps are integers, so every sum below is
-                // exact in any order.
+                // Column tiles go by groups of CULL_GROUP (8) tiles: the boxes of
+                // 32 groups are tested at once, and only the tiles of the kept
+                // groups are tested, 32 at a time (four groups); runs of kept
+                // tiles become stages.  Gaps are integers, so every sum below
+                // is exact in any order.
+                static_assert(CULL_GROUP == 8, "32 tile slots hold four groups");
                 // The unit's box is the union of its row tiles' boxes.
                 const float *rbx0 = a.rbox + (size_t)rb * 2 * a.d;
                 const float *rbx1 = a.rbox + (size_t)(rb + nrow - 1) * 2 * a.d;
                 auto rlo = [&](int kk) { return fminf(rbx0[2 * kk], rbx1[2 * kk]); };
                 auto rhi = [&](int kk) { return fmaxf(rbx0[2 * kk + 1], rbx1[2 * kk + 1]); };
                 // d > 4: the lanes split the dimensions (lane and lane + 32), each
-                // keeping its share of the unit's box in registers
+                // keeping its share of the unit's box in registers; d <= 4: every
+                // lane keeps the whole box and tests a box of its own
                 const bool split = a.d > 4;
                 float rl0 = 0.f, rh0 = 0.f, rl1 = 0.f, rh1 = 0.f;
+                float rl[4] = {0.f, 0.f, 0.f, 0.f}, rh[4] = {0.f, 0.f, 0.f, 0.f};
                 if (split) {
                     if (lane < a.d) { rl0 = rlo(lane); rh0 = rhi(lane); }
                     if (lane + 32 < a.d) { rl1 = rlo(lane + 32); rh1 = rhi(lane + 32); }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        if (kk < a.d) { rl[kk] = rlo(kk); rh[kk] = rhi(kk); }
                 }
                 // this lane's part of the squared gap between the unit's box and box bx
                 auto part = [&](const float *bx) -> float {
@@ -492,39 +499,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                     }
                     return g2;
                 };
-                for (int g = t0 / 32; g * 32 < t1 && ok; ++g) {
-                    {
-                        // every lane gets the same sum
-                        const float *gbx = a.cgbox + (size_t)g * 2 * a.d;
-                        float g2 = 0.f;
-                        if (split) {
-                            g2 = part(gbx);
-#pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) g2 += __shfl_xor_sync(FULL, g2, o);
-                        } else {
-                            for (int kk = 0; kk < a.d; ++kk) {
-                                const float gap = fmaxf(0.f, fmaxf(gbx[2 * kk] - rhi(kk), rlo(kk) - gbx[2 * kk + 1]));
-                                g2 = fmaf(gap, gap, g2);
-                            }
-                        }
-                        if (!(g2 < cthr)) continue;
-                    }
-                    const int w0 = g * 32;
-                    const int tt = w0 + lane;
-                    bool keep = false;
+                // Bit j: the box at bx0 + ix(j) (every ix(j) in range) is closer
+                // than eps to the unit's box.  Split: every lane's parts for all
+                // 32 boxes, then a butterfly reduce-scatter -- after the round of
+                // offset o a lane keeps the half of the boxes whose index bit o
+                // matches its own, so lane j ends with box j's sum.
+                auto test32 = [&](const float *bx0, auto ix) -> unsigned {
+                    float g2 = 0.f;
                     if (split) {
-                        // every lane's parts for all 32 tiles (tiles outside
-                        // [t0, t1) read an in-range box and are dropped below),
-                        // then a butterfly reduce-scatter: after the round of
-                        // offset o a lane keeps the half of its tiles whose
-                        // index bit o matches its own, so lane t ends with the
-                        // sum for tile t
                         float pv[32];
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) {
-                            const int tc = min(max(w0 + t, t0), t1 - 1);
-                            pv[t] = part(a.cbox + (size_t)tc * 2 * a.d);
-                        }
+                        for (int jj = 0; jj < 32; ++jj) pv[jj] = part(bx0 + (size_t)ix(jj) * 2 * a.d);
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1) {
                             const bool up = (lane & o) != 0;
@@ -535,23 +520,52 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                                 pv[jj] = mine + __shfl_xor_sync(FULL, send, o);
                             }
                         }
-                        keep = tt >= t0 && tt < t1 && pv[0] < cthr;
-                    } else if (tt >= t0 && tt < t1) {
-                        const float *cbx = a.cbox + (size_t)tt * 2 * a.d;
-                        float g2 = 0.f;
-                        for (int kk = 0; kk < a.d; ++kk) {
-                            const float g = fmaxf(0.f, fmaxf(cbx[2 * kk] - rhi(kk), rlo(kk) - cbx[2 * kk + 1]));
-                            g2 = fmaf(g, g, g2);
-                        }
-                        keep = g2 < cthr;   // some pair could be a neighbour
+                        g2 = pv[0];
+                    } else {
+                        const float *bx = bx0 + (size_t)ix(lane) * 2 * a.d;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            if (kk < a.d) {
+                                const float gp = fmaxf(0.f, fmaxf(bx[2 * kk] - rh[kk], rl[kk] - bx[2 * kk + 1]));
+                                g2 = fmaf(gp, gp, g2);
+                            }
                     }
-                    unsigned km = __ballot_sync(FULL, keep);
-                    while (km && ok) {
-                        const int s0 = __ffs(km) - 1;
-                        const unsigned gaps = ~(km >> s0);
-                        const int len = gaps ? __ffs(gaps) - 1 : 32 - s0;
-                        km = (s0 + len >= 32) ? 0u : (km & (0xffffffffu << (s0 + len)));
-                        ok = emit(w0 + s0, w0 + s0 + len);
+                    return __ballot_sync(FULL, g2 < cthr);
+                };
+                const int gend = (t1 + CULL_GROUP - 1) / CULL_GROUP;
+                for (int gb = t0 / CULL_GROUP; gb < gend && ok; gb += 32) {
+                    unsigned gk = test32(a.cgbox, [&](int jj) { return min(gb + jj, gend - 1); });
+                    if (gend - gb < 32) gk &= (1u << (gend - gb)) - 1u;
+                    while (gk && ok) {
+                        // up to four kept groups (5-bit offsets from gb in sel); slot
+                        // s holds tile s & 7 of the (s >> 3)-th of them
+                        uint32_t sel = 0;
+                        int ns = 0;
+                        while (gk && ns < 4) {
+                            sel |= (uint32_t)(__ffs(gk) - 1) << (5 * ns);
+                            gk &= gk - 1;
+                            ++ns;
+                        }
+                        auto slot_tile = [&](int sl) {
+                            return (gb + (int)((sel >> (5 * (sl >> 3))) & 31u)) * CULL_GROUP + (sl & 7);
+                        };
+                        const int my = slot_tile(lane);
+                        const unsigned valid = __ballot_sync(FULL, (lane >> 3) < ns && my >= t0 && my < t1);
+                        unsigned km = valid & test32(a.cbox, [&](int sl) {
+                                          return min(max(slot_tile(sl), t0), t1 - 1);
+                                      });
+                        // a run breaks where the next group does not follow on
+                        unsigned brk = 0;
+                        for (int q = 1; q < ns; ++q)
+                            if (((sel >> (5 * q)) & 31u) != ((sel >> (5 * (q - 1))) & 31u) + 1u) brk |= 1u << (8 * q);
+                        while (km && ok) {
+                            const int s0 = __ffs(km) - 1;
+                            int e = s0 + 1;
+                            while (e < 32 && ((km >> e) & 1u) && !((brk >> e) & 1u)) ++e;
+                            km = e >= 32 ? 0u : (km & (0xffffffffu << e));
+                            const int ts = slot_tile(s0);
+                            ok = emit(ts, ts + (e - s0));
+                        }
                     }
                 }
             }
