@@ -9,28 +9,30 @@
 // w_ij < 0.  The CUDA cores only read the accumulator and test signs.
 //
 // CTA = 18 warps, one per SM (the CTA owns all 512 TMEM columns):
-//   warp 16     producer: pulls work units (a row block and a run of column
-//               tiles; for the union, one row block per band of tile distances)
-//               and bulk-copies (cp.async.bulk) the unit's row operand tile and
-//               groups of up to 32 consecutive column tiles (plus their aux
-//               ints) into a ring of shared-memory stages; lanes take turns
-//               issuing, since the bulk copies of one thread complete one after
-//               another.  With tile culling it streams only the column tiles
-//               whose bounding boxes are within eps of the row tile's;
+//   warp 16     producer: pulls work units (a row unit of one or two row
+//               blocks and a run of column tiles; for the union, one per band
+//               of tile distances) and bulk-copies (cp.async.bulk) the unit's
+//               row operand tiles and groups of up to 32 consecutive column
+//               tiles (plus their aux ints) into a ring of shared-memory
+//               stages, each stage in parts from rotating lanes, since the bulk
+//               copies of one thread complete one after another.  With tile
+//               culling it streams only the column tiles whose bounding boxes
+//               are within eps of the unit's;
 //   warp 17     MMA: one thread issues a 128 x 256 x K MMA per pair of column
-//               tiles into one of two 256-column TMEM accumulators and commits
-//               completion to mbarriers;
+//               tiles and row block into one of two 256-column TMEM
+//               accumulators and commits completion to mbarriers; its loop
+//               is the critical path of the sweep and keeps everything it
+//               needs in registers;
 //   warps 0-15  epilogue: every warp reads every tile pair, 32 rows x 64
 //               columns (two tcgen05.ld, or one packed load of an f16
-//               accumulator), and frees the accumulator before it
-//               tests anything -- the accumulator round trip is bound by how
-//               fast TMEM is drained, and TMEM read bandwidth grows with the
-//               number of warps loading.  A warp ORs the sign bits of its 64
-//               columns and, only where a 32 x 32 block holds a neighbour,
-//               builds exact per-row bit masks.  Counting credits the row with a popcount
-//               and the columns by atomics (few neighbours) or a warp bit
-//               transpose (many); union and border act on each neighbour pair
-//               as on CUDA cores.
+//               accumulator), and frees the accumulator before it tests
+//               anything -- TMEM read bandwidth grows with the number of warps
+//               loading.  A warp ORs the sign bits of its 64 columns and, only
+//               where a 32 x 32 block holds a neighbour, builds exact per-row
+//               bit masks.  Counting credits the row with a popcount and the
+//               columns by atomics (few neighbours) or a warp bit transpose
+//               (many); union and border act on each neighbour pair as on CUDA
+//               cores.
 // Every role polls its barriers without suspending: each reaction (MMA issue,
 // accumulator drain, stage refill) lies on the critical path of the
 // accumulator round trip, and a suspended thread resumes hundreds of cycles

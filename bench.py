@@ -150,19 +150,37 @@ def count_flops(n: int, d: int) -> float:
     return 2.0 * d * n * (n - 1) / 2.0
 
 
-def recorded_traffic(kernel_src: str, workload: str):
+KERNEL_FILES = ("sweep_tc.cu", "tc_schedule.h", "dbscan_internal.cuh")
+
+
+def kernel_code_hash() -> str:
+    """sha256 of the tensor-core sweep's code: its source and the headers it
+    includes, with comments and blank lines removed (a comment edit does not
+    change the kernel)."""
+    h = hashlib.sha256()
+    for name in KERNEL_FILES:
+        text = open(os.path.join(ROOT, "all_pairs_distance_gb300", "csrc", name)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [ln.strip() for ln in text.splitlines() if ln.strip()]
+        h.update(("\n".join(lines) + "\n").encode())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str, path: str):
     """Per-launch DRAM bytes of the count sweep from the committed ncu summary,
-    or None when the summary is missing or the kernel source changed since."""
-    path = os.path.join(ROOT, "profiles", f"count_sweep_{workload}.md")
-    if not os.path.exists(path):
+    or None when the summary is missing, the kernel's code changed since, or
+    this run took another path."""
+    summary = os.path.join(ROOT, "profiles", f"count_sweep_{workload}.md")
+    if not os.path.exists(summary):
         return None
-    text = open(path).read()
+    text = open(summary).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    h = re.search(r"sweep_source_sha256:\s*([0-9a-f]+)", text)
-    if not m or not h:
+    h = re.search(r"sweep_code_sha256:\s*([0-9a-f]+)", text)
+    k = re.search(r"sweep_path:\s*(\w+)", text)
+    if not m or not h or not k or k.group(1) != path:
         return None
-    cur = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-    return float(m.group(1)) if h.group(1) == cur else None
+    return float(m.group(1)) if h.group(1) == kernel_code_hash() else None
 
 
 def cpu_baseline(P, eps, min_pts, target_s=12.0):
@@ -283,8 +301,7 @@ def run_gb300(args, dist: Dist):
     max_mhz = (peaks or {}).get("sm_max_mhz", SM_MAX_MHZ_FALLBACK)
     fp32_peak = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12
     achieved = count_flops(n, d) / (count_ms * 1e-3) / 1e12
-    src = "sweep_tc.cu" if info["path"] != "fp32" else "sweep.cu"
-    traffic = recorded_traffic(os.path.join(ROOT, "all_pairs_distance_gb300", "csrc", src), w.name)
+    traffic = recorded_traffic(w.name, info["path"])
     # d <= 16: the distance pass is d FMAs per pair, so its roofline is the FP32
     # CUDA-core peak whichever unit evaluates it; d > 16: the bf16 tensor peak.
     tc_peak = None
