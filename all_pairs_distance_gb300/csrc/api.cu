@@ -85,6 +85,7 @@ Layout make_layout(int64_t n, int32_t d) {
     L.off_box_cand = off;    off += align256(L.box_floats * sizeof(float));
     L.off_gbox_all = off;    off += align256(L.gbox_floats * sizeof(float));
     L.off_gbox_core = off;   off += align256(L.gbox_floats * sizeof(float));
+    L.off_troot = off;       off += align256((size_t)L.ntiles * sizeof(int));
     L.total = off;
     return L;
 }
@@ -150,6 +151,7 @@ Work carve(void *base, const Layout &L) {
     w.bstart = reinterpret_cast<int *>(b + L.off_bstart);
     w.btot = reinterpret_cast<int *>(b + L.off_btot);
     w.rootmin = reinterpret_cast<int *>(b + L.off_rootmin);
+    w.troot = reinterpret_cast<int *>(b + L.off_troot);
     w.box_all = reinterpret_cast<float *>(b + L.off_box_all);
     w.box_core = reinterpret_cast<float *>(b + L.off_box_core);
     w.box_cand = reinterpret_cast<float *>(b + L.off_box_cand);

@@ -72,6 +72,7 @@ struct Layout {
     size_t gbox_floats;   // floats of one group-box array (ceil(ntiles / CULL_GROUP) x 2d)
     size_t off_box_all, off_box_core, off_box_cand;
     size_t off_gbox_all, off_gbox_core;
+    size_t off_troot;     // [ntiles] ints: common root of each core tile's points, or -1
     int64_t nscan_blocks;
     size_t total;
 };
@@ -100,6 +101,7 @@ struct Work {
     int *rootmin;         // [n] smallest input index of each union-find root's component
     float *box_all, *box_core, *box_cand;   // [ntiles][d][min, max] tile bounding boxes
     float *gbox_all, *gbox_core;            // [ntiles / CULL_GROUP][d][min, max] group boxes
+    int *troot;           // [ntiles] common root of each core tile's points, or -1 (union)
 };
 
 Work carve(void *base, const Layout &L);

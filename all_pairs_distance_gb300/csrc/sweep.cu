@@ -519,6 +519,36 @@ __global__ void k_compress(Ctrl *ctrl, int *parent, int tc) {
     }
 }
 
+// Common root of each core tile's points, or -1 when they are not all in one
+// set (tensor-core path, after k_compress: every parent is then a root).  A
+// union tile pair whose row and column tiles share one common root holds no
+// pair the union could still join, and the sweep skips it; sets only merge,
+// so a snapshot taken before a band stays safe through it.
+__global__ void k_tile_roots(const Ctrl *ctrl, const int *parent, int *troot) {
+    if (ctrl->tc_kind == TC_NONE) return;
+    const int n_core = ctrl->n_core;
+    const int nt = (n_core + BT - 1) / BT;
+    const int lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < nt; t += gridDim.x * wpb) {
+        int mn = 0x7fffffff, mx = -1;
+        for (int j = lane; j < BT; j += 32) {
+            const int p = t * BT + j;
+            if (p < n_core) {
+                const int r = __ldcg(parent + p);
+                mn = min(mn, r);
+                mx = max(mx, r);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        if (lane == 0) troot[t] = mn == mx ? mn : -1;
+    }
+}
+
 // ===========================================================================
 // host side
 // ===========================================================================
@@ -624,13 +654,20 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
     // first, compressed between bands: in locality order most neighbour pairs
     // lie near the diagonal, so the far bands find merged roots in their
     // staged parent snapshots and skip their pairs without a global access.
+    // Each band also skips the tile pairs whose tiles share one root (a
+    // snapshot per band, k_tile_roots; the tile-local union leaves every
+    // parent a root, so the first snapshot needs no compression).
+    const unsigned rgrid = (unsigned)((L.ntiles + 7) / 8);
     for (int bd = 0; bd < UNION_BANDS; ++bd) {
-        cudaError_t e = launch_union_tc_band(w, L, bd, kUnionBandEdges[bd], kUnionBandEdges[bd + 1], s);
-        if (e != cudaSuccess) return e;
-        if (bd + 1 < UNION_BANDS) {
+        cudaError_t e;
+        if (bd > 0) {
             k_compress<<<grid, 256, 0, s>>>(w.ctrl, w.parent, 1);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
+        k_tile_roots<<<rgrid, 256, 0, s>>>(w.ctrl, w.parent, w.troot);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_union_tc_band(w, L, bd, kUnionBandEdges[bd], kUnionBandEdges[bd + 1], s);
+        if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

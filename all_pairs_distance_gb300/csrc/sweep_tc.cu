@@ -79,6 +79,7 @@ struct TcArgs {
     int band, blo, bhi;       // band != 0: one unit per row block, tiles rb+blo .. rb+bhi-1
     const float *rbox, *cbox; // per-tile bounding boxes of rows / columns (d x (min, max))
     const float *cgbox;       // boxes of groups of CULL_GROUP column tiles
+    const int *troot;         // union: common root of each tile's points, or -1 (else null)
     int cull, d;              // cull != 0: skip column tiles whose box is eps or more away
     unsigned *ctr;
     Ctrl *ctrl;
@@ -534,6 +535,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                     }
                     return __ballot_sync(FULL, g2 < cthr);
                 };
+                // union: the common root of the unit's row tiles, or -1; a column
+                // tile with the same common root holds no pair left to join
+                int uroot = -1;
+                if (MODE == SWEEP_UNION && a.troot) {
+                    uroot = a.troot[rb];
+                    if (nrow > 1 && a.troot[rb + 1] != uroot) uroot = -1;
+                }
                 const int gend = (t1 + CULL_GROUP - 1) / CULL_GROUP;
                 for (int gb = t0 / CULL_GROUP; gb < gend && ok; gb += 32) {
                     unsigned gk = test32(a.cgbox, [&](int jj) { return min(gb + jj, gend - 1); });
@@ -552,7 +560,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                             return (gb + (int)((sel >> (5 * (sl >> 3))) & 31u)) * CULL_GROUP + (sl & 7);
                         };
                         const int my = slot_tile(lane);
-                        const unsigned valid = __ballot_sync(FULL, (lane >> 3) < ns && my >= t0 && my < t1);
+                        const bool inr = (lane >> 3) < ns && my >= t0 && my < t1;
+                        const bool joined = inr && uroot >= 0 && a.troot[my] == uroot;
+                        const unsigned valid = __ballot_sync(FULL, inr && !joined);
                         unsigned km = valid & test32(a.cbox, [&](int sl) {
                                           return min(max(slot_tile(sl), t0), t1 - 1);
                                       });
@@ -931,6 +941,7 @@ cudaError_t launch_union_tc_band(const Work &w, const Layout &L, int band, int b
     a.band = 1; a.blo = blo; a.bhi = bhi;
     a.ctr = &w.ctrl->band_ctr[band]; a.ctrl = w.ctrl; a.parent = w.parent;
     a.rbox = w.box_core; a.cbox = w.box_core; a.cgbox = w.gbox_core; a.cull = L.cull_nbr; a.d = L.d;
+    a.troot = w.troot;
     return run_tc_both<SWEEP_UNION>(a, L, s);
 }
 
