@@ -152,7 +152,7 @@ def dbscan_fit_ex(points: torch.Tensor, eps: float, min_pts: int, *, labels=None
 def dbscan_fit_culled(points: torch.Tensor, eps: float, min_pts: int, *, labels=None,
                   is_core=None, workspace=None, stream=None):
     """dbscan_fit_ex with tile culling (tile pairs whose bounding boxes are eps
-    or more apart are skipped; identical results for exact data, d <= 8)."""
+    or more apart are skipped; identical results for exact data, d <= 64)."""
     p = _points(points)
     n, d = p.shape
     if labels is None:

@@ -18,8 +18,11 @@
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+#include <map>
 #include <mutex>
 #include <set>
+#include <string>
+#include <tuple>
 #include <vector>
 
 namespace dbscan {
@@ -321,6 +324,74 @@ static int read_status(const void *ws, cudaStream_t s) {
     return err;
 }
 
+// ---- graph replay ----------------------------------------------------------
+// A call is some sixty launches whose every decision is taken on the device,
+// so a call on a caller's stream and workspace is captured once into a CUDA
+// graph and replayed while its arguments repeat (the graph reads whatever the
+// buffers hold at replay).  Keys: every argument, the device, and the two
+// environment switches the host consults.  Not on the legacy default stream
+// (it cannot be captured), not while the stream is already capturing (the
+// caller's own capture then takes the launches), not while stage profiling
+// records events; DBSCAN_GRAPHS=0 turns it off.  At most kGraphCap graphs
+// are kept; further keys launch directly.
+using GraphKey = std::tuple<int, const void *, int, int64_t, int, uint32_t, int, void *, void *, void *,
+                            void *, int, std::string>;
+static std::mutex g_graph_mu;
+static std::map<GraphKey, cudaGraphExec_t> g_graphs;
+constexpr size_t kGraphCap = 16;
+
+static bool graphs_enabled(cudaStream_t s) {
+    const char *e = getenv("DBSCAN_GRAPHS");
+    if (e && e[0] == '0') return false;
+    if (s == nullptr || s == cudaStreamLegacy || g_prof.on) return false;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return cs == cudaStreamCaptureStatusNone;
+}
+
+static std::string env_switches() {
+    const char *f = getenv("DBSCAN_FORCE_PATH"), *r = getenv("DBSCAN_TC_ROWS");
+    return std::string(f ? f : "") + "|" + (r ? r : "");
+}
+
+// run() through a cached graph; -1 when the graph path does not apply.
+static int run_graph(const void *points, int dtype, int64_t n, int d, float eps, int min_pts,
+                     int32_t *labels, uint8_t *is_core, int32_t *cnt_out, void *ws, const Layout &L,
+                     cudaStream_t s) {
+    if (!graphs_enabled(s)) return -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    uint32_t eb;
+    memcpy(&eb, &eps, sizeof(eb));
+    const GraphKey key(dev, points, dtype, n, d, eb, min_pts, labels, is_core, cnt_out, ws, L.cull,
+                       env_switches());
+    std::lock_guard<std::mutex> lock(g_graph_mu);
+    auto it = g_graphs.find(key);
+    if (it == g_graphs.end()) {
+        if (g_graphs.size() >= kGraphCap) return -1;
+        if (cudaStreamBeginCapture(s, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+            cudaGetLastError();
+            return -1;
+        }
+        const int st = run(points, dtype, n, d, eps, min_pts, labels, is_core, cnt_out, ws, L, s);
+        cudaGraph_t g = nullptr;
+        const cudaError_t ec = cudaStreamEndCapture(s, &g);
+        cudaGraphExec_t ex = nullptr;
+        const bool ok = st == DBSCAN_OK && ec == cudaSuccess && g != nullptr &&
+                        cudaGraphInstantiate(&ex, g, 0) == cudaSuccess;
+        if (g) cudaGraphDestroy(g);
+        if (!ok) {
+            cudaGetLastError();
+            return -1;   // launched directly instead
+        }
+        it = g_graphs.emplace(key, ex).first;
+    }
+    return cudaGraphLaunch(it->second, s) == cudaSuccess ? DBSCAN_OK : DBSCAN_ERR_CUDA;
+}
+
 // Shared body of dbscan_fit_ex and dbscan_neighbor_counts.
 static int fit_common(const void *points, int32_t dtype, int64_t n, int32_t d, float eps,
                       int32_t min_pts, int32_t *labels, uint8_t *is_core, int32_t *cnt_out,
@@ -346,8 +417,12 @@ static int fit_common(const void *points, int32_t dtype, int64_t n, int32_t d, f
     if (workspace && check_device_ptr(workspace) != DBSCAN_OK) return DBSCAN_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    if (workspace)
+    if (workspace) {
+        const int gst = run_graph(points, dtype, n, d, eps, min_pts, labels, is_core, cnt_out,
+                                  workspace, L, s);
+        if (gst >= 0) return gst;
         return run(points, dtype, n, d, eps, min_pts, labels, is_core, cnt_out, workspace, L, s);
+    }
 
     keep_pool();
     void *ws = nullptr;
