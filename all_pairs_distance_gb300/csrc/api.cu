@@ -338,6 +338,7 @@ using GraphKey = std::tuple<int, const void *, int, int64_t, int, uint32_t, int,
                             void *, int, std::string>;
 static std::mutex g_graph_mu;
 static std::map<GraphKey, cudaGraphExec_t> g_graphs;
+static std::set<GraphKey> g_graph_failed;   // keys whose capture failed: launched directly
 constexpr size_t kGraphCap = 16;
 
 static bool graphs_enabled(cudaStream_t s) {
@@ -371,9 +372,10 @@ static int run_graph(const void *points, int dtype, int64_t n, int d, float eps,
     std::lock_guard<std::mutex> lock(g_graph_mu);
     auto it = g_graphs.find(key);
     if (it == g_graphs.end()) {
-        if (g_graphs.size() >= kGraphCap) return -1;
+        if (g_graphs.size() >= kGraphCap || g_graph_failed.count(key)) return -1;
         if (cudaStreamBeginCapture(s, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
             cudaGetLastError();
+            if (g_graph_failed.size() < 64) g_graph_failed.insert(key);
             return -1;
         }
         const int st = run(points, dtype, n, d, eps, min_pts, labels, is_core, cnt_out, ws, L, s);
@@ -385,6 +387,7 @@ static int run_graph(const void *points, int dtype, int64_t n, int d, float eps,
         if (g) cudaGraphDestroy(g);
         if (!ok) {
             cudaGetLastError();
+            if (g_graph_failed.size() < 64) g_graph_failed.insert(key);
             return -1;   // launched directly instead
         }
         it = g_graphs.emplace(key, ex).first;
