@@ -201,6 +201,24 @@ def cpu_baseline(P, eps, min_pts, target_s=12.0):
                       f"(count + BFS), single-threaded, {dt:.1f} s"}
 
 
+def cpu_baseline_parallel(P, eps, min_pts, m=40000):
+    """The same oracle source built with OpenMP (its count loop on all host
+    cores; the cluster expansion stays serial, and dominates) on the first m
+    points.  -> dict, or None without an OpenMP compiler."""
+    import oracle
+    threads = oracle.parallel_threads()
+    if threads == 0:
+        return None
+    m = min(len(P), m)
+    t = time.perf_counter()
+    oracle.dbscan_parallel(P[:m], eps, min_pts)
+    dt = time.perf_counter() - t
+    return {"value": m * m / dt, "unit": UNIT, "cores": threads,
+            "kind": "oracle, OpenMP build of the same source",
+            "sample": f"first {m} of {len(P)} points of the workload, full oracle DBSCAN "
+                      f"(count on {threads} threads, cluster expansion serial), {dt:.1f} s"}
+
+
 # ---------------------------------------------------------------------------
 def run_reference(args, dist: Dist):
     if dist.rank != 0:
@@ -430,6 +448,7 @@ def run_gb300(args, dist: Dist):
                        "api": "dbscan_fit_host (pinned host buffers, copies inside the timed call)"}
     if dist.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(P, w.eps, w.min_pts)
+        line["cpu_baseline_parallel"] = cpu_baseline_parallel(P, w.eps, w.min_pts)
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     return 0

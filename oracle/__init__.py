@@ -23,8 +23,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "dbscan_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD, "liboracle.so")
+_LIB_OMP = os.path.join(_BUILD, "liboracle_omp.so")
 _lock = threading.Lock()
 _lib = None
+_lib_omp = None
 
 
 def build(force: bool = False) -> str:
@@ -38,22 +40,77 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def build_parallel(force: bool = False):
+    """The same source built with OpenMP (its count loop on all host cores),
+    or None when the compiler cannot build it.  A separately timed baseline
+    only: the tests and the single-threaded baseline use ``build()``."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_OMP) or os.path.getmtime(_LIB_OMP) < os.path.getmtime(_SRC):
+        tmp = _LIB_OMP + f".tmp{os.getpid()}"
+        try:
+            subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp",
+                                   "-o", tmp, _SRC], stderr=subprocess.DEVNULL)
+        except (subprocess.CalledProcessError, OSError):
+            return None
+        os.replace(tmp, _LIB_OMP)
+    return _LIB_OMP
+
+
+def _declare(lib):
+    P = ctypes.c_void_p
+    i64, i32, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    lib.oracle_counts.argtypes = [P, i64, i32, f32, P]
+    lib.oracle_counts.restype = None
+    lib.oracle_row_counts.argtypes = [P, i64, i32, f32, P, i64, P]
+    lib.oracle_row_counts.restype = None
+    lib.oracle_row_neighbours.argtypes = [P, i64, i32, f32, i64, P, i64]
+    lib.oracle_row_neighbours.restype = i64
+    lib.oracle_dbscan.argtypes = [P, i64, i32, f32, i32, P, P, P]
+    lib.oracle_dbscan.restype = ctypes.c_int
+    lib.oracle_threads.argtypes = []
+    lib.oracle_threads.restype = ctypes.c_int
+    return lib
+
+
+def _load_parallel():
+    global _lib_omp
+    with _lock:
+        if _lib_omp is None:
+            path = build_parallel()
+            if path is None:
+                return None
+            _lib_omp = _declare(ctypes.CDLL(path))
+    return _lib_omp
+
+
+def parallel_threads() -> int:
+    """Threads of the OpenMP build's count loop (0 when it cannot be built)."""
+    lib = _load_parallel()
+    return int(lib.oracle_threads()) if lib is not None else 0
+
+
+def dbscan_parallel(points, eps: float, min_pts: int):
+    """``dbscan`` through the OpenMP build (same source; identical results)."""
+    lib = _load_parallel()
+    if lib is None:
+        raise RuntimeError("the OpenMP build of the oracle is not available")
+    p = _as_f64(points)
+    n, d = p.shape
+    cnt = np.zeros(n, np.int32)
+    core = np.zeros(n, np.uint8)
+    label = np.zeros(n, np.int32)
+    rc = lib.oracle_dbscan(_ptr(p), n, d, float(eps), int(min_pts), _ptr(cnt), _ptr(core),
+                           _ptr(label))
+    if rc != 0:
+        raise MemoryError("oracle_dbscan could not allocate its queue")
+    return cnt, core, label
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            P = ctypes.c_void_p
-            i64, i32, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
-            lib.oracle_counts.argtypes = [P, i64, i32, f32, P]
-            lib.oracle_counts.restype = None
-            lib.oracle_row_counts.argtypes = [P, i64, i32, f32, P, i64, P]
-            lib.oracle_row_counts.restype = None
-            lib.oracle_row_neighbours.argtypes = [P, i64, i32, f32, i64, P, i64]
-            lib.oracle_row_neighbours.restype = i64
-            lib.oracle_dbscan.argtypes = [P, i64, i32, f32, i32, P, P, P]
-            lib.oracle_dbscan.restype = ctypes.c_int
-            _lib = lib
+            _lib = _declare(ctypes.CDLL(build()))
     return _lib
 
 

@@ -38,6 +38,9 @@
  */
 #include <stdint.h>
 #include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* eps^2 as the single-precision product of the single-precision eps. */
 static double threshold_sq(float eps)
@@ -105,6 +108,18 @@ int64_t oracle_row_neighbours(const double *pts, int64_t n, int32_t d,
     return c;
 }
 
+/* Threads the count loop of oracle_dbscan uses: 1 unless this file was built
+ * with OpenMP (a separately timed baseline; the loop's iterations are
+ * independent, so the result does not depend on it). */
+int oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
 /* Full DBSCAN.  Outputs: cnt[n], core[n] (0/1), label[n] (cluster name or -1).
  * Returns 0, or -1 if the work queue cannot be allocated. */
 int oracle_dbscan(const double *pts, int64_t n, int32_t d, float eps,
@@ -112,6 +127,7 @@ int oracle_dbscan(const double *pts, int64_t n, int32_t d, float eps,
 {
     double thr = threshold_sq(eps);
 
+#pragma omp parallel for schedule(dynamic, 64)
     for (int64_t i = 0; i < n; ++i) {
         cnt[i] = neighbour_count(pts, n, d, thr, i);
         core[i] = (uint8_t)(cnt[i] >= min_pts);

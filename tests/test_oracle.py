@@ -311,3 +311,16 @@ def test_compact_labels_of_a_clustering_keeps_the_partition():
     for i in range(len(lab)):
         for j in range(len(lab)):
             assert (lab[i] == lab[j]) == (out[i] == out[j])
+
+
+def test_openmp_build_gives_identical_results():
+    # the separately timed OpenMP build of the same source (count loop on all
+    # host cores) must return exactly what the single-threaded build does
+    if oracle.parallel_threads() == 0:
+        pytest.skip("no OpenMP-capable compiler")
+    for P, eps, mp in ((synth.scaled("blobs_1m_d3", 3_000, seed=81), 10.0, 8),
+                       (synth.scaled("blobs_200k_d16", 1_500, seed=82), 120.0, 20)):
+        a = oracle.dbscan(P, eps, mp)
+        b = oracle.dbscan_parallel(P, eps, mp)
+        for x, y in zip(a, b):
+            assert np.array_equal(x, y)
