@@ -213,8 +213,12 @@ def cpu_baseline_parallel(P, eps, min_pts, m=40000):
     t = time.perf_counter()
     oracle.dbscan_parallel(P[:m], eps, min_pts)
     dt = time.perf_counter() - t
+    t = time.perf_counter()
+    oracle.dbscan(P[:m], eps, min_pts)       # the single-threaded build on the same sample
+    ds = time.perf_counter() - t
     return {"value": m * m / dt, "unit": UNIT, "cores": threads,
             "kind": "oracle, OpenMP build of the same source",
+            "single_thread_same_sample": m * m / ds,
             "sample": f"first {m} of {len(P)} points of the workload, full oracle DBSCAN "
                       f"(count on {threads} threads, cluster expansion serial), {dt:.1f} s"}
 
