@@ -14,6 +14,7 @@
 //   finalize candidates without a core neighbour become noise        O(Nb)
 // Nothing of size N x N is ever stored.
 #include "dbscan_internal.cuh"
+#include "tc_schedule.h"
 
 #include <math.h>
 #include <stdlib.h>
@@ -227,7 +228,10 @@ static int stage_launches(int d, float eps2, int stage) {
     case 0: return 9 + umma;
     case 1: return 1 + ntc;
     case 2: return 4 + umma;
-    case 3: return 1 + 2 + 1 + 6 * ntc + 5;
+    // tile-local union, two CUDA-core waves and their compression, and per
+    // tensor-core band: a launch per kind, a tile-root snapshot and (after the
+    // first) a compression
+    case 3: return 1 + 2 + 1 + UNION_BANDS * (ntc + 1) + (UNION_BANDS - 1);
     case 4: return 2;
     case 5: return umma + 1 + ntc;
     default: return 1;
