@@ -85,14 +85,17 @@ __host__ __device__ inline bool use_pivots(int d) { return d > PIVOT_MIN_D && d 
 // coordinates pivot_dim picks (at most 16: enough to tell clusters apart).
 // Pivots are the input points floor(j n / P).  |x - p|^2 = |x|^2 + |p|^2 - 2 x.p, and
 // |x|^2 is the same for every pivot, so each thread minimises |p|^2 - 2 x.p
-// with its point in registers, four pivots at a time (one 16-byte load of
-// -2p feeds four independent FMA chains).  Float rounding only perturbs the
-// order, never a result.
-__global__ void __launch_bounds__(256) k_pivot_assign(const void *pts, int dtype, int64_t n, int d,
-                                                      int *pid) {
+// for PIVOT_PPT points held in registers, four pivots at a time: one 16-byte
+// shared-memory load of -2p feeds 4 x PIVOT_PPT independent FMA chains (the
+// pivot table is read once per PIVOT_PPT points, which bounds the kernel).
+// Float rounding only perturbs the order, never a result.
+constexpr int PIVOT_PPT = 4;
+constexpr int PIVOT_THREADS = 256;
+__global__ void __launch_bounds__(PIVOT_THREADS) k_pivot_assign(const void *pts, int dtype, int64_t n,
+                                                                int d, int *pid) {
     constexpr int P = 1 << PIVOT_BITS;
     __shared__ __align__(16) float s_piv[PIVOT_DIMS * P];   // -2 p_jm at m * P + j
-    __shared__ float s_pn[P];                                // |p_j|^2 over those coordinates
+    __shared__ __align__(16) float s_pn[P];                  // |p_j|^2 over those coordinates
     for (int e = threadIdx.x; e < P * PIVOT_DIMS; e += blockDim.x) {
         const int j = e % P, m = e / P;
         const int64_t src = (int64_t)j * n / P;
@@ -105,29 +108,55 @@ __global__ void __launch_bounds__(256) k_pivot_assign(const void *pts, int dtype
         s_pn[j] = 0.25f * q;
     }
     __syncthreads();
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    float x[PIVOT_DIMS];
+    // point q of this thread: base + q * blockDim.x (consecutive threads,
+    // consecutive points)
+    const int64_t base = (int64_t)blockIdx.x * blockDim.x * PIVOT_PPT + threadIdx.x;
+    float x[PIVOT_PPT][PIVOT_DIMS];
 #pragma unroll
-    for (int m = 0; m < PIVOT_DIMS; ++m) x[m] = pivot_coord(pts, dtype, i, m, d);
-    float best = INFINITY;
-    int bj = 0;
+    for (int q = 0; q < PIVOT_PPT; ++q) {
+        const int64_t i = base + (int64_t)q * blockDim.x;
+#pragma unroll
+        for (int m = 0; m < PIVOT_DIMS; ++m) x[q][m] = i < n ? pivot_coord(pts, dtype, i, m, d) : 0.f;
+    }
+    float best[PIVOT_PPT];
+    int bj[PIVOT_PPT];
+#pragma unroll
+    for (int q = 0; q < PIVOT_PPT; ++q) {
+        best[q] = INFINITY;
+        bj[q] = 0;
+    }
     for (int j0 = 0; j0 < P; j0 += 4) {
-        float a0 = s_pn[j0], a1 = s_pn[j0 + 1], a2 = s_pn[j0 + 2], a3 = s_pn[j0 + 3];
+        const float4 pn = *reinterpret_cast<const float4 *>(s_pn + j0);
+        float a[PIVOT_PPT][4];
+#pragma unroll
+        for (int q = 0; q < PIVOT_PPT; ++q) {
+            a[q][0] = pn.x;
+            a[q][1] = pn.y;
+            a[q][2] = pn.z;
+            a[q][3] = pn.w;
+        }
 #pragma unroll
         for (int m = 0; m < PIVOT_DIMS; ++m) {
             const float4 pv = *reinterpret_cast<const float4 *>(s_piv + m * P + j0);
-            a0 = fmaf(x[m], pv.x, a0);
-            a1 = fmaf(x[m], pv.y, a1);
-            a2 = fmaf(x[m], pv.z, a2);
-            a3 = fmaf(x[m], pv.w, a3);
+#pragma unroll
+            for (int q = 0; q < PIVOT_PPT; ++q) {
+                a[q][0] = fmaf(x[q][m], pv.x, a[q][0]);
+                a[q][1] = fmaf(x[q][m], pv.y, a[q][1]);
+                a[q][2] = fmaf(x[q][m], pv.z, a[q][2]);
+                a[q][3] = fmaf(x[q][m], pv.w, a[q][3]);
+            }
         }
-        if (a0 < best) { best = a0; bj = j0; }
-        if (a1 < best) { best = a1; bj = j0 + 1; }
-        if (a2 < best) { best = a2; bj = j0 + 2; }
-        if (a3 < best) { best = a3; bj = j0 + 3; }
+#pragma unroll
+        for (int q = 0; q < PIVOT_PPT; ++q)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (a[q][c] < best[q]) { best[q] = a[q][c]; bj[q] = j0 + c; }
     }
-    pid[i] = bj;
+#pragma unroll
+    for (int q = 0; q < PIVOT_PPT; ++q) {
+        const int64_t i = base + (int64_t)q * blockDim.x;
+        if (i < n) pid[i] = bj[q];
+    }
 }
 
 // One thread: the axes' lower bounds and quantisation scales into Ctrl.
@@ -270,7 +299,10 @@ cudaError_t launch_order(const void *points, int dtype, int64_t n, int d, const 
     if (cudaMemsetAsync(w.hist, 0, (size_t)nbins * sizeof(int), s) != cudaSuccess) return cudaGetLastError();
     k_order_setup<<<1, 32, 0, s>>>(w.ctrl, w.stat_min, w.stat_max, d);
     const int blocks = (int)((n + 255) / 256);
-    if (use_pivots(d)) k_pivot_assign<<<blocks, 256, 0, s>>>(points, dtype, n, d, w.bin);
+    if (use_pivots(d)) {
+        const int64_t per = (int64_t)PIVOT_THREADS * PIVOT_PPT;
+        k_pivot_assign<<<(unsigned)((n + per - 1) / per), PIVOT_THREADS, 0, s>>>(points, dtype, n, d, w.bin);
+    }
     k_order_key<<<blocks, 256, 0, s>>>(points, dtype, n, d, w.ctrl, 30 - L.order_bits, w.bin,
                                        w.hist);
     k_bin_scan<<<nblk, BIN_SCAN_THREADS, 0, s>>>(w.hist, nbins, w.bstart, w.btot);
