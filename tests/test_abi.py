@@ -94,3 +94,19 @@ def test_host_side_argument_errors(lib):
     assert f(fake, 0, 10, 3, 1.0, 2, fake, fake, ctypes.c_void_p(0x10010), 1 << 30, None) == INVALID
     # n == 0 is a no-op, whatever the pointers
     assert f(None, 0, 0, 3, 1.0, 2, None, None, None, 0, None) == 0
+
+
+def test_compact_labels_host_side_errors(lib):
+    f = lib.dbscan_compact_labels
+    f.restype = ctypes.c_int
+    P = ctypes.c_void_p
+    f.argtypes = [P, ctypes.c_int64, P, P, P]
+    INVALID, UNSUP = -1, -2
+    k = ctypes.c_int32(-7)
+    assert f(None, -1, None, ctypes.byref(k), None) == INVALID       # negative n
+    assert f(None, 10, None, None, None) == INVALID                  # no place for k
+    assert f(None, 1 << 31, None, ctypes.byref(k), None) == UNSUP    # beyond int32 labels
+    assert f(None, 10, None, ctypes.byref(k), None) == INVALID       # null buffers with n > 0
+    assert k.value == -7                                             # untouched on error
+    assert f(None, 0, None, ctypes.byref(k), None) == 0               # n == 0: k = 0
+    assert k.value == 0
