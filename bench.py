@@ -153,13 +153,15 @@ def count_flops(n: int, d: int) -> float:
 KERNEL_FILES = ("sweep_tc.cu", "tc_schedule.h", "dbscan_internal.cuh")
 
 
-def kernel_code_hash() -> str:
+def kernel_code_hash(texts=None) -> str:
     """sha256 of the tensor-core sweep's code: its source and the headers it
-    includes, with comments and blank lines removed (a comment edit does not
-    change the kernel)."""
+    includes (or the given texts), with comments and blank lines removed (a
+    comment edit does not change the kernel)."""
+    if texts is None:
+        texts = [open(os.path.join(ROOT, "all_pairs_distance_gb300", "csrc", name)).read()
+                 for name in KERNEL_FILES]
     h = hashlib.sha256()
-    for name in KERNEL_FILES:
-        text = open(os.path.join(ROOT, "all_pairs_distance_gb300", "csrc", name)).read()
+    for text in texts:
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
         lines = [ln.strip() for ln in text.splitlines() if ln.strip()]

@@ -64,3 +64,15 @@ def test_reference_arm_prints_one_line_from_rank_zero():
     assert line["value"] == pytest.approx(2000 * 2000 / (line["ms_per_step"] * 1e-3), rel=1e-9)
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_kernel_code_hash_ignores_comments_only():
+    # the recorded ncu traffic stays valid across comment edits, not code edits
+    import bench
+    code = ["int f(int x) {\n    return x + 1;\n}\n", "#define N 4\n"]
+    commented = ["// f adds one\nint f(int x) {   /* body */\n\n    return x + 1;  // done\n}\n",
+                 "/* size\n   of it */\n#define N 4\n"]
+    changed = ["int f(int x) {\n    return x + 2;\n}\n", "#define N 4\n"]
+    assert bench.kernel_code_hash(code) == bench.kernel_code_hash(commented)
+    assert bench.kernel_code_hash(code) != bench.kernel_code_hash(changed)
+    assert bench.kernel_code_hash() == bench.kernel_code_hash(None)
