@@ -101,6 +101,14 @@ int dbscan_fit(const float *points, int64_t n, int32_t d, float eps,
  * With a caller workspace nothing waits for the GPU: host-side argument
  * errors and launch errors are returned, device-side errors are read later
  * with dbscan_workspace_status().
+ * Graph replay: with a caller workspace on a stream other than the legacy
+ * default stream, the first call with a given set of arguments (pointers,
+ * sizes, eps, min_pts, device) is captured into a CUDA graph, and later calls
+ * with the same arguments replay it; the graph reads whatever the buffers
+ * hold at replay, so results are those of a direct call.  The same holds for
+ * dbscan_fit_culled, dbscan_neighbor_counts and dbscan_fit_noalloc.  Not
+ * while the stream is being captured by the caller or stage profiling is on;
+ * the environment variable DBSCAN_GRAPHS=0 turns it off.
  * Cites: §II, §IV-A, §IV-B, §IV-B1, §IV-B2, §IV-C.
  */
 int dbscan_fit_ex(const void *points, int32_t dtype, int64_t n, int32_t d,
