@@ -169,20 +169,27 @@ def kernel_code_hash(texts=None) -> str:
     return h.hexdigest()
 
 
-def recorded_traffic(workload: str, path: str):
-    """Per-launch DRAM bytes of the count sweep from the committed ncu summary,
-    or None when the summary is missing, the kernel's code changed since, or
-    this run took another path."""
+def recorded_profile(workload: str, path: str, key: str):
+    """A figure of the count sweep's committed ncu summary (``key: value``
+    line), or None when the summary is missing, the kernel's code changed
+    since, or this run took another path."""
     summary = os.path.join(ROOT, "profiles", f"count_sweep_{workload}.md")
     if not os.path.exists(summary):
         return None
     text = open(summary).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m = re.search(rf"{key}:\s*([0-9.eE+]+)", text)
     h = re.search(r"sweep_code_sha256:\s*([0-9a-f]+)", text)
     k = re.search(r"sweep_path:\s*(\w+)", text)
     if not m or not h or not k or k.group(1) != path:
         return None
     return float(m.group(1)) if h.group(1) == kernel_code_hash() else None
+
+
+def recorded_traffic(workload: str, path: str):
+    """Per-launch DRAM bytes of the count sweep from the committed ncu summary,
+    or None when the summary is missing, the kernel's code changed since, or
+    this run took another path."""
+    return recorded_profile(workload, path, "traffic_bytes_per_launch")
 
 
 def cpu_baseline(P, eps, min_pts, target_s=12.0):
@@ -337,6 +344,7 @@ def run_gb300(args, dist: Dist):
     fp32_peak = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12
     achieved = count_flops(n, d) / (count_ms * 1e-3) / 1e12
     traffic = recorded_traffic(w.name, info["path"])
+    tp_active = recorded_profile(w.name, info["path"], "tensor_pipe_active_pct")
     # d <= 16: the distance pass is d FMAs per pair, so its roofline is the FP32
     # CUDA-core peak whichever unit evaluates it; d > 16: the bf16 tensor peak.
     tc_peak = None
@@ -376,6 +384,9 @@ def run_gb300(args, dist: Dist):
                                         "frac": achieved / fp32_peak,
                                         "note": "same algorithmic FLOP (2d per unordered pair) "
                                                 "against the derived FP32 CUDA-core peak"}}
+    # the executed view: the tensor pipe's active share in the committed ncu
+    # capture of this kernel and path (null once the kernel's code changed)
+    roofline["ncu_tensor_pipe_active"] = tp_active / 100.0 if tp_active is not None else None
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
