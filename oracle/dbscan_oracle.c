@@ -139,6 +139,17 @@ int oracle_dbscan(const double *pts, int64_t n, int32_t d, float eps,
     int64_t *queue = (int64_t *)malloc((size_t)n * sizeof(int64_t));
     if (!queue)
         return -1;
+#ifdef _OPENMP
+    /* OpenMP build only: the scan of one expansion step tests every j in
+     * parallel first (hit[j]), then applies the hits in ascending j.  Testing
+     * j reads label[j] alone and applying a hit writes label[j] alone, so the
+     * labels and the queue order are those of the plain loop below. */
+    uint8_t *hit = (uint8_t *)malloc((size_t)n);
+    if (!hit) {
+        free(queue);
+        return -1;
+    }
+#endif
 
     for (int64_t root = 0; root < n; ++root) {
         if (!core[root] || label[root] != -1)
@@ -149,6 +160,18 @@ int oracle_dbscan(const double *pts, int64_t n, int32_t d, float eps,
         queue[tail++] = root;
         while (head < tail) {
             int64_t q = queue[head++];          /* q is a core point */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+            for (int64_t j = 0; j < n; ++j)
+                hit[j] = (uint8_t)(label[j] == -1 && sq_dist(pts, d, q, j) <= thr);
+            for (int64_t j = 0; j < n; ++j) {
+                if (!hit[j])
+                    continue;
+                label[j] = name;
+                if (core[j])
+                    queue[tail++] = j;
+            }
+#else
             for (int64_t j = 0; j < n; ++j) {
                 if (label[j] != -1)
                     continue;
@@ -158,8 +181,12 @@ int oracle_dbscan(const double *pts, int64_t n, int32_t d, float eps,
                 if (core[j])
                     queue[tail++] = j;          /* only core points expand */
             }
+#endif
         }
     }
+#ifdef _OPENMP
+    free(hit);
+#endif
     free(queue);
     return 0;
 }
