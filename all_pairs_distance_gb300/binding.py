@@ -7,6 +7,7 @@ built (``__graft_entry__.build()``), every call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import enum
 import os
@@ -28,6 +29,15 @@ class Status(enum.IntEnum):
 
 
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+# Tensor-core path bits of dbscan_options.paths (dbscan.h DBSCAN_PATH_*).
+PATH_BITS = {"tf32": 1, "bf16": 2, "f16": 4, "f16acc16": 8}
+PATHS_DEFAULT = 1 | 2 | 4
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("paths", ctypes.c_uint32), ("rows", ctypes.c_int32 * 3),
+                ("graphs", ctypes.c_int32)]
 
 
 class DbscanError(RuntimeError):
@@ -80,6 +90,10 @@ def load():
         lib.dbscan_profile_end.restype = ctypes.c_int
         lib.dbscan_strerror.argtypes = [ctypes.c_int]
         lib.dbscan_strerror.restype = ctypes.c_char_p
+        lib.dbscan_set_options.argtypes = [P]
+        lib.dbscan_set_options.restype = ctypes.c_int
+        lib.dbscan_get_options.argtypes = [P]
+        lib.dbscan_get_options.restype = ctypes.c_int
         _lib = lib
         return _lib
 
@@ -101,6 +115,49 @@ def _points(points: torch.Tensor):
     if points.dtype not in DTYPES:
         raise TypeError("points must be float32 or bfloat16")
     return points.contiguous()
+
+
+def dbscan_get_options() -> dict:
+    """The process-wide tuning switches in force."""
+    o = Options()
+    _check(load().dbscan_get_options(ctypes.byref(o)), "dbscan_get_options")
+    return {"paths": int(o.paths), "rows": tuple(int(r) for r in o.rows), "graphs": int(o.graphs)}
+
+
+def dbscan_set_options(paths=None, rows=None, graphs=None, *, reset=False) -> None:
+    """Change the switches (arguments left None keep their value); ``paths``
+    is a bit mask or an iterable of names from PATH_BITS ("fp32" alone, or an
+    empty iterable, allows CUDA cores only); ``rows`` one int for every sweep
+    or three (count, union, border); ``reset`` restores the defaults."""
+    lib = load()
+    if reset:
+        _check(lib.dbscan_set_options(None), "dbscan_set_options")
+        return
+    cur = dbscan_get_options()
+    o = Options()
+    if paths is None:
+        o.paths = cur["paths"]
+    elif isinstance(paths, int):
+        o.paths = paths
+    else:
+        names = [paths] if isinstance(paths, str) else list(paths)
+        o.paths = sum(PATH_BITS[p] for p in names if p != "fp32")
+    r = cur["rows"] if rows is None else ((rows,) * 3 if isinstance(rows, int) else tuple(rows))
+    for i in range(3):
+        o.rows[i] = int(r[i])
+    o.graphs = cur["graphs"] if graphs is None else int(bool(graphs))
+    _check(lib.dbscan_set_options(ctypes.byref(o)), "dbscan_set_options")
+
+
+@contextlib.contextmanager
+def options(**kw):
+    """Switches changed inside a ``with`` block, restored afterwards."""
+    saved = dbscan_get_options()
+    dbscan_set_options(**kw)
+    try:
+        yield
+    finally:
+        dbscan_set_options(paths=saved["paths"], rows=saved["rows"], graphs=saved["graphs"])
 
 
 def dbscan_strerror(status: int) -> str:
@@ -219,7 +276,9 @@ def dbscan_workspace_status(workspace: torch.Tensor, stream=None) -> int:
     return int(load().dbscan_workspace_status(workspace.data_ptr(), _stream_handle(stream)))
 
 
-PATHS = {0: "fp32", 1: "tf32", 2: "bf16", 3: "f16"}
+# path codes of dbscan_workspace_info: f16 accumulates in f32; f16acc16 is the
+# opt-in f16 accumulator
+PATHS = {0: "fp32", 1: "tf32", 2: "bf16", 3: "f16", 4: "f16acc16"}
 
 
 def dbscan_workspace_info(workspace: torch.Tensor, stream=None) -> dict:

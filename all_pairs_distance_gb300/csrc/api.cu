@@ -19,6 +19,7 @@
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+#include <list>
 #include <map>
 #include <mutex>
 #include <set>
@@ -56,8 +57,8 @@ Layout make_layout(int64_t n, int32_t d) {
     L.off_bsum = off;        off += align256((size_t)2 * (L.nscan_blocks + 1) * sizeof(int));
     // tensor-core operand tiles, sized for the largest path this shape allows
     size_t kb = 0;
-    for (int kind = TC_TF32; kind <= TC_F16; ++kind) {
-        const int nt = kind == TC_F16 ? 2 : 3;   // the most threshold digits a kind takes
+    for (int kind = TC_TF32; kind <= TC_NKINDS; ++kind) {
+        const int nt = tc_is_f16(kind) ? 2 : 3;   // the most threshold digits a kind takes
         const int b = tc_kbytes(kind, d, nt);
         if (tc_fits(kind, d, nt) && (size_t)b > kb) kb = (size_t)b;
     }
@@ -94,35 +95,69 @@ Layout make_layout(int64_t n, int32_t d) {
     return L;
 }
 
-// The layout of one call: sizes plus eps and the culling switches.  Union and
-// border act only on neighbour pairs, all of which the count sweep has
-// evaluated; they skip tile pairs that the box test proves hold none (exact
-// data only, checked on the device).  The count sweep itself evaluates every
-// pair unless the caller asked for culling.
-static Layout call_layout(int64_t n, int32_t d, float eps, int cull) {
+// ---- tuning switches -----------------------------------------------------
+// Process-wide, read from the environment once (at the first call) and
+// replaced with dbscan_set_options; every call works on a snapshot.
+static std::mutex g_opt_mu;
+static bool g_opt_init = false;
+static dbscan_options g_opt;
+
+static dbscan_options options_from_env() {
+    dbscan_options o{};
+    o.paths = DBSCAN_PATHS_DEFAULT;
+    o.graphs = 1;
+    const char *f = getenv("DBSCAN_FORCE_PATH");
+    if (f && *f) {
+        if (!strcmp(f, "fp32")) o.paths = 0;
+        else if (!strcmp(f, "tf32")) o.paths = DBSCAN_PATH_TF32;
+        else if (!strcmp(f, "bf16")) o.paths = DBSCAN_PATH_BF16;
+        else if (!strcmp(f, "f16")) o.paths = DBSCAN_PATH_F16;
+        else if (!strcmp(f, "f16acc16")) o.paths = DBSCAN_PATH_F16_ACC16;
+    }
+    if (const char *r = getenv("DBSCAN_TC_ROWS")) {
+        const size_t len = strlen(r);
+        for (int m = 0; m < 3; ++m) {
+            const char c = len == 1 ? r[0] : (len == 3 ? r[m] : '0');
+            o.rows[m] = (c == '1' || c == '2') ? c - '0' : 0;
+        }
+    }
+    const char *g = getenv("DBSCAN_GRAPHS");
+    if (g && g[0] == '0') o.graphs = 0;
+    return o;
+}
+
+static dbscan_options options_snapshot() {
+    std::lock_guard<std::mutex> lock(g_opt_mu);
+    if (!g_opt_init) {
+        g_opt = options_from_env();
+        g_opt_init = true;
+    }
+    return g_opt;
+}
+
+// Tensor-core kinds a call may take: the allowed paths whose operand rows fit
+// dimension d with the threshold digits eps allows.
+static unsigned allowed_tc(int d, float eps2, unsigned paths) {
+    unsigned allow = 0;
+    for (int kind = TC_TF32; kind <= TC_NKINDS; ++kind)
+        if ((paths & tc_allow_bit(kind)) && tc_fits(kind, d, tc_nt_bound(kind, eps2)))
+            allow |= tc_allow_bit(kind);
+    return allow;
+}
+
+// The layout of one call: sizes plus eps, the culling switches and the
+// tuning switches in force.  Union and border act only on neighbour pairs,
+// all of which the count sweep has evaluated; they skip tile pairs that the
+// box test proves hold none (exact data only, checked on the device).  The
+// count sweep itself evaluates every pair unless the caller asked for culling.
+static Layout call_layout(int64_t n, int32_t d, float eps, int cull, const dbscan_options &o) {
     Layout L = make_layout(n, d);
     L.eps2 = eps * eps;
+    L.allow = L.umma_tile_bytes ? allowed_tc(d, L.eps2, o.paths) : 0u;
+    for (int m = 0; m < 3; ++m) L.rows[m] = o.rows[m];
     L.cull_nbr = L.box_floats > 0 && L.umma_tile_bytes > 0;
     L.cull = cull && L.cull_nbr;
     return L;
-}
-
-// Tensor-core paths this call may use (operand rows that fit the kind for the
-// threshold digits eps allows), narrowed by DBSCAN_FORCE_PATH ("fp32", "tf32",
-// "bf16" or "f16") when it is set.
-static int allowed_tc(int d, float eps2) {
-    int allow = 0;
-    if (tc_fits(TC_TF32, d, tc_nt_bound(TC_TF32, eps2))) allow |= TC_ALLOW_TF32;
-    if (tc_fits(TC_BF16, d, tc_nt_bound(TC_BF16, eps2))) allow |= TC_ALLOW_BF16;
-    if (tc_fits(TC_F16, d, tc_nt_bound(TC_F16, eps2))) allow |= TC_ALLOW_F16;
-    const char *f = getenv("DBSCAN_FORCE_PATH");
-    if (f && *f) {
-        if (!strcmp(f, "fp32")) allow = 0;
-        else if (!strcmp(f, "tf32")) allow &= TC_ALLOW_TF32;
-        else if (!strcmp(f, "bf16")) allow &= TC_ALLOW_BF16;
-        else if (!strcmp(f, "f16")) allow &= TC_ALLOW_F16;
-    }
-    return allow;
 }
 
 Work carve(void *base, const Layout &L) {
@@ -212,17 +247,16 @@ static void keep_pool(void) {
 }
 
 // ---- stage timing ------------------------------------------------------------
-// Kernels each stage launches for dimension d.  Every sweep launches its
-// CUDA-core kernel and one kernel per tensor-core path the shape allows
-// (ntc); all but the path chosen on the device return at once.
+// Kernels each stage launches.  Every sweep launches its CUDA-core kernel and
+// one kernel per tensor-core kind the call allows (ntc: the allowed paths
+// whose operand rows fit the shape); all but the path chosen on the device
+// return at once.
 //   prep 4 + 5 locality order (+1 operand staging), count 1 + ntc,
 //   compact 4 (+1 operand staging), union 1 tile-local + 2 CUDA-core waves
 //   + 1 compression + 6 tensor-core bands x ntc + 5 compressions, flatten 2,
 //   border (+1 operand staging) 1 + ntc, finalize 1.
-static int stage_launches(int d, float eps2, int stage) {
-    int ntc = 0;
-    for (int kind = TC_TF32; kind <= TC_F16; ++kind)
-        if (tc_fits(kind, d, tc_nt_bound(kind, eps2))) ++ntc;
+static int stage_launches(unsigned allow, int stage) {
+    const int ntc = __builtin_popcount(allow);
     const int umma = ntc > 0 ? 1 : 0;
     switch (stage) {
     case 0: return 9 + umma;
@@ -240,10 +274,9 @@ static int stage_launches(int d, float eps2, int stage) {
 
 struct ProfCall {
     cudaEvent_t ev[DBSCAN_NUM_STAGES + 1];
-    int stages;   // number of stages the call ran
-    int d;        // dimension of the call (sets the kernels per stage)
-    float eps2;   // eps^2 of the call (sets the tensor-core kinds launched)
-    int cull;     // 1: culled count, 2: culled union and border (box kernels)
+    int stages;       // number of stages the call ran
+    unsigned allow;   // tensor-core kinds launched by the call's sweeps
+    int cull;         // 1: culled count, 2: culled union and border (box kernels)
 };
 struct ProfState {
     bool on = false;
@@ -256,9 +289,8 @@ struct StageMarks {
     ProfCall call{};
     bool on = false;
     int next = 0;
-    StageMarks(cudaStream_t s, int d, float eps2, int cull) {
-        call.d = d;
-        call.eps2 = eps2;
+    StageMarks(cudaStream_t s, unsigned allow, int cull) {
+        call.allow = allow;
         call.cull = cull;
         if (!g_prof.on) return;
         for (int i = 0; i <= DBSCAN_NUM_STAGES; ++i) {
@@ -289,10 +321,10 @@ static int run(const void *points, int dtype, int64_t n, int d, float eps, int m
                int32_t *labels, uint8_t *is_core, int32_t *cnt_out, void *ws, const Layout &L,
                cudaStream_t s) {
     Work w = carve(ws, L);
-    StageMarks marks(s, d, L.eps2, L.cull + 2 * L.cull_nbr);
+    StageMarks marks(s, L.allow, L.cull + 2 * L.cull_nbr);
     if (cudaMemsetAsync(w.ctrl, 0, sizeof(Ctrl), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     if (cudaMemsetAsync(w.cnt, 0, (size_t)n * sizeof(int), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
-    if (launch_prep(points, dtype, n, d, eps, allowed_tc(d, L.eps2), w, L, s) != cudaSuccess)
+    if (launch_prep(points, dtype, n, d, eps, L.allow, w, L, s) != cudaSuccess)
         return DBSCAN_ERR_CUDA;
     if (L.cull && launch_tile_boxes(w, L, 0, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     marks.mark(s);
@@ -332,22 +364,27 @@ static int read_status(const void *ws, cudaStream_t s) {
 // A call is some sixty launches whose every decision is taken on the device,
 // so a call on a caller's stream and workspace is captured once into a CUDA
 // graph and replayed while its arguments repeat (the graph reads whatever the
-// buffers hold at replay).  Keys: every argument, the device, and the two
-// environment switches the host consults.  Not on the legacy default stream
-// (it cannot be captured), not while the stream is already capturing (the
-// caller's own capture then takes the launches), not while stage profiling
-// records events; DBSCAN_GRAPHS=0 turns it off.  At most kGraphCap graphs
-// are kept; further keys launch directly.
+// buffers hold at replay).  Keys: every argument, the device, and the tuning
+// switches of the call.  Not on the legacy default stream (it cannot be
+// captured), not while the stream is already capturing (the caller's own
+// capture then takes the launches), not while stage profiling records
+// events, not with the graphs switch off.  At most kGraphCap graphs are kept,
+// the least recently used one destroyed to make room (an instance still
+// running is freed when it completes).
 using GraphKey = std::tuple<int, const void *, int, int64_t, int, uint32_t, int, void *, void *, void *,
-                            void *, int, std::string>;
+                            void *, int, unsigned, int, int, int>;
+struct GraphEntry {
+    GraphKey key;
+    cudaGraphExec_t exec;
+};
 static std::mutex g_graph_mu;
-static std::map<GraphKey, cudaGraphExec_t> g_graphs;
+static std::list<GraphEntry> g_graph_lru;   // most recently used first
+static std::map<GraphKey, std::list<GraphEntry>::iterator> g_graphs;
 static std::set<GraphKey> g_graph_failed;   // keys whose capture failed: launched directly
 constexpr size_t kGraphCap = 16;
 
-static bool graphs_enabled(cudaStream_t s) {
-    const char *e = getenv("DBSCAN_GRAPHS");
-    if (e && e[0] == '0') return false;
+static bool graphs_enabled(cudaStream_t s, const dbscan_options &o) {
+    if (!o.graphs) return false;
     if (s == nullptr || s == cudaStreamLegacy || g_prof.on) return false;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
@@ -357,26 +394,23 @@ static bool graphs_enabled(cudaStream_t s) {
     return cs == cudaStreamCaptureStatusNone;
 }
 
-static std::string env_switches() {
-    const char *f = getenv("DBSCAN_FORCE_PATH"), *r = getenv("DBSCAN_TC_ROWS");
-    return std::string(f ? f : "") + "|" + (r ? r : "");
-}
-
 // run() through a cached graph; -1 when the graph path does not apply.
 static int run_graph(const void *points, int dtype, int64_t n, int d, float eps, int min_pts,
                      int32_t *labels, uint8_t *is_core, int32_t *cnt_out, void *ws, const Layout &L,
-                     cudaStream_t s) {
-    if (!graphs_enabled(s)) return -1;
+                     const dbscan_options &o, cudaStream_t s) {
+    if (!graphs_enabled(s, o)) return -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     uint32_t eb;
     memcpy(&eb, &eps, sizeof(eb));
     const GraphKey key(dev, points, dtype, n, d, eb, min_pts, labels, is_core, cnt_out, ws, L.cull,
-                       env_switches());
+                       L.allow, L.rows[0], L.rows[1], L.rows[2]);
     std::lock_guard<std::mutex> lock(g_graph_mu);
     auto it = g_graphs.find(key);
-    if (it == g_graphs.end()) {
-        if (g_graphs.size() >= kGraphCap || g_graph_failed.count(key)) return -1;
+    if (it != g_graphs.end()) {
+        g_graph_lru.splice(g_graph_lru.begin(), g_graph_lru, it->second);
+    } else {
+        if (g_graph_failed.count(key)) return -1;
         if (cudaStreamBeginCapture(s, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
             cudaGetLastError();
             if (g_graph_failed.size() < 64) g_graph_failed.insert(key);
@@ -394,22 +428,31 @@ static int run_graph(const void *points, int dtype, int64_t n, int d, float eps,
             if (g_graph_failed.size() < 64) g_graph_failed.insert(key);
             return -1;   // launched directly instead
         }
-        it = g_graphs.emplace(key, ex).first;
+        if (g_graphs.size() >= kGraphCap) {   // make room: drop the least recently used
+            cudaGraphExecDestroy(g_graph_lru.back().exec);
+            g_graphs.erase(g_graph_lru.back().key);
+            g_graph_lru.pop_back();
+        }
+        g_graph_lru.push_front(GraphEntry{key, ex});
+        it = g_graphs.emplace(key, g_graph_lru.begin()).first;
     }
-    return cudaGraphLaunch(it->second, s) == cudaSuccess ? DBSCAN_OK : DBSCAN_ERR_CUDA;
+    return cudaGraphLaunch(it->second->exec, s) == cudaSuccess ? DBSCAN_OK : DBSCAN_ERR_CUDA;
 }
 
 // Shared body of dbscan_fit_ex and dbscan_neighbor_counts.
+// use_graph = false: launch directly, never capture (dbscan_fit_noalloc).
 static int fit_common(const void *points, int32_t dtype, int64_t n, int32_t d, float eps,
                       int32_t min_pts, int32_t *labels, uint8_t *is_core, int32_t *cnt_out,
-                      void *workspace, size_t workspace_bytes, void *stream, int cull = 0) {
+                      void *workspace, size_t workspace_bytes, void *stream, int cull = 0,
+                      bool use_graph = true) {
     int st = check_shape(n, d, dtype);
     if (st != DBSCAN_OK) return st;
     if ((st = check_scalars(eps, min_pts)) != DBSCAN_OK) return st;
     if (n == 0) return DBSCAN_OK;
     if (!points) return DBSCAN_ERR_INVALID_ARG;
     if (!cnt_out && (!labels || !is_core)) return DBSCAN_ERR_INVALID_ARG;
-    const Layout L = call_layout(n, d, eps, cull);
+    const dbscan_options opt = options_snapshot();
+    const Layout L = call_layout(n, d, eps, cull, opt);
     if (workspace) {
         if (workspace_bytes < L.total) return DBSCAN_ERR_INVALID_ARG;
         if (reinterpret_cast<uintptr_t>(workspace) & 255) return DBSCAN_ERR_INVALID_ARG;
@@ -425,8 +468,9 @@ static int fit_common(const void *points, int32_t dtype, int64_t n, int32_t d, f
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     if (workspace) {
-        const int gst = run_graph(points, dtype, n, d, eps, min_pts, labels, is_core, cnt_out,
-                                  workspace, L, s);
+        const int gst = use_graph ? run_graph(points, dtype, n, d, eps, min_pts, labels, is_core,
+                                              cnt_out, workspace, L, opt, s)
+                                  : -1;
         if (gst >= 0) return gst;
         return run(points, dtype, n, d, eps, min_pts, labels, is_core, cnt_out, workspace, L, s);
     }
@@ -442,6 +486,13 @@ static int fit_common(const void *points, int32_t dtype, int64_t n, int32_t d, f
     cudaFreeAsync(ws, s);
     if (cudaStreamSynchronize(s) != cudaSuccess && st == DBSCAN_OK) st = DBSCAN_ERR_CUDA;
     return st != DBSCAN_OK ? st : dev_st;
+}
+
+int fit_direct(const void *points, int32_t dtype, int64_t n, int32_t d, float eps, int32_t min_pts,
+               int32_t *labels, uint8_t *is_core, void *workspace, size_t workspace_bytes,
+               void *stream) {
+    return fit_common(points, dtype, n, d, eps, min_pts, labels, is_core, nullptr, workspace,
+                      workspace_bytes, stream, 0, false);
 }
 
 }  // namespace dbscan
@@ -495,6 +546,31 @@ int dbscan_neighbor_counts(const void *points, int32_t dtype, int64_t n, int32_t
                       workspace_bytes, stream);
 }
 
+int dbscan_set_options(const dbscan_options *opt) {
+    dbscan_options o;
+    if (opt) {
+        const unsigned known = DBSCAN_PATH_TF32 | DBSCAN_PATH_BF16 | DBSCAN_PATH_F16 |
+                               DBSCAN_PATH_F16_ACC16;
+        if (opt->paths & ~known) return DBSCAN_ERR_INVALID_ARG;
+        for (int m = 0; m < 3; ++m)
+            if (opt->rows[m] < 0 || opt->rows[m] > 2) return DBSCAN_ERR_INVALID_ARG;
+        if (opt->graphs < 0 || opt->graphs > 1) return DBSCAN_ERR_INVALID_ARG;
+        o = *opt;
+    } else {
+        o = options_from_env();
+    }
+    std::lock_guard<std::mutex> lock(g_opt_mu);
+    g_opt = o;
+    g_opt_init = true;
+    return DBSCAN_OK;
+}
+
+int dbscan_get_options(dbscan_options *opt) {
+    if (!opt) return DBSCAN_ERR_INVALID_ARG;
+    *opt = options_snapshot();
+    return DBSCAN_OK;
+}
+
 int dbscan_workspace_info(const void *workspace, void *stream, int64_t *info, int32_t n) {
     if (!workspace || !info || n < 1) return DBSCAN_ERR_INVALID_ARG;
     Ctrl c;
@@ -529,7 +605,7 @@ int dbscan_profile_end(float *stage_ms, int32_t max_stages, int64_t *calls,
             acc[i] += ms;
             // box kernels: all points in prep (culled count), core and
             // candidate arrays after compaction (union and border)
-            launches += stage_launches(c.d, c.eps2, i) + ((c.cull & 1) && i == 0 ? 2 : 0) +
+            launches += stage_launches(c.allow, i) + ((c.cull & 1) && i == 0 ? 2 : 0) +
                         ((c.cull & 2) && i == 2 ? 3 : 0);
         }
         for (int i = 0; i <= c.stages; ++i) cudaEventDestroy(c.ev[i]);
@@ -591,7 +667,7 @@ int dbscan_fit_host(const void *points_host, int32_t dtype, int64_t n, int32_t d
     if (n == 0) return DBSCAN_OK;
     if (!points_host || !labels_host || !is_core_host) return DBSCAN_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const Layout L = call_layout(n, d, eps, 0);
+    const Layout L = call_layout(n, d, eps, 0, options_snapshot());
     const size_t esz = dtype == DBSCAN_BF16 ? 2 : 4;
     const size_t pbytes = align256((size_t)n * d * esz);
     const size_t lbytes = align256((size_t)n * sizeof(int32_t));

@@ -41,7 +41,7 @@ struct Ctrl {
     int n_all;          // number of points
     unsigned unit_ctr[8];   // work-unit counters: count, union waves 1-4, border
     float range_sq;     // sum_k (max_k - min_k)^2
-    int tc_kind;        // tensor-core path chosen by setup: TC_NONE, TC_TF32, TC_BF16
+    int tc_kind;        // tensor-core path chosen by setup: a TcKind (TC_NONE = CUDA cores)
     int tc_kpad;        // padded K of the tensor-core operands (elements)
     int tc_kbytes;      // bytes of one operand row (tc_kpad * element size)
     int tc_nt;          // digits of the threshold constant in the operands
@@ -57,6 +57,8 @@ struct Layout {
     int64_t n;
     int32_t d;
     float eps2;           // fl32(eps * eps) of the call (0 in a bare size query)
+    unsigned allow;       // tensor-core kinds the call may take (TC_ALLOW_* bits)
+    int rows[3];          // row blocks per unit of count, union, border (0 = automatic)
     int64_t ntiles;       // ceil(n / BT)
     size_t tile_floats;   // (d + 1) * BT
     size_t off_ctrl, off_stats, off_staged_all, off_staged_core, off_staged_cand;
@@ -114,20 +116,32 @@ enum SweepMode { SWEEP_COUNT = 0, SWEEP_UNION = 1, SWEEP_BORDER = 2 };
 // MMA yields w_ij = |c_i - c_j|^2 - thrx exactly (see prep.cu):
 //   TF32: elements exact up to 2048, base 2048, 2 digits per norm, f32 accumulator
 //   BF16: elements exact up to 256,  base 256,  3 digits per norm, f32 accumulator
-//   F16:  elements exact up to 2048, base 2048, 2 digits per norm, f16 accumulator;
-//         only when every operand row fits one K = 16 MMA, so the exact sum is
-//         rounded to f16 once (its sign, all the sweep reads, survives)
-// plus nt digits of thrx (1..3; at most 2 for F16, whose largest power is B).
-enum TcKind { TC_NONE = 0, TC_TF32 = 1, TC_BF16 = 2, TC_F16 = 3 };
-// Allowed-path mask passed from the host (all by default).
-enum { TC_ALLOW_TF32 = 1, TC_ALLOW_BF16 = 2, TC_ALLOW_F16 = 4 };
+//   F16:  elements exact up to 2048, base 2048, 2 digits per norm, f32 accumulator
+//   F16H: the F16 operands with an f16 accumulator, only when the whole operand
+//         row fits one K = 16 MMA (so the exact integer sum is rounded to f16
+//         once); chosen only when the caller opts in (DBSCAN_PATH_F16_ACC16):
+//         that the tensor core forms the K = 16 sum exactly before its one
+//         rounding is not documented, only observed on GB300 by the tests
+// plus nt digits of thrx (1..3; at most 2 for F16 and F16H, whose largest
+// power is B).
+enum TcKind { TC_NONE = 0, TC_TF32 = 1, TC_BF16 = 2, TC_F16 = 3, TC_F16H = 4 };
+constexpr int TC_NKINDS = 4;
+// Allowed-path mask passed from the host: the DBSCAN_PATH_* bits of dbscan.h.
+enum {
+    TC_ALLOW_TF32 = DBSCAN_PATH_TF32,
+    TC_ALLOW_BF16 = DBSCAN_PATH_BF16,
+    TC_ALLOW_F16 = DBSCAN_PATH_F16,
+    TC_ALLOW_F16H = DBSCAN_PATH_F16_ACC16
+};
+__host__ __device__ inline unsigned tc_allow_bit(int kind) { return 1u << (kind - 1); }
 // Largest operand row the tensor-core sweep stages: two row tiles and two
 // stages of two column tiles (plus their aux ints) must fit 224 KB of shared
-// memory, 768 x kbytes + 2 KB; 288 bytes is 144 bf16 (d <= 137) or 72 tf32
-// (d <= 67) elements.
+// memory, 768 x kbytes + 2 KB; 288 bytes is 144 bf16/f16 (d <= 137) or 72
+// tf32 (d <= 67) elements.
 constexpr int TC_MAX_KBYTES = 288;
-constexpr int TC_F16_KBYTES = 32;    // the one K = 16 MMA of the F16 path
+constexpr int TC_F16H_KBYTES = 32;   // the one K = 16 MMA of the F16H path
 
+__host__ __device__ inline bool tc_is_f16(int kind) { return kind == TC_F16 || kind == TC_F16H; }
 __host__ __device__ inline int tc_norm_digits(int kind) { return kind == TC_BF16 ? 3 : 2; }
 __host__ __device__ inline int tc_kpad(int kind, int d, int nt) {
     const int used = d + 2 * tc_norm_digits(kind) + nt;
@@ -138,7 +152,8 @@ __host__ __device__ inline int tc_kbytes(int kind, int d, int nt) {
 }
 // Whether a kind can hold the operand rows of dimension d with nt threshold digits.
 __host__ __device__ inline bool tc_fits(int kind, int d, int nt) {
-    if (kind == TC_F16) return nt <= 2 && tc_kbytes(kind, d, nt) <= TC_F16_KBYTES;
+    if (kind == TC_F16H) return nt <= 2 && tc_kbytes(kind, d, nt) <= TC_F16H_KBYTES;
+    if (kind == TC_F16) return nt <= 2 && tc_kbytes(kind, d, nt) <= TC_MAX_KBYTES;
     return tc_kbytes(kind, d, nt) <= TC_MAX_KBYTES;
 }
 // Digits of the threshold constant thrx (<= floor(eps2) + 1, see prep.cu)
@@ -187,6 +202,12 @@ cudaError_t launch_union_tc_band(const Work &w, const Layout &L, int band, int b
 cudaError_t launch_border_tc(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
 
 int persistent_ctas(const void *kernel, int threads, size_t smem);
+
+// dbscan_fit_ex with a caller workspace, its kernels always launched directly
+// (no graph capture or instantiation): the body of dbscan_fit_noalloc.
+int fit_direct(const void *points, int32_t dtype, int64_t n, int32_t d, float eps, int32_t min_pts,
+               int32_t *labels, uint8_t *is_core, void *workspace, size_t workspace_bytes,
+               void *stream);
 
 // Label compaction (labels.cu): scratch bytes for n labels; the ranking passes
 // (*k_err points at the cluster count and the error flag in the scratch); the

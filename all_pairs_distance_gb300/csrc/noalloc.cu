@@ -1,7 +1,9 @@
 // dbscan_fit_noalloc: the full DBSCAN with its workspace in static device
 // memory, for callers that cannot allocate device memory (see dbscan.h).
 // Nothing here calls cudaMalloc, cudaFree or any allocating routine; the
-// pipeline itself is dbscan_fit_ex, handed this file's array as workspace.
+// pipeline itself is dbscan_fit_ex's, handed this file's array as workspace,
+// with every kernel launched directly: it never captures or instantiates a
+// CUDA graph, which would take device resources of its own.
 #include "dbscan_internal.cuh"
 
 #include <mutex>
@@ -56,6 +58,6 @@ extern "C" int dbscan_fit_noalloc(const void *points, int32_t dtype, int64_t n, 
     if (st != DBSCAN_OK) return st;
     // The pipeline clears its control block and counters at the start of
     // every call, so the previous call's contents of the array do no harm.
-    return dbscan_fit_ex(points, dtype, n, d, eps, min_pts, labels_out, is_core_out, ws,
-                         (size_t)DBSCAN_NOALLOC_SCRATCH_BYTES, stream);
+    return dbscan::fit_direct(points, dtype, n, d, eps, min_pts, labels_out, is_core_out, ws,
+                              (size_t)DBSCAN_NOALLOC_SCRATCH_BYTES, stream);
 }

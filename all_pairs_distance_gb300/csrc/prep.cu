@@ -28,10 +28,12 @@
 // every element exactly representable.  The positive terms sum to at most
 // 4 S and the negative ones to at most 2 S + thrx (S = sum_k M_k^2); when both
 // are below 2^24 every partial sum the tensor core forms, in any order, is an
-// exact integer, and w_ij < 0 <=> neighbour.  The f16 kind is used only when
-// the whole row fits one K = 16 MMA: its f16 accumulator then rounds the exact
-// sum once, which keeps the sign (the smallest nonzero |w| is 1; overflow gives
-// +-inf; an exact zero is stored as +0).
+// exact integer, and w_ij < 0 <=> neighbour.  Every kind accumulates in f32,
+// except the opt-in F16H kind, taken only when the whole row fits one K = 16
+// MMA: its f16 accumulator rounds the sum once, which keeps the sign (the
+// smallest nonzero |w| is 1; overflow gives +-inf; an exact zero is stored as
+// +0) provided the tensor core forms the K = 16 sum exactly first -- not
+// documented by NVIDIA, observed on GB300 by the tests.
 #include "dbscan_internal.cuh"
 
 #include <math.h>
@@ -87,7 +89,7 @@ __global__ void k_stats(const void *pts, int dtype, int64_t n, int d, Ctrl *ctrl
 }
 
 // One block: centres, the exactness bound, the threshold constant and the
-// tensor-core path (allow: mask of TC_ALLOW_* the caller permits).
+// tensor-core path (allow: mask of TC_ALLOW_* the call permits).
 __global__ void k_setup(Ctrl *ctrl, const int *smin, const int *smax, float *centre,
                         int d, float eps2, int allow) {
     __shared__ double part[DBSCAN_MAX_D];
@@ -127,14 +129,19 @@ __global__ void k_setup(Ctrl *ctrl, const int *smin, const int *smax, float *cen
         const int nt = tc_nt_for(TC_TF32, thrx);
         int kind = TC_NONE;
         if (integral && !ctrl->nonfinite && 4.0 * S < 16777216.0 && 2.0 * S + thrx < 16777216.0) {
-            // preference: F16 (one MMA, half-width accumulator reads), then BF16, then TF32
+            // preference: the opt-in F16H (one MMA, half-width accumulator reads),
+            // then BF16 (ranges up to 256), F16 (up to 2048; the same MMA rate),
+            // TF32 (half the rate; threshold constants of three digits)
             const int ntb = tc_nt_for(TC_BF16, thrx);
-            if ((allow & TC_ALLOW_F16) && rmax <= 2048.0 && tc_fits(TC_F16, d, nt)) {
-                kind = TC_F16;
+            if ((allow & TC_ALLOW_F16H) && rmax <= 2048.0 && tc_fits(TC_F16H, d, nt)) {
+                kind = TC_F16H;
                 ctrl->tc_nt = nt;
             } else if ((allow & TC_ALLOW_BF16) && rmax <= 256.0 && tc_fits(TC_BF16, d, ntb)) {
                 kind = TC_BF16;
                 ctrl->tc_nt = ntb;
+            } else if ((allow & TC_ALLOW_F16) && rmax <= 2048.0 && tc_fits(TC_F16, d, nt)) {
+                kind = TC_F16;
+                ctrl->tc_nt = nt;
             } else if ((allow & TC_ALLOW_TF32) && rmax <= 2048.0 && tc_fits(TC_TF32, d, nt)) {
                 kind = TC_TF32;
                 ctrl->tc_nt = nt;
@@ -173,7 +180,7 @@ struct OperandRow {
 
 __device__ __forceinline__ uint32_t pack_pair(int kind, float lo, float hi) {
     uint16_t a, b;
-    if (kind == TC_F16) {
+    if (tc_is_f16(kind)) {
         const __half x = __float2half_rn(lo), y = __float2half_rn(hi);
         a = *reinterpret_cast<const uint16_t *>(&x);
         b = *reinterpret_cast<const uint16_t *>(&y);

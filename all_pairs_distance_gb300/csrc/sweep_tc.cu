@@ -185,6 +185,8 @@ __device__ __forceinline__ uint32_t umma_idesc(int fmt, int n, bool f32acc) {
     return ((f32acc ? 1u : 0u) << 4) | ((uint32_t)fmt << 7) | ((uint32_t)fmt << 10) |
            (((uint32_t)n >> 3) << 17) | ((128u >> 4) << 24);
 }
+// kind::f16 serves the bf16, f16 and f16-accumulator kinds (the instruction
+// descriptor carries the element and accumulator types), kind::tf32 the tf32 one.
 template <int KIND>
 __device__ __forceinline__ void umma(uint32_t tmem, uint64_t da, uint64_t db, uint32_t idesc,
                                      uint32_t accumulate) {
@@ -606,7 +608,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             // every shared-memory address is below 2^18), stage index and
             // phase -- and nothing is divided.
             const int fmt = KIND == TC_TF32 ? 2 : (KIND == TC_BF16 ? 1 : 0);
-            const bool f32acc = KIND != TC_F16;
+            const bool f32acc = KIND != TC_F16H;
             const uint32_t idesc256 = umma_idesc(fmt, 256, f32acc), idesc128 = umma_idesc(fmt, 128, f32acc);
             const uint64_t dbase = umma_desc(0, sbo);
             const uint32_t bar_bf = smem_addr(b_full), bar_af = smem_addr(a_full), bar_ae = smem_addr(a_empty);
@@ -709,12 +711,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                                       !(a.tri && (MODE == SWEEP_UNION ? tile <= rt : (RT > 1 && tile < rt)));
                     const bool diag = a.tri && tile == rt;
                     // f32 accumulator: v0, v1 = columns 0-31, 32-63 of the warp's 64;
-                    // f16 accumulator: v0 = all 64 columns, two per register
+                    // f16 accumulator (F16H): v0 = all 64 columns, two per register
                     uint32_t v0[32], v1[32];
                     if (have) {
                         const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) +
                                                (uint32_t)(b * ACC_COLS + cq * 64);
-                        if (KIND == TC_F16) {
+                        if (KIND == TC_F16H) {
                             tmem_ld32p(taddr, v0);
                         } else {
                             tmem_ld32(taddr, v0);
@@ -728,7 +730,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                     if (!have) continue;
                     const int p = r ? p1 : p0;
                     const bool rowvalid = r ? valid1 : valid0;
-                    const uint32_t neg = KIND == TC_F16 ? (or32(v0) & 0x80008000u) : (or64(v0, v1) >> 31);
+                    const uint32_t neg = KIND == TC_F16H ? (or32(v0) & 0x80008000u) : (or64(v0, v1) >> 31);
                     if (!__any_sync(FULL, rowvalid && neg)) continue;
                     int rowadd = 0, rowmin = 0x7fffffff;
                     int acc = r ? acc1 : acc0, lastq = r ? lastq1 : lastq0;
@@ -738,7 +740,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                         const int qbase = tile * BT + cb;
                         // bit c of mask = (w_c < 0) for the block's 32 columns
                         uint32_t mask;
-                        if (KIND == TC_F16) {
+                        if (KIND == TC_F16H) {
                             uint32_t o = 0;
 #pragma unroll
                             for (int c = 0; c < 16; c += 2) o |= v0[16 * blk + c] | v0[16 * blk + c + 1];
@@ -858,15 +860,10 @@ size_t tc_smem_bytes(int tile_bytes, int rows, int stage_bytes, int stages) {
 // box is then the union of the two row tiles' boxes).  A full-length unit gains
 // nothing from it and pays for the second row's bookkeeping in the epilogue.
 // The border sweep keeps one row block: its candidate tiles are sparse.
-// DBSCAN_TC_ROWS overrides: one digit (1 or 2) for every sweep, or three for
-// count, union and border.
-int tc_rows(int mode, int cull) {
-    if (const char *e = getenv("DBSCAN_TC_ROWS")) {
-        const size_t len = strlen(e);
-        const char c = len == 1 ? e[0] : (len == 3 ? e[mode] : '0');
-        if (c == '1') return 1;
-        if (c == '2') return 2;
-    }
+// The rows tuning switch (dbscan_set_options) overrides per sweep.
+int tc_rows(const Layout &L, int mode, int cull) {
+    const int r = L.rows[mode];
+    if (r == 1 || r == 2) return r;
     return cull && mode != SWEEP_BORDER ? 2 : 1;
 }
 
@@ -876,11 +873,13 @@ cudaError_t run_tc(TcArgs a, const Layout &L, cudaStream_t s) {
     // of threshold digits never exceeds the host's bound)
     const int ntb = tc_nt_bound(KIND, L.eps2);
     const int kb = tc_kbytes(KIND, L.d, ntb);
-    if (L.umma_tile_bytes == 0 || !tc_fits(KIND, L.d, ntb)) return cudaSuccess;   // never selected
+    // never selected: not allowed for this call, or the operand rows do not fit
+    if (L.umma_tile_bytes == 0 || !(L.allow & tc_allow_bit(KIND)) || !tc_fits(KIND, L.d, ntb))
+        return cudaSuccess;
     const int tile = 128 * kb;
     const int aux = MODE != SWEEP_COUNT ? BT * 4 : 0;
     const size_t budget = 224 * 1024;
-    int rows = tc_rows(MODE, a.cull);
+    int rows = tc_rows(L, MODE, a.cull);
     // two row blocks need room for four row tiles next to two stages of two
     // column tiles; wide operand rows keep one
     if (rows == 2 && 4 * (size_t)tile + 4 * (size_t)(tile + aux) > budget) rows = 1;
@@ -917,7 +916,8 @@ cudaError_t run_tc_both(const TcArgs &a, const Layout &L, cudaStream_t s) {
     cudaError_t e = run_tc<MODE, TC_TF32>(a, L, s);
     if (e != cudaSuccess) return e;
     if ((e = run_tc<MODE, TC_BF16>(a, L, s)) != cudaSuccess) return e;
-    return run_tc<MODE, TC_F16>(a, L, s);
+    if ((e = run_tc<MODE, TC_F16>(a, L, s)) != cudaSuccess) return e;
+    return run_tc<MODE, TC_F16H>(a, L, s);
 }
 
 }  // namespace

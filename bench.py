@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-culled", action="store_true")
+    ap.add_argument("--no-f16acc", action="store_true",
+                    help="skip timing the opt-in f16-accumulator variant")
     return ap.parse_args()
 
 
@@ -170,26 +172,33 @@ def kernel_code_hash(texts=None) -> str:
 
 
 def recorded_profile(workload: str, path: str, key: str):
-    """A figure of the count sweep's committed ncu summary (``key: value``
-    line), or None when the summary is missing, the kernel's code changed
-    since, or this run took another path."""
-    summary = os.path.join(ROOT, "profiles", f"count_sweep_{workload}.md")
-    if not os.path.exists(summary):
+    """A figure of the count sweep's committed ncu capture
+    (``profiles/count_sweep_<workload>.json``), or None when the record is
+    missing, the kernel's code changed since it was taken, or this run took
+    another path."""
+    rec_path = os.path.join(ROOT, "profiles", f"count_sweep_{workload}.json")
+    if not os.path.exists(rec_path):
         return None
-    text = open(summary).read()
-    m = re.search(rf"{key}:\s*([0-9.eE+]+)", text)
-    h = re.search(r"sweep_code_sha256:\s*([0-9a-f]+)", text)
-    k = re.search(r"sweep_path:\s*(\w+)", text)
-    if not m or not h or not k or k.group(1) != path:
+    with open(rec_path) as f:
+        rec = json.load(f)
+    if rec.get("sweep_path") != path or rec.get("sweep_code_sha256") != kernel_code_hash():
         return None
-    return float(m.group(1)) if h.group(1) == kernel_code_hash() else None
+    v = rec.get(key)
+    return float(v) if v is not None else None
 
 
 def recorded_traffic(workload: str, path: str):
-    """Per-launch DRAM bytes of the count sweep from the committed ncu summary,
-    or None when the summary is missing, the kernel's code changed since, or
+    """Per-launch DRAM bytes of the count sweep from the committed ncu record,
+    or None when the record is missing, the kernel's code changed since, or
     this run took another path."""
     return recorded_profile(workload, path, "traffic_bytes_per_launch")
+
+
+def executed_count_flops(n: int, kpad: int) -> float:
+    """FLOP the tensor-core count sweep executes per launch: every 128 x 128
+    tile pair of the upper triangle (diagonal included) as a K = kpad MMA."""
+    t = (n + 127) // 128
+    return t * (t + 1) / 2.0 * 128.0 * 128.0 * 2.0 * kpad
 
 
 def cpu_baseline(P, eps, min_pts, target_s=12.0):
@@ -230,6 +239,58 @@ def cpu_baseline_parallel(P, eps, min_pts, m=40000):
             "single_thread_same_sample": m * m / ds,
             "sample": f"first {m} of {len(P)} points of the workload, full oracle DBSCAN "
                       f"(count on {threads} threads, cluster expansion serial), {dt:.1f} s"}
+
+
+# arithmetic of each path: operand type and accumulator
+DTYPE_NAMES = {"fp32": "f32", "tf32": "tf32-f32acc", "bf16": "bf16-f32acc", "f16": "f16-f32acc",
+               "f16acc16": "f16-f16acc"}
+
+
+def roofline_fields(info, n, d, count_ms, peaks, sms, max_mhz) -> dict:
+    """Roofline of the count sweep against the peak of the unit that runs it:
+    the FP32 CUDA-core peak (derived) for the fp32 path, else the dense tensor
+    peak of the MMA kind (f16 and bf16 at the measured bf16 rate, tf32 at the
+    nominal tf32/bf16 ratio).  ``achieved`` counts algorithmic FLOP (2d per
+    unordered pair); ``executed_frac`` counts what the MMAs execute (the
+    operand rows padded to K), and ``encoding_ceiling`` is their ratio, the
+    most ``frac`` can reach with the tensor pipe saturated."""
+    path = info["path"]
+    achieved = count_flops(n, d) / (count_ms * 1e-3) / 1e12
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12
+    fp32_source = (f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
+                   f"{max_mhz:.0f} MHz (max SM clock" +
+                   (", MEASURED_PEAKS.json)" if peaks else ", recipe fallback)"))
+    if path == "fp32":
+        return {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp32_peak,
+                "kernel": "count sweep on CUDA cores (fp32 FFMA, upper triangle)",
+                "peak_source": fp32_source + " -- of derived FP32 FMA peak"}
+    bf16 = (peaks or {}).get("bf16_tflops", BF16_FALLBACK_TFLOPS)
+    sust = (peaks or {}).get("bf16_tflops_sustained")
+    ratio = TF32_PER_BF16 if path == "tf32" else 1.0
+    tc_peak = bf16 * ratio
+    src = ("measured bf16 burst (MEASURED_PEAKS.json) -- of measured" if peaks else
+           "recipe fallback bf16 -- of fallback")
+    if path == "tf32":
+        src += f"; x {TF32_PER_BF16:.3f} (nominal dense tf32/bf16 ratio 1.1/2.25)"
+    elif path != "bf16":
+        src += "; f16 shares the dense bf16 rate"
+    executed = executed_count_flops(n, info["kpad"]) / (count_ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+            "frac": achieved / tc_peak,
+            "executed_tflops": executed, "executed_frac": executed / tc_peak,
+            "encoding_ceiling": count_flops(n, d) / executed_count_flops(n, info["kpad"]),
+            "encoding_note": f"2d = {2 * d} algorithmic FLOP per pair against 2K = "
+                             f"{2 * info['kpad']} executed (K = {info['kpad']}: the d coordinates "
+                             "plus the norm and threshold digits, padded to the MMA's K step)",
+            "frac_vs_sustained": achieved / (sust * ratio) if sust else None,
+            "kernel": f"count sweep on tensor cores (tcgen05 {DTYPE_NAMES[path]}, "
+                      f"K={info['kpad']}, upper triangle)",
+            "peak_source": src,
+            "fp32_equivalent": {"achieved": achieved, "peak": fp32_peak,
+                                "frac": achieved / fp32_peak,
+                                "note": "the same algorithmic FLOP against the derived FP32 "
+                                        "CUDA-core peak (" + fp32_source + ")"}}
 
 
 # ---------------------------------------------------------------------------
@@ -341,57 +402,17 @@ def run_gb300(args, dist: Dist):
     props = torch.cuda.get_device_properties(dev)
     sms = getattr(props, "multi_processor_count", SM_COUNT_FALLBACK)
     max_mhz = (peaks or {}).get("sm_max_mhz", SM_MAX_MHZ_FALLBACK)
-    fp32_peak = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12
-    achieved = count_flops(n, d) / (count_ms * 1e-3) / 1e12
-    traffic = recorded_traffic(w.name, info["path"])
-    tp_active = recorded_profile(w.name, info["path"], "tensor_pipe_active_pct")
-    # d <= 16: the distance pass is d FMAs per pair, so its roofline is the FP32
-    # CUDA-core peak whichever unit evaluates it; d > 16: the bf16 tensor peak.
-    tc_peak = None
-    if info["path"] != "fp32":
-        bf16 = (peaks or {}).get("bf16_tflops", BF16_FALLBACK_TFLOPS)
-        # f16 and bf16 MMAs share the dense rate; tf32 runs at the nominal ratio
-        tc_peak = bf16 if info["path"] in ("bf16", "f16") else bf16 * TF32_PER_BF16
-        tc_source = (("measured bf16 burst (MEASURED_PEAKS.json)" if peaks else "recipe fallback bf16") +
-                     ("" if info["path"] in ("bf16", "f16") else
-                      f" x {TF32_PER_BF16:.3f} (nominal tf32/bf16 ratio 1.1/2.25)"))
-    kname = ("count sweep on CUDA cores (fp32 FFMA, upper triangle)" if info["path"] == "fp32" else
-             f"count sweep on tensor cores (tcgen05 {info['path']}, K={info['kpad']}, upper triangle)")
-    fp32_source = (f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
-                   f"{max_mhz:.0f} MHz (max SM clock" +
-                   (", MEASURED_PEAKS.json)" if peaks else ", recipe fallback)"))
-    if d <= 16 or info["path"] == "fp32":
-        roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
-                    "frac": achieved / fp32_peak, "traffic": traffic, "kernel": kname,
-                    "peak_source": fp32_source + " -- of derived FP32 FMA peak"}
-        if tc_peak is not None:
-            roofline["tensor_pipe"] = {"achieved": achieved, "peak": tc_peak,
-                                       "frac": achieved / tc_peak, "peak_source": tc_source,
-                                       "note": "the same algorithmic FLOP against the tensor peak of "
-                                               "the MMA kind the sweep runs on"}
-    else:
-        sust = (peaks or {}).get("bf16_tflops_sustained")
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
-                    "frac": achieved / tc_peak, "traffic": traffic, "kernel": kname,
-                    "peak_source": tc_source + " -- of measured",
-                    # the count sweep is timed inside a long multi-kernel step; the
-                    # measured sustained peak (a seconds-long GEMM loop at the power
-                    # cap) is the other denominator for that case
-                    "frac_vs_sustained": (achieved / (sust * (1.0 if info["path"] in ("bf16", "f16")
-                                                              else TF32_PER_BF16))
-                                          if sust else None),
-                    "fp32_equivalent": {"achieved": achieved, "peak": fp32_peak,
-                                        "frac": achieved / fp32_peak,
-                                        "note": "same algorithmic FLOP (2d per unordered pair) "
-                                                "against the derived FP32 CUDA-core peak"}}
+    roofline = roofline_fields(info, n, d, count_ms, peaks, sms, max_mhz)
+    roofline["traffic"] = recorded_traffic(w.name, info["path"])
     # the executed view: the tensor pipe's active share in the committed ncu
     # capture of this kernel and path (null once the kernel's code changed)
+    tp_active = recorded_profile(w.name, info["path"], "tensor_pipe_active_pct")
     roofline["ncu_tensor_pipe_active"] = tp_active / 100.0 if tp_active is not None else None
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {"fp32": "f32", "tf32": "tf32", "bf16": "bf16", "f16": "f16"}[info["path"]],
+            "dtype": DTYPE_NAMES[info["path"]],
             "data": "synthetic",
             "config": {"workload": w.name if args.n is None else f"{w.name} scaled to n={n}",
                        "n": n, "d": d, "eps": w.eps, "min_pts": w.min_pts,
@@ -445,6 +466,50 @@ def run_gb300(args, dist: Dist):
                           "note": "tile pairs whose bounding boxes are eps apart are skipped "
                                   "(identical labels); not an all-pairs evaluation, so no "
                                   "pair-evals/s figure"}
+
+    # The opt-in f16-accumulator variant of the f16 path (DBSCAN_PATH_F16_ACC16),
+    # reported in a field of its own: it accumulates in f16, narrower than the
+    # float32 the headline uses.
+    if info["path"] == "f16" and not args.no_f16acc:
+        with binding.options(paths=binding.PATHS_DEFAULT | binding.PATH_BITS["f16acc16"]):
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    flush.zero_()
+                    step()
+            torch.cuda.synchronize()
+            hs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+            he = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+            dist.barrier()
+            with torch.cuda.stream(stream):
+                for k in range(args.steps):
+                    flush.zero_()
+                    hs[k].record(stream)
+                    step()
+                    he[k].record(stream)
+            torch.cuda.synchronize()
+            dist.barrier()
+            binding.dbscan_profile_begin()
+            with torch.cuda.stream(stream):
+                for k in range(args.steps):
+                    flush.zero_()
+                    step()
+            torch.cuda.synchronize()
+            h_stage_ms, h_calls, _ = binding.dbscan_profile_end()
+            h_info = binding.dbscan_workspace_info(ws)
+        st = binding.dbscan_workspace_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {binding.dbscan_strerror(st)}")
+        h_ms = dist.max(sum(a.elapsed_time(b) for a, b in zip(hs, he)) / args.steps)
+        h_count = h_stage_ms["count"] / max(h_calls, 1)
+        line["f16_accumulator_optin"] = {
+            "path": h_info["path"], "dtype": DTYPE_NAMES[h_info["path"]], "ms_per_step": h_ms,
+            "value": dist.world * float(n) * n / (h_ms * 1e-3), "unit": UNIT,
+            "count_ms": h_count,
+            "count_frac_of_tensor_peak": count_flops(n, d) / (h_count * 1e-3) / 1e12 /
+                                         roofline["peak"],
+            "note": "opt-in DBSCAN_PATH_F16_ACC16: f16 operands and an f16 accumulator (one K = 16 "
+                    "MMA per tile pair); identical results here, but narrower than the float32 "
+                    "accumulation of the headline, whose exactness NVIDIA does not document"}
 
     if not args.no_e2e:
         ph = torch.from_numpy(P).to(dtype).pin_memory()

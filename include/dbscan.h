@@ -31,12 +31,15 @@
  * ">= MinPts" or "> MinPts", and which cluster a border point shared by two
  * clusters joins; the answers above are the readings this library takes.
  *
+ * Arithmetic: float32 throughout -- fp32 FMAs on CUDA cores, or tensor-core
+ * MMAs (tf32, bf16 or f16 operands) with a float32 accumulator.
  * Exactness: when every coordinate is an integer and sum_k (max_k - min_k)^2
- * over the data's per-dimension ranges is below 2^24, every sum the kernels
- * form is an integer below 2^24 (the f16 tensor-core path rounds its final
- * sum once, which keeps its sign, the only thing read) and the results are
- * exact (identical to a double-precision evaluation).  Otherwise pairs within
- * float32 rounding of the eps boundary may be classified either way.
+ * over the data's per-dimension ranges is below 2^24, every product and
+ * partial sum the kernels form is an integer below 2^24, which float32 holds
+ * exactly, and the results are exact (identical to a double-precision
+ * evaluation).  Otherwise pairs within float32 rounding of the eps boundary
+ * may be classified either way.  (The opt-in DBSCAN_PATH_F16_ACC16 path is
+ * the one exception to float32 accumulation; see dbscan_set_options.)
  *
  * Memory: every pointer argument is a DEVICE pointer unless the entry point's
  * name ends in _host.  The caller owns all buffers; the library never frees
@@ -78,6 +81,48 @@ typedef enum {
 #define DBSCAN_MAX_D 256
 
 /*
+ * Process-wide tuning switches.  They change how the kernels run, never what
+ * they compute; every call takes a snapshot when it starts.
+ *   paths   tensor-core paths the device may choose among (DBSCAN_PATH_* bits);
+ *           the device takes the first one the data allow, in the order
+ *           F16_ACC16 (only when set), BF16, F16, TF32, else fp32 FMAs on CUDA
+ *           cores (always allowed; paths = 0 forces them).  A path is taken
+ *           only when its operands hold the data exactly (integer coordinates,
+ *           ranges within the element type, sums below 2^24).
+ *   rows    row blocks per work unit of the tensor-core count, union and
+ *           border sweeps: 0 automatic, 1 or 2
+ *   graphs  1: replay repeated calls from CUDA graphs (see dbscan_fit_ex);
+ *           0: launch every kernel directly
+ * DBSCAN_PATH_F16_ACC16 is an opt-in: f16 operands with an f16 accumulator
+ * (one K = 16 MMA per tile pair, d <= 10).  Its integer sum is rounded to f16
+ * once, which keeps the sign the sweep reads -- provided the tensor core forms
+ * the K = 16 sum exactly before that rounding.  NVIDIA does not document the
+ * internal width of that sum; the library's tests observe it on GB300 only.
+ * Defaults: paths = DBSCAN_PATHS_DEFAULT, rows automatic, graphs on; the
+ * environment variables DBSCAN_FORCE_PATH (fp32, tf32, bf16, f16, f16acc16),
+ * DBSCAN_TC_ROWS (one digit, or three for count, union, border) and
+ * DBSCAN_GRAPHS (0 = off) override the defaults, read once per process at
+ * the first call into the library.
+ */
+#define DBSCAN_PATH_TF32 1u
+#define DBSCAN_PATH_BF16 2u
+#define DBSCAN_PATH_F16 4u        /* f16 operands, f32 accumulator */
+#define DBSCAN_PATH_F16_ACC16 8u  /* f16 operands, f16 accumulator (opt-in) */
+#define DBSCAN_PATHS_DEFAULT (DBSCAN_PATH_TF32 | DBSCAN_PATH_BF16 | DBSCAN_PATH_F16)
+typedef struct {
+    uint32_t paths;
+    int32_t rows[3];
+    int32_t graphs;
+} dbscan_options;
+
+/* Replace the switches (NULL restores the defaults above, environment
+ * included).  DBSCAN_ERR_INVALID_ARG for unknown path bits or a rows entry
+ * outside 0..2, or graphs outside 0..1. */
+int dbscan_set_options(const dbscan_options *opt);
+/* The switches in force (host pointer). */
+int dbscan_get_options(dbscan_options *opt);
+
+/*
  * Full DBSCAN on float32 device points; synchronous on the legacy default
  * stream.  Allocates and frees its own workspace (stream-ordered).
  *   points      [n, d] float32, device, read only
@@ -106,9 +151,11 @@ int dbscan_fit(const float *points, int64_t n, int32_t d, float eps,
  * sizes, eps, min_pts, device) is captured into a CUDA graph, and later calls
  * with the same arguments replay it; the graph reads whatever the buffers
  * hold at replay, so results are those of a direct call.  The same holds for
- * dbscan_fit_culled, dbscan_neighbor_counts and dbscan_fit_noalloc.  Not
- * while the stream is being captured by the caller or stage profiling is on;
- * the environment variable DBSCAN_GRAPHS=0 turns it off.
+ * dbscan_fit_culled and dbscan_neighbor_counts.  Not while the stream is
+ * being captured by the caller or stage profiling is on, nor with the
+ * graphs switch off (dbscan_set_options).  At most 16 graphs are kept; the
+ * least recently used one is destroyed to make room (an instance still
+ * running is freed when it completes).
  * Cites: §II, §IV-A, §IV-B, §IV-B1, §IV-B2, §IV-C.
  */
 int dbscan_fit_ex(const void *points, int32_t dtype, int64_t n, int32_t d,
@@ -203,7 +250,9 @@ int dbscan_neighbor_counts(const void *points, int32_t dtype, int64_t n,
  *     must start at zero, so calls that overlap on the GPU (different streams,
  *     different host threads) race and must be serialised by the caller;
  *   - device-side errors are not reported (there is no workspace handle to
- *     read them from); host-side argument errors are returned as usual.
+ *     read them from); host-side argument errors are returned as usual;
+ *   - it never captures or instantiates a CUDA graph (graph instantiation
+ *     takes device resources): its kernels are always launched directly.
  */
 #define DBSCAN_NOALLOC_SCRATCH_BYTES (64u << 20)
 int dbscan_fit_noalloc(const void *points, int32_t dtype, int64_t n, int32_t d,
@@ -222,7 +271,9 @@ int dbscan_workspace_status(const void *workspace, void *stream);
  * Facts about the last call that used `workspace` (synchronises `stream`
  * first).  Fills up to n of, in this order:
  *   0  arithmetic path of the sweeps: 0 CUDA-core fp32, 1 tf32 tensor cores,
- *      2 bf16 tensor cores, 3 f16 tensor cores (f16 accumulator)
+ *      2 bf16 tensor cores, 3 f16 tensor cores (f32 accumulator), 4 f16
+ *      tensor cores with the opt-in f16 accumulator (all others accumulate
+ *      in float32)
  *   1  number of core points
  *   2  number of border candidates (non-core points with a neighbour
  *      besides themselves)

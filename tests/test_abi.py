@@ -110,3 +110,41 @@ def test_compact_labels_host_side_errors(lib):
     assert k.value == -7                                             # untouched on error
     assert f(None, 0, None, ctypes.byref(k), None) == 0               # n == 0: k = 0
     assert k.value == 0
+
+
+def test_options_roundtrip_and_validation(lib, monkeypatch):
+    # the tuning switches are process-wide host state: no GPU involved
+    from all_pairs_distance_gb300 import binding
+    binding.dbscan_set_options(reset=True)
+    try:
+        o = binding.dbscan_get_options()
+        assert o == {"paths": binding.PATHS_DEFAULT, "rows": (0, 0, 0), "graphs": 1} or \
+            os.environ.get("DBSCAN_FORCE_PATH") or os.environ.get("DBSCAN_TC_ROWS") or \
+            os.environ.get("DBSCAN_GRAPHS")
+        binding.dbscan_set_options(paths=["f16"], rows=(1, 2, 1), graphs=0)
+        assert binding.dbscan_get_options() == {"paths": 4, "rows": (1, 2, 1), "graphs": 0}
+        with binding.options(paths=["fp32"], rows=2):
+            assert binding.dbscan_get_options() == {"paths": 0, "rows": (2, 2, 2), "graphs": 0}
+        assert binding.dbscan_get_options() == {"paths": 4, "rows": (1, 2, 1), "graphs": 0}
+        # out-of-range switches are refused and leave the state alone
+        bad = binding.Options()
+        bad.paths = 16
+        assert lib.dbscan_set_options(ctypes.byref(bad)) == -1
+        bad.paths, bad.rows[1] = 1, 3
+        assert lib.dbscan_set_options(ctypes.byref(bad)) == -1
+        bad.rows[1], bad.graphs = 0, 2
+        assert lib.dbscan_set_options(ctypes.byref(bad)) == -1
+        assert lib.dbscan_get_options(None) == -1
+        assert binding.dbscan_get_options() == {"paths": 4, "rows": (1, 2, 1), "graphs": 0}
+        # the environment is read once per process and again only on a reset
+        monkeypatch.setenv("DBSCAN_FORCE_PATH", "f16acc16")
+        monkeypatch.setenv("DBSCAN_TC_ROWS", "212")
+        monkeypatch.setenv("DBSCAN_GRAPHS", "0")
+        assert binding.dbscan_get_options()["paths"] == 4
+        binding.dbscan_set_options(reset=True)
+        assert binding.dbscan_get_options() == {"paths": 8, "rows": (2, 1, 2), "graphs": 0}
+    finally:
+        monkeypatch.delenv("DBSCAN_FORCE_PATH", raising=False)
+        monkeypatch.delenv("DBSCAN_TC_ROWS", raising=False)
+        monkeypatch.delenv("DBSCAN_GRAPHS", raising=False)
+        binding.dbscan_set_options(reset=True)

@@ -12,8 +12,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("case", ["d3", "d64_bf16", "d2_culled"])
-def test_replay_follows_the_buffers(case, monkeypatch):
-    monkeypatch.delenv("DBSCAN_GRAPHS", raising=False)
+def test_replay_follows_the_buffers(case):
     if case == "d3":
         sets = [synth.scaled("blobs_1m_d3", 9_001, seed=s) for s in (71, 72)]
         eps, mp, dt = 10.0, 8, torch.float32
@@ -29,7 +28,7 @@ def test_replay_follows_the_buffers(case, monkeypatch):
     ws = binding.workspace_for(x)
     labels = torch.empty(len(sets[0]), dtype=torch.int32, device="cuda")
     core = torch.empty(len(sets[0]), dtype=torch.uint8, device="cuda")
-    with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream), binding.options(graphs=1):
         # the same arguments four times (captured once, then replayed), the
         # input overwritten in place between rounds
         for rnd in range(4):
@@ -44,15 +43,14 @@ def test_replay_follows_the_buffers(case, monkeypatch):
             assert_same(labels.cpu().numpy(), label_ref, f"{case} round {rnd} labels")
 
 
-def test_replay_and_direct_launches_agree(monkeypatch):
+def test_replay_and_direct_launches_agree():
     P = synth.scaled("blobs_1m_d3", 7_001, seed=77)
     x = torch.from_numpy(P).to("cuda")
     ws = binding.workspace_for(x)
     stream = torch.cuda.Stream()
     out = {}
     for mode in ("1", "0"):
-        monkeypatch.setenv("DBSCAN_GRAPHS", mode)
-        with torch.cuda.stream(stream):
+        with torch.cuda.stream(stream), binding.options(graphs=int(mode)):
             for _ in range(2):
                 lab, core = binding.dbscan_fit_ex(x, 10.0, 8, workspace=ws, stream=stream)
                 cnt = binding.dbscan_neighbor_counts(x, 10.0, workspace=ws, stream=stream)
@@ -60,3 +58,25 @@ def test_replay_and_direct_launches_agree(monkeypatch):
         out[mode] = (lab.cpu().numpy(), core.cpu().numpy(), cnt.cpu().numpy())
     for a, b, w in zip(out["1"], out["0"], ("labels", "core", "counts")):
         assert_same(a, b, f"graph vs direct {w}")
+
+
+def test_graph_cache_evicts_beyond_its_capacity():
+    # more distinct argument sets than the cache holds (16): the least recently
+    # used graphs are destroyed to make room and every call stays correct
+    P = synth.scaled("blobs_100k_d2", 3_001, seed=78)
+    _, core_ref, label_ref = oracle.dbscan(P, 20.0, 10)
+    x = torch.from_numpy(P).to("cuda")
+    ws = binding.workspace_for(x)
+    stream = torch.cuda.Stream()
+    outs = [(torch.empty(len(P), dtype=torch.int32, device="cuda"),
+             torch.empty(len(P), dtype=torch.uint8, device="cuda")) for _ in range(20)]
+    with torch.cuda.stream(stream), binding.options(graphs=1):
+        for rnd in range(2):
+            for lab, core in outs:   # 20 keys (output pointers differ)
+                lab.fill_(-7)
+                binding.dbscan_fit_ex(x, 20.0, 10, labels=lab, is_core=core, workspace=ws,
+                                      stream=stream)
+            stream.synchronize()
+            for lab, core in outs:
+                assert_same(lab.cpu().numpy(), label_ref, f"round {rnd} labels")
+                assert_same(core.cpu().numpy(), core_ref, f"round {rnd} core flags")

@@ -109,7 +109,7 @@ def test_min_pts_one_every_point_is_core():
 
 
 @pytest.mark.parametrize("order", ["sorted", "reversed", "interleaved"])
-def test_input_order_does_not_matter(order, monkeypatch):
+def test_input_order_does_not_matter(order):
     # the kernels sort the points into a locality order of their own; results
     # are defined on input indices, so any input order must match the oracle
     # run on that same order (already sorted input included)
@@ -124,11 +124,8 @@ def test_input_order_does_not_matter(order, monkeypatch):
     P = np.ascontiguousarray(P)
     ref = oracle.dbscan(P, 10.0, 8)
     for path in ("fp32", "default"):
-        if path == "fp32":
-            monkeypatch.setenv("DBSCAN_FORCE_PATH", "fp32")
-        else:
-            monkeypatch.delenv("DBSCAN_FORCE_PATH", raising=False)
-        got = gpu_run(P, 10.0, 8)
+        with binding.options(paths=(["fp32"] if path == "fp32" else binding.PATHS_DEFAULT)):
+            got = gpu_run(P, 10.0, 8)
         for g, e, w in zip(got, ref, ("cnt", "core", "label")):
             assert_same(g, e, f"{order} path={path} {w}")
 
@@ -242,46 +239,52 @@ def test_device_side_errors_and_bad_pointers():
     assert np.all(cnt == 5)
 
 
+ALL_TC = {"tf32", "bf16", "f16", "f16acc16"}
 PATH_CASES = {
     # name: (points, eps, min_pts, dtype, tensor-core paths the data qualifies for)
     "c4_like_12k_d3": (lambda: synth.scaled("blobs_1m_d3", 12_007, seed=31), 10.0, 8, torch.float32,
-                       {"tf32", "f16"}),
+                       {"tf32", "f16", "f16acc16"}),
     "c2_like_9k_d2": (lambda: synth.scaled("blobs_100k_d2", 9_001, seed=32), 20.0, 10, torch.float32,
-                      {"tf32", "f16"}),
+                      {"tf32", "f16", "f16acc16"}),
     "c3_like_3k_d16": (lambda: synth.scaled("blobs_200k_d16", 3_001, seed=33), 120.0, 20,
-                       torch.float32, {"tf32"}),
-    "c5_like_3k_d64": (lambda: synth.scaled("blobs_500k_d64", 2_999, seed=34), 100.0, 16,
-                       torch.bfloat16, {"bf16", "tf32"}),
-    "small_box_d3": (lambda: synth.uniform_ints(4_000, 3, 200, 35), 9.0, 6, torch.float32,
-                     {"tf32", "bf16", "f16"}),
-    "corners_d3": (lambda: (np.random.default_rng(36).integers(0, 2, size=(700, 3)) * 2047)
-                   .astype(np.float32), 2047.0, 5, torch.float32, {"tf32", "f16"}),
-    # d = 10 with two threshold digits fills the f16 path's single K = 16 MMA
-    "d10_two_digits": (lambda: synth.blob_set(3_000, 10, 511, 12, 20.0, 300, 37), 60.0, 4,
                        torch.float32, {"tf32", "f16"}),
-    # d = 11 no longer fits one K = 16 MMA: f16 is not eligible
+    "c5_like_3k_d64": (lambda: synth.scaled("blobs_500k_d64", 2_999, seed=34), 100.0, 16,
+                       torch.bfloat16, {"bf16", "tf32", "f16"}),
+    "small_box_d3": (lambda: synth.uniform_ints(4_000, 3, 200, 35), 9.0, 6, torch.float32, ALL_TC),
+    "corners_d3": (lambda: (np.random.default_rng(36).integers(0, 2, size=(700, 3)) * 2047)
+                   .astype(np.float32), 2047.0, 5, torch.float32, {"tf32", "f16", "f16acc16"}),
+    # d = 10 with two threshold digits fills the f16 accumulator's single K = 16 MMA
+    "d10_two_digits": (lambda: synth.blob_set(3_000, 10, 511, 12, 20.0, 300, 37), 60.0, 4,
+                       torch.float32, {"tf32", "f16", "f16acc16"}),
+    # d = 11 no longer fits one K = 16 MMA: the f16 accumulator is not eligible,
+    # f16 operands with an f32 accumulator take two K steps
     "d11_blobs": (lambda: synth.blob_set(2_500, 11, 511, 10, 20.0, 250, 38), 60.0, 5,
-                  torch.float32, {"tf32"}),
-    # the widest rows: 144 bf16 elements at d = 128, 72 tf32 elements at d = 64
-    # (a range of 400 is too wide for bf16 and narrow enough for exact tf32)
+                  torch.float32, {"tf32", "f16"}),
+    # the widest rows: 144 bf16/f16 elements at d = 128, 72 tf32 elements at d = 64
+    # (a range of 400 is too wide for bf16 and narrow enough for exact tf32 and f16)
     "d128_bf16": (lambda: synth.blob_set(2_500, 128, 255, 8, 6.0, 250, 39), 110.0, 5,
-                  torch.bfloat16, {"bf16"}),
+                  torch.bfloat16, {"bf16", "f16"}),
     "d64_tf32_wide": (lambda: synth.blob_set(2_000, 64, 400, 8, 12.0, 200, 40), 150.0, 5,
-                      torch.float32, {"tf32"}),
+                      torch.float32, {"tf32", "f16"}),
+    # a threshold constant of three base-2048 digits (eps^2 >= 2048^2): f16
+    # operands hold at most two, tf32 takes three
+    "d3_three_digits": (lambda: synth.uniform_ints(1_500, 3, 2047, 41), 2100.0, 40, torch.float32,
+                        {"tf32"}),
 }
 
 
-@pytest.mark.parametrize("path", ["fp32", "tf32", "bf16", "f16"])
+@pytest.mark.parametrize("path", ["fp32", "tf32", "bf16", "f16", "f16acc16"])
 @pytest.mark.parametrize("name", sorted(PATH_CASES))
-def test_parity_every_path(name, path, monkeypatch):
-    # the library picks a path per call from the data; forcing one narrows the
-    # choice (a path the data cannot use exactly falls back to CUDA cores)
-    monkeypatch.setenv("DBSCAN_FORCE_PATH", path)
+def test_parity_every_path(name, path):
+    # the library picks a path per call from the data; allowing one path only
+    # narrows the choice (a path the data cannot use exactly falls back to CUDA
+    # cores)
     make, eps, min_pts, dtype, eligible = PATH_CASES[name]
     P = make()
     ref = oracle.dbscan(P, eps, min_pts)
     info = {}
-    got = gpu_run(P, eps, min_pts, dtype, info=info)
+    with binding.options(paths=[path]):
+        got = gpu_run(P, eps, min_pts, dtype, info=info)
     assert info["path"] == (path if path in eligible else "fp32")
     assert info["exact"]
     assert info["n_core"] == int(ref[1].sum())
@@ -290,20 +293,26 @@ def test_parity_every_path(name, path, monkeypatch):
 
 
 def test_default_path_choice():
-    # without forcing, integer data whose operand rows fit one K = 16 MMA go to
-    # f16, other data in a 256-wide box to bf16, in a 2048-wide box to tf32,
-    # and wider or fractional data stays on CUDA cores
-    for P, expect in ((synth.uniform_ints(3000, 3, 2047, 1), "f16"),
-                      (synth.uniform_ints(3000, 3, 255, 2), "f16"),
-                      (synth.uniform_ints(3000, 16, 255, 5), "bf16"),
-                      (synth.uniform_ints(3000, 12, 511, 6), "tf32"),
-                      (synth.uniform_ints(3000, 128, 255, 7), "bf16"),
-                      (synth.uniform_ints(3000, 64, 400, 8), "tf32"),
-                      (synth.uniform_ints(3000, 2, 3000, 3), "fp32"),
-                      (synth.uniform_ints(3000, 2, 100, 4) + np.float32(0.5), "fp32")):
+    # by default integer data in a 256-wide box go to bf16, in a 2048-wide box
+    # to f16 (both f32 accumulation), threshold constants too large for f16
+    # operands to tf32, and wider or fractional data stay on CUDA cores; the
+    # f16 accumulator is never chosen unless allowed
+    for P, eps, expect in ((synth.uniform_ints(3000, 3, 2047, 1), 4.0, "f16"),
+                           (synth.uniform_ints(3000, 3, 255, 2), 4.0, "bf16"),
+                           (synth.uniform_ints(3000, 16, 255, 5), 4.0, "bf16"),
+                           (synth.uniform_ints(3000, 12, 511, 6), 4.0, "f16"),
+                           (synth.uniform_ints(3000, 128, 255, 7), 4.0, "bf16"),
+                           (synth.uniform_ints(3000, 64, 400, 8), 4.0, "f16"),
+                           (synth.uniform_ints(3000, 3, 2047, 9), 2100.0, "tf32"),
+                           (synth.uniform_ints(3000, 2, 3000, 3), 4.0, "fp32"),
+                           (synth.uniform_ints(3000, 2, 100, 4) + np.float32(0.5), 4.0, "fp32")):
         info = {}
-        gpu_run(P, 4.0, 3, info=info, counts=False)
+        gpu_run(P, eps, 3, info=info, counts=False)
         assert info["path"] == expect, (expect, info)
+    with binding.options(paths=binding.PATHS_DEFAULT | binding.PATH_BITS["f16acc16"]):
+        info = {}
+        gpu_run(synth.uniform_ints(3000, 3, 2047, 1), 4.0, 3, info=info, counts=False)
+        assert info["path"] == "f16acc16", info
 
 
 def gpu_run_culled(P, eps, min_pts, dtype=torch.float32):
@@ -331,24 +340,21 @@ CULL_CASES = {
 }
 
 
-@pytest.mark.parametrize("path", ["default", "tf32", "bf16", "fp32"])
+@pytest.mark.parametrize("path", ["default", "tf32", "bf16", "f16", "fp32"])
 @pytest.mark.parametrize("name", sorted(CULL_CASES))
-def test_culled_matches_oracle(name, path, monkeypatch):
-    if path == "default":
-        monkeypatch.delenv("DBSCAN_FORCE_PATH", raising=False)
-    else:
-        monkeypatch.setenv("DBSCAN_FORCE_PATH", path)
+def test_culled_matches_oracle(name, path):
     make, eps, min_pts, dtype = CULL_CASES[name]
     P = make()
     _, core_ref, label_ref = oracle.dbscan(P, eps, min_pts)
-    core, label = gpu_run_culled(P, eps, min_pts, dtype)
+    with binding.options(paths=binding.PATHS_DEFAULT if path == "default" else [path]):
+        core, label = gpu_run_culled(P, eps, min_pts, dtype)
     assert_same(core, core_ref, f"{name} [{path}] culled core flags")
     assert_same(label, label_ref, f"{name} [{path}] culled labels")
 
 
 ROW_CASES = {
-    # the tensor-core sweeps take one or two row blocks per unit; DBSCAN_TC_ROWS
-    # forces either for every sweep (one digit) or per sweep (count, union, border)
+    # the tensor-core sweeps take one or two row blocks per unit; the rows switch
+    # forces either for every sweep or per sweep (count, union, border)
     "c4_like_9k_d3": (lambda: synth.scaled("blobs_1m_d3", 9_001, seed=51), 10.0, 8, torch.float32),
     "c5_like_2k_d64": (lambda: synth.scaled("blobs_500k_d64", 2_177, seed=52), 100.0, 16,
                        torch.bfloat16),
@@ -363,17 +369,18 @@ ROW_CASES = {
 
 @pytest.mark.parametrize("rows", ["1", "2", "212", "121"])
 @pytest.mark.parametrize("name", sorted(ROW_CASES))
-def test_row_units_match_oracle(name, rows, monkeypatch):
-    monkeypatch.setenv("DBSCAN_TC_ROWS", rows)
+def test_row_units_match_oracle(name, rows):
     make, eps, min_pts, dtype = ROW_CASES[name]
     P = make()
     assert len(P) == {"c4_like_9k_d3": 9_001, "c5_like_2k_d64": 2_177, "d16_blobs": 3_203,
                       "odd_tiles_d2": 1_074, "fractional_d3": 4_001}[name]
     cnt_ref, core_ref, label_ref = oracle.dbscan(P, eps, min_pts)
-    cnt, core, label = gpu_run(P, eps, min_pts, dtype)
+    r = [int(c) for c in rows] * (3 if len(rows) == 1 else 1)
+    with binding.options(rows=r):
+        cnt, core, label = gpu_run(P, eps, min_pts, dtype)
+        core_c, label_c = gpu_run_culled(P, eps, min_pts, dtype)
     assert_same(cnt, cnt_ref, f"{name} [rows {rows}] counts")
     assert_same(core, core_ref, f"{name} [rows {rows}] core flags")
     assert_same(label, label_ref, f"{name} [rows {rows}] labels")
-    core_c, label_c = gpu_run_culled(P, eps, min_pts, dtype)
     assert_same(core_c, core_ref, f"{name} [rows {rows}] culled core flags")
     assert_same(label_c, label_ref, f"{name} [rows {rows}] culled labels")
