@@ -24,12 +24,15 @@
 //               is the critical path of the sweep and keeps everything it
 //               needs in registers;
 //   warps 0-15  epilogue: every warp reads every tile pair, 32 rows x 64
-//               columns (two tcgen05.ld, or one packed load of an f16
-//               accumulator), and frees the accumulator before it tests
-//               anything -- TMEM read bandwidth grows with the number of warps
-//               loading.  A warp ORs the sign bits of its 64 columns and, only
-//               where a 32 x 32 block holds a neighbour, builds exact per-row
-//               bit masks.  Counting credits the row with a popcount and the
+//               columns (two reducing tcgen05.ld.red.min, or one packed load
+//               of an f16 accumulator), and frees the accumulator before it
+//               tests anything -- TMEM read bandwidth grows with the number of
+//               warps loading.  The reducing loads return each row's minimum
+//               with the values, so the common case (no neighbour among the
+//               64 columns) costs one sign test instead of an OR over 64
+//               registers on the ALU pipe, which the MMA thread's SMSP shares;
+//               only where a 32 x 32 block holds a neighbour does a warp build
+//               exact per-row bit masks.  Counting credits the row with a popcount and the
 //               columns by atomics (few neighbours) or a warp bit transpose
 //               (many); union and border act on each neighbour pair as on CUDA
 //               cores.
@@ -211,17 +214,20 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+// 32 lanes x 32 columns of an f32 accumulator (one register per column), and
+// per lane the minimum of the 32 values as an f32: the reduction runs in the
+// TMEM load path, not on the ALU pipe.
+__device__ __forceinline__ void tmem_ld32min(uint32_t taddr, uint32_t (&r)[32], uint32_t &mn) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.min.f32 "
         "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
           "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
+          "=r"(r[31]), "=r"(mn)
         : "r"(taddr));
 }
 // 32 lanes x 64 columns of an f16 accumulator, two columns per register:
@@ -274,22 +280,6 @@ __device__ __forceinline__ uint32_t or32(const uint32_t (&a)[32]) {
     for (int g = 0; g < 10; ++g) t[g] = a[3 * g] | a[3 * g + 1] | a[3 * g + 2];
     t[10] = a[30] | a[31];
     return (t[0] | t[1] | t[2]) | (t[3] | t[4] | t[5]) | (t[6] | t[7] | t[8]) | (t[9] | t[10]);
-}
-
-// OR of 64 words as a shallow tree of three-input ORs.
-__device__ __forceinline__ uint32_t or64(const uint32_t (&a)[32], const uint32_t (&b)[32]) {
-    uint32_t t[22];
-#pragma unroll
-    for (int g = 0; g < 10; ++g) t[g] = a[3 * g] | a[3 * g + 1] | a[3 * g + 2];
-    t[10] = a[30] | a[31] | b[0];
-#pragma unroll
-    for (int g = 0; g < 10; ++g) t[11 + g] = b[3 * g + 1] | b[3 * g + 2] | b[3 * g + 3];
-    t[21] = b[31];
-    uint32_t u[8];
-#pragma unroll
-    for (int g = 0; g < 7; ++g) u[g] = t[3 * g] | t[3 * g + 1] | t[3 * g + 2];
-    u[7] = t[21];
-    return (u[0] | u[1] | u[2]) | (u[3] | u[4] | u[5]) | (u[6] | u[7]);
 }
 
 // 32 x 32 bit transpose across a warp: lane i bit j -> lane j bit i.
@@ -710,17 +700,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                     const bool have = ti < m.ntiles &&
                                       !(a.tri && (MODE == SWEEP_UNION ? tile <= rt : (RT > 1 && tile < rt)));
                     const bool diag = a.tri && tile == rt;
-                    // f32 accumulator: v0, v1 = columns 0-31, 32-63 of the warp's 64;
+                    // f32 accumulator: v0, v1 = columns 0-31, 32-63 of the warp's 64,
+                    // and mn0, mn1 the minimum of each half (from the loads);
                     // f16 accumulator (F16H): v0 = all 64 columns, two per register
-                    uint32_t v0[32], v1[32];
+                    uint32_t v0[32], v1[32], mn0 = 0, mn1 = 0;
                     if (have) {
                         const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) +
                                                (uint32_t)(b * ACC_COLS + cq * 64);
                         if (KIND == TC_F16H) {
                             tmem_ld32p(taddr, v0);
                         } else {
-                            tmem_ld32(taddr, v0);
-                            tmem_ld32(taddr + 32, v1);
+                            tmem_ld32min(taddr, v0, mn0);
+                            tmem_ld32min(taddr + 32, v1, mn1);
                         }
                         tmem_ld_wait();
                     }
@@ -730,7 +721,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                     if (!have) continue;
                     const int p = r ? p1 : p0;
                     const bool rowvalid = r ? valid1 : valid0;
-                    const uint32_t neg = KIND == TC_F16H ? (or32(v0) & 0x80008000u) : (or64(v0, v1) >> 31);
+                    // a negative minimum has its sign bit set (an exact zero is +0)
+                    const uint32_t neg = KIND == TC_F16H ? (or32(v0) & 0x80008000u) : ((mn0 | mn1) >> 31);
                     if (!__any_sync(FULL, rowvalid && neg)) continue;
                     int rowadd = 0, rowmin = 0x7fffffff;
                     int acc = r ? acc1 : acc0, lastq = r ? lastq1 : lastq0;
