@@ -37,7 +37,7 @@ PATHS_DEFAULT = 1 | 2 | 4
 
 class Options(ctypes.Structure):
     _fields_ = [("paths", ctypes.c_uint32), ("rows", ctypes.c_int32 * 3),
-                ("graphs", ctypes.c_int32)]
+                ("graphs", ctypes.c_int32), ("fused", ctypes.c_int32)]
 
 
 class DbscanError(RuntimeError):
@@ -121,14 +121,16 @@ def dbscan_get_options() -> dict:
     """The process-wide tuning switches in force."""
     o = Options()
     _check(load().dbscan_get_options(ctypes.byref(o)), "dbscan_get_options")
-    return {"paths": int(o.paths), "rows": tuple(int(r) for r in o.rows), "graphs": int(o.graphs)}
+    return {"paths": int(o.paths), "rows": tuple(int(r) for r in o.rows), "graphs": int(o.graphs),
+            "fused": int(o.fused)}
 
 
-def dbscan_set_options(paths=None, rows=None, graphs=None, *, reset=False) -> None:
+def dbscan_set_options(paths=None, rows=None, graphs=None, fused=None, *, reset=False) -> None:
     """Change the switches (arguments left None keep their value); ``paths``
     is a bit mask or an iterable of names from PATH_BITS ("fp32" alone, or an
     empty iterable, allows CUDA cores only); ``rows`` one int for every sweep
-    or three (count, union, border); ``reset`` restores the defaults."""
+    or three (count, union, border); ``fused`` 0 keeps small problems on the
+    multi-kernel path; ``reset`` restores the defaults."""
     lib = load()
     if reset:
         _check(lib.dbscan_set_options(None), "dbscan_set_options")
@@ -146,6 +148,7 @@ def dbscan_set_options(paths=None, rows=None, graphs=None, *, reset=False) -> No
     for i in range(3):
         o.rows[i] = int(r[i])
     o.graphs = cur["graphs"] if graphs is None else int(bool(graphs))
+    o.fused = cur["fused"] if fused is None else int(bool(fused))
     _check(lib.dbscan_set_options(ctypes.byref(o)), "dbscan_set_options")
 
 
@@ -157,7 +160,8 @@ def options(**kw):
     try:
         yield
     finally:
-        dbscan_set_options(paths=saved["paths"], rows=saved["rows"], graphs=saved["graphs"])
+        dbscan_set_options(paths=saved["paths"], rows=saved["rows"], graphs=saved["graphs"],
+                           fused=saved["fused"])
 
 
 def dbscan_strerror(status: int) -> str:
@@ -283,11 +287,12 @@ PATHS = {0: "fp32", 1: "tf32", 2: "bf16", 3: "f16", 4: "f16acc16"}
 
 def dbscan_workspace_info(workspace: torch.Tensor, stream=None) -> dict:
     """Path chosen, core / candidate counts and exactness of the last call."""
-    out = (ctypes.c_int64 * 5)()
-    _check(load().dbscan_workspace_info(workspace.data_ptr(), _stream_handle(stream), out, 5),
+    out = (ctypes.c_int64 * 6)()
+    _check(load().dbscan_workspace_info(workspace.data_ptr(), _stream_handle(stream), out, 6),
            "dbscan_workspace_info")
     return {"path": PATHS.get(int(out[0]), str(out[0])), "n_core": int(out[1]),
-            "n_cand": int(out[2]), "exact": bool(out[3]), "kpad": int(out[4])}
+            "n_cand": int(out[2]), "exact": bool(out[3]), "kpad": int(out[4]),
+            "fused": bool(out[5])}
 
 
 STAGES = ("prep", "count", "compact", "union", "flatten", "border", "finalize")

@@ -123,6 +123,9 @@ static dbscan_options options_from_env() {
     }
     const char *g = getenv("DBSCAN_GRAPHS");
     if (g && g[0] == '0') o.graphs = 0;
+    o.fused = 1;
+    const char *fu = getenv("DBSCAN_FUSED");
+    if (fu && fu[0] == '0') o.fused = 0;
     return o;
 }
 
@@ -155,6 +158,7 @@ static Layout call_layout(int64_t n, int32_t d, float eps, int cull, const dbsca
     L.eps2 = eps * eps;
     L.allow = L.umma_tile_bytes ? allowed_tc(d, L.eps2, o.paths) : 0u;
     for (int m = 0; m < 3; ++m) L.rows[m] = o.rows[m];
+    L.fused = o.fused && fused_eligible(n, d);
     L.cull_nbr = L.box_floats > 0 && L.umma_tile_bytes > 0;
     L.cull = cull && L.cull_nbr;
     return L;
@@ -277,6 +281,7 @@ struct ProfCall {
     int stages;       // number of stages the call ran
     unsigned allow;   // tensor-core kinds launched by the call's sweeps
     int cull;         // 1: culled count, 2: culled union and border (box kernels)
+    int fused;        // 1: the fused single-launch pipeline (one kernel)
 };
 struct ProfState {
     bool on = false;
@@ -289,9 +294,10 @@ struct StageMarks {
     ProfCall call{};
     bool on = false;
     int next = 0;
-    StageMarks(cudaStream_t s, unsigned allow, int cull) {
+    StageMarks(cudaStream_t s, unsigned allow, int cull, int fused) {
         call.allow = allow;
         call.cull = cull;
+        call.fused = fused;
         if (!g_prof.on) return;
         for (int i = 0; i <= DBSCAN_NUM_STAGES; ++i) {
             if (cudaEventCreate(&call.ev[i]) != cudaSuccess) {
@@ -321,7 +327,20 @@ static int run(const void *points, int dtype, int64_t n, int d, float eps, int m
                int32_t *labels, uint8_t *is_core, int32_t *cnt_out, void *ws, const Layout &L,
                cudaStream_t s) {
     Work w = carve(ws, L);
-    StageMarks marks(s, L.allow, L.cull + 2 * L.cull_nbr);
+    StageMarks marks(s, L.allow, L.cull + 2 * L.cull_nbr, L.fused);
+    if (L.fused) {
+        // one launch does every stage; its time is reported under "count"
+        const size_t zero = L.off_stats + 2 * DBSCAN_MAX_D * sizeof(int);   // Ctrl + min/max
+        if (cudaMemsetAsync(w.ctrl, 0, zero, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+        if (cudaMemsetAsync(w.cnt, 0, (size_t)L.ntiles * BT * sizeof(int), s) != cudaSuccess)
+            return DBSCAN_ERR_CUDA;
+        marks.mark(s);
+        if (launch_fused(points, dtype, n, d, eps, min_pts, labels, is_core, cnt_out, w, L, s) !=
+            cudaSuccess)
+            return DBSCAN_ERR_CUDA;
+        for (int i = 0; i < DBSCAN_NUM_STAGES - 1; ++i) marks.mark(s);
+        return DBSCAN_OK;
+    }
     if (cudaMemsetAsync(w.ctrl, 0, sizeof(Ctrl), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     if (cudaMemsetAsync(w.cnt, 0, (size_t)n * sizeof(int), s) != cudaSuccess) return DBSCAN_ERR_CUDA;
     if (launch_prep(points, dtype, n, d, eps, L.allow, w, L, s) != cudaSuccess)
@@ -372,7 +391,7 @@ static int read_status(const void *ws, cudaStream_t s) {
 // the least recently used one destroyed to make room (an instance still
 // running is freed when it completes).
 using GraphKey = std::tuple<int, const void *, int, int64_t, int, uint32_t, int, void *, void *, void *,
-                            void *, int, unsigned, int, int, int>;
+                            void *, int, unsigned, int, int, int, int>;
 struct GraphEntry {
     GraphKey key;
     cudaGraphExec_t exec;
@@ -404,7 +423,7 @@ static int run_graph(const void *points, int dtype, int64_t n, int d, float eps,
     uint32_t eb;
     memcpy(&eb, &eps, sizeof(eb));
     const GraphKey key(dev, points, dtype, n, d, eb, min_pts, labels, is_core, cnt_out, ws, L.cull,
-                       L.allow, L.rows[0], L.rows[1], L.rows[2]);
+                       L.allow, L.rows[0], L.rows[1], L.rows[2], L.fused);
     std::lock_guard<std::mutex> lock(g_graph_mu);
     auto it = g_graphs.find(key);
     if (it != g_graphs.end()) {
@@ -555,6 +574,7 @@ int dbscan_set_options(const dbscan_options *opt) {
         for (int m = 0; m < 3; ++m)
             if (opt->rows[m] < 0 || opt->rows[m] > 2) return DBSCAN_ERR_INVALID_ARG;
         if (opt->graphs < 0 || opt->graphs > 1) return DBSCAN_ERR_INVALID_ARG;
+        if (opt->fused < 0 || opt->fused > 1) return DBSCAN_ERR_INVALID_ARG;
         o = *opt;
     } else {
         o = options_from_env();
@@ -577,8 +597,8 @@ int dbscan_workspace_info(const void *workspace, void *stream, int64_t *info, in
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DBSCAN_ERR_CUDA;
     if (cudaMemcpy(&c, workspace, sizeof(Ctrl), cudaMemcpyDeviceToHost) != cudaSuccess)
         return DBSCAN_ERR_CUDA;
-    const int64_t v[5] = {c.tc_kind, c.n_core, c.n_cand, c.exact, c.tc_kpad};
-    for (int i = 0; i < n && i < 5; ++i) info[i] = v[i];
+    const int64_t v[6] = {c.tc_kind, c.n_core, c.n_cand, c.exact, c.tc_kpad, c.fused};
+    for (int i = 0; i < n && i < 6; ++i) info[i] = v[i];
     return DBSCAN_OK;
 }
 
@@ -605,8 +625,11 @@ int dbscan_profile_end(float *stage_ms, int32_t max_stages, int64_t *calls,
             acc[i] += ms;
             // box kernels: all points in prep (culled count), core and
             // candidate arrays after compaction (union and border)
-            launches += stage_launches(c.allow, i) + ((c.cull & 1) && i == 0 ? 2 : 0) +
-                        ((c.cull & 2) && i == 2 ? 3 : 0);
+            if (c.fused)
+                launches += i == 1 ? 1 : 0;   // the one fused kernel, in the count stage
+            else
+                launches += stage_launches(c.allow, i) + ((c.cull & 1) && i == 0 ? 2 : 0) +
+                            ((c.cull & 2) && i == 2 ? 3 : 0);
         }
         for (int i = 0; i <= c.stages; ++i) cudaEventDestroy(c.ev[i]);
     }

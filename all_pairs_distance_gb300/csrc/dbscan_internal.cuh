@@ -48,7 +48,11 @@ struct Ctrl {
     float ord_lo[3];    // locality order: lower bound of each key axis
     float ord_scale[3]; // locality order: quantisation scale of each key axis
     unsigned band_ctr[8];   // work-unit counters of the tensor-core union bands
-    int pad1[29];
+    int fused;          // 1 when the call ran the fused single-launch pipeline
+    unsigned bar_gen;   // fused pipeline: grid barrier generation
+    unsigned bar_count; // fused pipeline: blocks arrived at the current barrier
+    int bar_abort;      // fused pipeline: set when a barrier wait timed out
+    int pad1[25];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl must be 256 bytes");
 
@@ -59,6 +63,7 @@ struct Layout {
     float eps2;           // fl32(eps * eps) of the call (0 in a bare size query)
     unsigned allow;       // tensor-core kinds the call may take (TC_ALLOW_* bits)
     int rows[3];          // row blocks per unit of count, union, border (0 = automatic)
+    int fused;            // 1: the whole call runs as the fused single-launch pipeline
     int64_t ntiles;       // ceil(n / BT)
     size_t tile_floats;   // (d + 1) * BT
     size_t off_ctrl, off_stats, off_staged_all, off_staged_core, off_staged_cand;
@@ -202,6 +207,20 @@ cudaError_t launch_union_tc_band(const Work &w, const Layout &L, int band, int b
 cudaError_t launch_border_tc(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
 
 int persistent_ctas(const void *kernel, int threads, size_t smem);
+
+// Fused single-launch pipeline (fused.cu): every stage in one cooperative
+// kernel, for problems small enough that launches dominate the multi-kernel
+// path.  cnt_out != NULL: counts only.  The control block and the statistics
+// arrays after it must be zero, and the counts array too.  Size limits from
+// GB300 measurements (the fused call against the multi-kernel call, both
+// replayed from graphs): faster up to ~5k points at d <= 4 and ~8k at d = 16.
+constexpr int64_t FUSED_MAX_N_LOW_D = 4096;   // d <= 4
+constexpr int64_t FUSED_MAX_N = 8192;         // 4 < d <= FUSED_MAX_D
+constexpr int FUSED_MAX_D = 32;
+bool fused_eligible(int64_t n, int d);
+cudaError_t launch_fused(const void *points, int dtype, int64_t n, int d, float eps, int min_pts,
+                         int32_t *labels, uint8_t *is_core, int32_t *cnt_out, const Work &w,
+                         const Layout &L, cudaStream_t s);
 
 // dbscan_fit_ex with a caller workspace, its kernels always launched directly
 // (no graph capture or instantiation): the body of dbscan_fit_noalloc.

@@ -93,16 +93,21 @@ typedef enum {
  *           border sweeps: 0 automatic, 1 or 2
  *   graphs  1: replay repeated calls from CUDA graphs (see dbscan_fit_ex);
  *           0: launch every kernel directly
+ *   fused   1: small problems -- at most 4,096 points with d <= 4, or 8,192
+ *           points with 4 < d <= 32 -- run as one fused, cooperative launch
+ *           whose grid-wide phases do every stage (CUDA cores, input order);
+ *           0: always the multi-kernel path
  * DBSCAN_PATH_F16_ACC16 is an opt-in: f16 operands with an f16 accumulator
  * (one K = 16 MMA per tile pair, d <= 10).  Its integer sum is rounded to f16
  * once, which keeps the sign the sweep reads -- provided the tensor core forms
  * the K = 16 sum exactly before that rounding.  NVIDIA does not document the
  * internal width of that sum; the library's tests observe it on GB300 only.
- * Defaults: paths = DBSCAN_PATHS_DEFAULT, rows automatic, graphs on; the
- * environment variables DBSCAN_FORCE_PATH (fp32, tf32, bf16, f16, f16acc16),
- * DBSCAN_TC_ROWS (one digit, or three for count, union, border) and
- * DBSCAN_GRAPHS (0 = off) override the defaults, read once per process at
- * the first call into the library.
+ * Defaults: paths = DBSCAN_PATHS_DEFAULT, rows automatic, graphs on, fused
+ * on; the environment variables DBSCAN_FORCE_PATH (fp32, tf32, bf16, f16,
+ * f16acc16), DBSCAN_TC_ROWS (one digit, or three for count, union, border),
+ * DBSCAN_GRAPHS (0 = off) and DBSCAN_FUSED (0 = off) override the defaults,
+ * read once per process at the first call into the library.  Start from
+ * dbscan_get_options when changing one switch.
  */
 #define DBSCAN_PATH_TF32 1u
 #define DBSCAN_PATH_BF16 2u
@@ -113,11 +118,12 @@ typedef struct {
     uint32_t paths;
     int32_t rows[3];
     int32_t graphs;
+    int32_t fused;
 } dbscan_options;
 
 /* Replace the switches (NULL restores the defaults above, environment
- * included).  DBSCAN_ERR_INVALID_ARG for unknown path bits or a rows entry
- * outside 0..2, or graphs outside 0..1. */
+ * included).  DBSCAN_ERR_INVALID_ARG for unknown path bits, a rows entry
+ * outside 0..2, or graphs or fused outside 0..1. */
 int dbscan_set_options(const dbscan_options *opt);
 /* The switches in force (host pointer). */
 int dbscan_get_options(dbscan_options *opt);
@@ -280,6 +286,8 @@ int dbscan_workspace_status(const void *workspace, void *stream);
  *   3  1 when every coordinate was an integer and sum_k (max_k - min_k)^2 <
  *      2^24, i.e. the results are exact (see "Exactness" above), else 0
  *   4  padded operand width K of the tensor-core path (0 on CUDA cores)
+ *   5  1 when the call ran as the fused single-launch pipeline (fp32 FMAs
+ *      on CUDA cores), else 0
  * info is a host pointer to n int64 values.  Returns DBSCAN_OK,
  * DBSCAN_ERR_INVALID_ARG for a NULL pointer or n < 1, or DBSCAN_ERR_CUDA.
  */

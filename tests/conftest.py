@@ -11,6 +11,22 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running check")
+    config.addinivalue_line("markers", "fused_pipeline: runs with the library's default "
+                                       "(small problems take the fused single-launch pipeline)")
+
+
+@pytest.fixture(autouse=True)
+def _multi_kernel_path_by_default(request):
+    """GPU tests exercise the multi-kernel path (tensor-core and CUDA-core
+    sweeps) even on the small sets the fused single-launch pipeline would
+    otherwise take; tests marked fused_pipeline keep the library default."""
+    if request.node.get_closest_marker("gpu") is None or \
+            request.node.get_closest_marker("fused_pipeline") is not None:
+        yield
+        return
+    from all_pairs_distance_gb300 import binding
+    with binding.options(fused=0):
+        yield
 
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
