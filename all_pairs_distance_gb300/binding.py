@@ -90,6 +90,10 @@ def load():
         lib.dbscan_profile_end.restype = ctypes.c_int
         lib.dbscan_strerror.argtypes = [ctypes.c_int]
         lib.dbscan_strerror.restype = ctypes.c_char_p
+        lib.dbscan_fit_shard.argtypes = [i32, P, i32, i64, i32, f32, i32, i32, i32, P, P, P, P, sz, P]
+        lib.dbscan_fit_shard.restype = ctypes.c_int
+        lib.dbscan_shard_buffer.argtypes = [P, i64, i32, i32, P, P]
+        lib.dbscan_shard_buffer.restype = ctypes.c_int
         lib.dbscan_set_options.argtypes = [P]
         lib.dbscan_set_options.restype = ctypes.c_int
         lib.dbscan_get_options.argtypes = [P]
@@ -162,6 +166,32 @@ def options(**kw):
     finally:
         dbscan_set_options(paths=saved["paths"], rows=saved["rows"], graphs=saved["graphs"],
                            fused=saved["fused"])
+
+
+SHARD_COUNTS, SHARD_PARENTS, SHARD_ORDER = 0, 1, 2
+
+
+def dbscan_fit_shard(stage: int, points: torch.Tensor, eps: float, min_pts: int, rank: int,
+                     world: int, *, workspace: torch.Tensor, labels=None, is_core=None,
+                     gathered=None, stream=None) -> None:
+    """One stage (0-4) of the sharded pipeline on this rank (dbscan.h)."""
+    p = _points(points)
+    n, d = p.shape
+    ptr = lambda t: None if t is None else t.data_ptr()
+    _check(load().dbscan_fit_shard(int(stage), p.data_ptr(), DTYPES[p.dtype], n, d, float(eps),
+                                   int(min_pts), int(rank), int(world), ptr(gathered), ptr(labels),
+                                   ptr(is_core), workspace.data_ptr(), workspace.numel(),
+                                   _stream_handle(stream)), f"dbscan_fit_shard stage {stage}")
+
+
+def dbscan_shard_buffer(workspace: torch.Tensor, n: int, d: int, which: int) -> torch.Tensor:
+    """The int32 workspace array the ranks combine between stages, as a view."""
+    ptr = ctypes.c_void_p()
+    count = ctypes.c_int64()
+    _check(load().dbscan_shard_buffer(workspace.data_ptr(), int(n), int(d), int(which),
+                                      ctypes.byref(ptr), ctypes.byref(count)), "dbscan_shard_buffer")
+    off = ptr.value - workspace.data_ptr()
+    return workspace[off:off + 4 * count.value].view(torch.int32)
 
 
 def dbscan_strerror(status: int) -> str:

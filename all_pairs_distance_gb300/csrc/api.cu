@@ -35,6 +35,8 @@ Layout make_layout(int64_t n, int32_t d) {
     Layout L{};
     L.n = n;
     L.d = d;
+    L.rank = 0;
+    L.world = 1;
     L.ntiles = (n + BT - 1) / BT;
     L.tile_floats = (size_t)(d + 1) * BT;
     const size_t staged = (size_t)L.ntiles * L.tile_floats * sizeof(float);
@@ -507,6 +509,49 @@ static int fit_common(const void *points, int32_t dtype, int64_t n, int32_t d, f
     return st != DBSCAN_OK ? st : dev_st;
 }
 
+// ---- sharding across processes ----------------------------------------------
+// One stage of the sharded pipeline.  Every rank stages the points in rank
+// 0's locality order (the caller broadcasts it after stage 0: the order's
+// counting sort places points within a bin in atomic order, so it can differ
+// between ranks), and staging, compaction, flatten and finalize are then
+// deterministic, so every position means the same point on every rank; the
+// count, union and border sweeps take only this rank's work units.  Between
+// stages the caller combines the ranks' buffers with collectives (dbscan.h,
+// dbscan_fit_shard).
+static int run_shard_stage(int stage, const void *points, int dtype, int64_t n, int d, float eps,
+                           int min_pts, const int32_t *gathered, int32_t *labels, uint8_t *is_core,
+                           void *ws, const Layout &L, cudaStream_t s) {
+    Work w = carve(ws, L);
+    switch (stage) {
+    case 0:
+        if (cudaMemsetAsync(w.ctrl, 0, sizeof(Ctrl), s) != cudaSuccess ||
+            cudaMemsetAsync(w.cnt, 0, (size_t)n * sizeof(int), s) != cudaSuccess)
+            return DBSCAN_ERR_CUDA;
+        return launch_prep_order(points, dtype, n, d, eps, L.allow, w, L, s) == cudaSuccess
+                   ? DBSCAN_OK
+                   : DBSCAN_ERR_CUDA;
+    case 1:
+        if (launch_prep_stage(points, dtype, n, d, w, L, s) != cudaSuccess ||
+            launch_count(w, L, s) != cudaSuccess)
+            return DBSCAN_ERR_CUDA;
+        return DBSCAN_OK;
+    case 2:
+        if (launch_compact(w, L, min_pts, labels, is_core, s) != cudaSuccess) return DBSCAN_ERR_CUDA;
+        if (L.cull_nbr && (launch_tile_boxes(w, L, 1, s) != cudaSuccess ||
+                           launch_tile_boxes(w, L, 2, s) != cudaSuccess))
+            return DBSCAN_ERR_CUDA;
+        return launch_union(w, L, s) == cudaSuccess ? DBSCAN_OK : DBSCAN_ERR_CUDA;
+    case 3:
+        if (launch_merge_forests(w, L, gathered, n, L.world, s) != cudaSuccess ||
+            launch_flatten(w, L, labels, s) != cudaSuccess ||
+            launch_stage_umma(w, L, 2, s) != cudaSuccess || launch_border(w, L, labels, s) != cudaSuccess)
+            return DBSCAN_ERR_CUDA;
+        return DBSCAN_OK;
+    default:
+        return launch_finalize(w, L, labels, s) == cudaSuccess ? DBSCAN_OK : DBSCAN_ERR_CUDA;
+    }
+}
+
 int fit_direct(const void *points, int32_t dtype, int64_t n, int32_t d, float eps, int32_t min_pts,
                int32_t *labels, uint8_t *is_core, void *workspace, size_t workspace_bytes,
                void *stream) {
@@ -563,6 +608,47 @@ int dbscan_neighbor_counts(const void *points, int32_t dtype, int64_t n, int32_t
                            void *stream) {
     return fit_common(points, dtype, n, d, eps, 1, nullptr, nullptr, cnt_out, workspace,
                       workspace_bytes, stream);
+}
+
+int dbscan_fit_shard(int32_t stage, const void *points, int32_t dtype, int64_t n, int32_t d, float eps,
+                     int32_t min_pts, int32_t rank, int32_t world, const int32_t *gathered_parents,
+                     int32_t *labels_out, uint8_t *is_core_out, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+    int st = check_shape(n, d, dtype);
+    if (st != DBSCAN_OK) return st;
+    if ((st = check_scalars(eps, min_pts)) != DBSCAN_OK) return st;
+    if (stage < 0 || stage > 4 || world < 1 || rank < 0 || rank >= world) return DBSCAN_ERR_INVALID_ARG;
+    if (n == 0) return DBSCAN_OK;
+    if (!workspace) return DBSCAN_ERR_INVALID_ARG;   // the stages share the workspace's state
+    Layout L = call_layout(n, d, eps, 0, options_snapshot());
+    L.fused = 0;   // the fused pipeline does not split its work
+    L.rank = rank;
+    L.world = world;
+    if (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return DBSCAN_ERR_INVALID_ARG;
+    if (check_device_ptr(workspace) != DBSCAN_OK) return DBSCAN_ERR_INVALID_ARG;
+    if (stage <= 1 && (!points || check_device_ptr(points) != DBSCAN_OK)) return DBSCAN_ERR_INVALID_ARG;
+    if (stage == 2 && (!labels_out || !is_core_out || check_device_ptr(labels_out) != DBSCAN_OK ||
+                       check_device_ptr(is_core_out) != DBSCAN_OK))
+        return DBSCAN_ERR_INVALID_ARG;
+    if (stage >= 3 && (!labels_out || check_device_ptr(labels_out) != DBSCAN_OK)) return DBSCAN_ERR_INVALID_ARG;
+    if (stage == 3 && (!gathered_parents || check_device_ptr(gathered_parents) != DBSCAN_OK))
+        return DBSCAN_ERR_INVALID_ARG;
+    return run_shard_stage(stage, points, dtype, n, d, eps, min_pts, gathered_parents, labels_out,
+                           is_core_out, workspace, L, static_cast<cudaStream_t>(stream));
+}
+
+int dbscan_shard_buffer(void *workspace, int64_t n, int32_t d, int32_t which, void **ptr,
+                        int64_t *count) {
+    if (!workspace || !ptr || !count || n < 0 || d < 1 || d > DBSCAN_MAX_D) return DBSCAN_ERR_INVALID_ARG;
+    if (which != DBSCAN_SHARD_COUNTS && which != DBSCAN_SHARD_PARENTS && which != DBSCAN_SHARD_ORDER)
+        return DBSCAN_ERR_INVALID_ARG;
+    const Layout L = make_layout(n, d);
+    char *b = static_cast<char *>(workspace);
+    *ptr = b + (which == DBSCAN_SHARD_COUNTS ? L.off_cnt
+                                             : (which == DBSCAN_SHARD_PARENTS ? L.off_parent : L.off_perm));
+    *count = n;
+    return DBSCAN_OK;
 }
 
 int dbscan_set_options(const dbscan_options *opt) {

@@ -64,6 +64,7 @@ struct Layout {
     unsigned allow;       // tensor-core kinds the call may take (TC_ALLOW_* bits)
     int rows[3];          // row blocks per unit of count, union, border (0 = automatic)
     int fused;            // 1: the whole call runs as the fused single-launch pipeline
+    int rank, world;      // sharding: the sweeps take work units u with u % world == rank
     int64_t ntiles;       // ceil(n / BT)
     size_t tile_floats;   // (d + 1) * BT
     size_t off_ctrl, off_stats, off_staged_all, off_staged_core, off_staged_cand;
@@ -190,6 +191,12 @@ cudaError_t launch_unpermute_counts(const Work &w, const Layout &L, int32_t *cnt
 cudaError_t launch_tile_boxes(const Work &w, const Layout &L, int which, cudaStream_t s);
 cudaError_t launch_prep(const void *points, int dtype, int64_t n, int d, float eps, int allow_tc,
                         const Work &w, const Layout &L, cudaStream_t s);
+// launch_prep in two parts: statistics, setup and the locality order (perm);
+// then the staged points and operand rows in that order.
+cudaError_t launch_prep_order(const void *points, int dtype, int64_t n, int d, float eps, int allow_tc,
+                              const Work &w, const Layout &L, cudaStream_t s);
+cudaError_t launch_prep_stage(const void *points, int dtype, int64_t n, int d, const Work &w,
+                              const Layout &L, cudaStream_t s);
 cudaError_t launch_stage_umma(const Work &w, const Layout &L, int which, cudaStream_t s);
 cudaError_t launch_count(const Work &w, const Layout &L, cudaStream_t s);
 cudaError_t launch_compact(const Work &w, const Layout &L, int min_pts,
@@ -198,6 +205,10 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s);
 cudaError_t launch_flatten(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
 cudaError_t launch_border(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
 cudaError_t launch_finalize(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s);
+// Sharding: unite every core position with every rank's union-find parent of
+// it (gathered: world arrays of stride ints).
+cudaError_t launch_merge_forests(const Work &w, const Layout &L, const int *gathered, int64_t stride,
+                                 int world, cudaStream_t s);
 
 cudaError_t launch_count_tc(const Work &w, const Layout &L, cudaStream_t s);
 // Tensor-core union over the tile pairs (rb, t) of the upper triangle with

@@ -301,8 +301,8 @@ __global__ void k_stage(const void *pts, int dtype, int64_t n, int d, const Ctrl
     }
 }
 
-cudaError_t launch_prep(const void *points, int dtype, int64_t n, int d, float eps, int allow_tc,
-                        const Work &w, const Layout &L, cudaStream_t s) {
+cudaError_t launch_prep_order(const void *points, int dtype, int64_t n, int d, float eps, int allow_tc,
+                              const Work &w, const Layout &L, cudaStream_t s) {
     const float eps2 = eps * eps;
     k_init_stats<<<1, 256, 0, s>>>(w.ctrl, w.stat_min, w.stat_max, n, d);
     int64_t elems = n * (int64_t)d;
@@ -313,15 +313,25 @@ cudaError_t launch_prep(const void *points, int dtype, int64_t n, int d, float e
     k_stats<<<blocks, 256, 0, s>>>(points, dtype, n, d, w.ctrl, w.stat_min, w.stat_max);
     k_setup<<<1, 256, 0, s>>>(w.ctrl, w.stat_min, w.stat_max, w.centre, d, eps2,
                               L.umma_tile_bytes ? allow_tc : 0);
-    cudaError_t e = launch_order(points, dtype, n, d, w, L, s);
-    if (e != cudaSuccess) return e;
+    return launch_order(points, dtype, n, d, w, L, s);
+}
+
+cudaError_t launch_prep_stage(const void *points, int dtype, int64_t n, int d, const Work &w,
+                              const Layout &L, cudaStream_t s) {
     const int64_t npad = L.ntiles * BT;
     int sblocks = (int)((npad + 255) / 256);
     k_stage<<<sblocks, 256, d * sizeof(float), s>>>(points, dtype, n, d, w.ctrl, w.centre,
                                                      w.perm, w.staged_all, w.T_all, npad);
-    e = cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_stage_umma(w, L, 0, s);
+}
+
+cudaError_t launch_prep(const void *points, int dtype, int64_t n, int d, float eps, int allow_tc,
+                        const Work &w, const Layout &L, cudaStream_t s) {
+    cudaError_t e = launch_prep_order(points, dtype, n, d, eps, allow_tc, w, L, s);
+    if (e != cudaSuccess) return e;
+    return launch_prep_stage(points, dtype, n, d, w, L, s);
 }
 
 }  // namespace dbscan

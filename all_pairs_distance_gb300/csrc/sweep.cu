@@ -63,6 +63,7 @@ struct SweepArgs {
     int *parent;           // pass 2: union-find parents
     const int *candidx;    // pass 3: original index of each candidate position
     int32_t *labels;       // pass 3: labels (original order)
+    int srank, sworld;     // sharding: this rank takes units ubegin + k * sworld + srank
 };
 
 // Position of a thread's m-th row (or column) inside a 128-point tile.  Two
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
     const Sched sc = make_sched(n_rows, n_cols, a.tri, a.ulo, a.uhi);
 
     for (;;) {
-        if (tid == 0) s_unit = sc.ubegin + atomicAdd(a.ctr, 1u);
+        if (tid == 0) s_unit = sc.ubegin + atomicAdd(a.ctr, 1u) * (unsigned)a.sworld + (unsigned)a.srank;
         __syncthreads();
         const unsigned u = s_unit;
         __syncthreads();
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
     const Sched sc = make_sched(n_rows, n_cols, a.tri, a.ulo, a.uhi);
 
     for (;;) {
-        if (tid == 0) s_unit = sc.ubegin + atomicAdd(a.ctr, 1u);
+        if (tid == 0) s_unit = sc.ubegin + atomicAdd(a.ctr, 1u) * (unsigned)a.sworld + (unsigned)a.srank;
         __syncthreads();
         const unsigned u = s_unit;
         __syncthreads();
@@ -611,6 +612,7 @@ static cudaError_t dispatch(const SweepArgs &args, int d, cudaStream_t s) {
 
 cudaError_t launch_count(const Work &w, const Layout &L, cudaStream_t s) {
     SweepArgs a{};
+    a.srank = L.rank; a.sworld = L.world;
     a.rows = w.staged_all; a.rowT = w.T_all; a.n_rows = &w.ctrl->n_all;
     a.cols = w.staged_all; a.n_cols = &w.ctrl->n_all;
     a.tri = 1; a.ulo = 0; a.uhi = -1;
@@ -622,6 +624,7 @@ cudaError_t launch_count(const Work &w, const Layout &L, cudaStream_t s) {
 
 cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
     SweepArgs a{};
+    a.srank = L.rank; a.sworld = L.world;
     a.rows = w.staged_core; a.rowT = w.T_core; a.n_rows = &w.ctrl->n_core;
     a.cols = w.staged_core; a.n_cols = &w.ctrl->n_core; a.aux = w.parent;
     a.tri = 1; a.ctrl = w.ctrl; a.parent = w.parent;
@@ -672,8 +675,31 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
     return cudaSuccess;
 }
 
+// Sharding: every rank's union-find forest links core positions of one
+// component (each link is a neighbour pair or a chain of them), so uniting
+// every core position i with every rank's parent of i joins exactly the union
+// of the neighbour pairs all ranks evaluated.
+__global__ void k_merge_forests(Ctrl *ctrl, int *parent, const int *gathered, int64_t stride,
+                                int world) {
+    const int nc = ctrl->n_core;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nc; i += gridDim.x * blockDim.x) {
+        for (int r = 0; r < world; ++r) {
+            const int p = gathered[(size_t)r * stride + i];
+            if (p != i && p >= 0 && p < nc) uf_unite(parent, i, p, ctrl);
+        }
+    }
+}
+
+cudaError_t launch_merge_forests(const Work &w, const Layout &L, const int *gathered, int64_t stride,
+                                 int world, cudaStream_t s) {
+    const int grid = persistent_ctas((const void *)k_compress, 256, 0);
+    k_merge_forests<<<grid, 256, 0, s>>>(w.ctrl, w.parent, gathered, stride, world);
+    return cudaGetLastError();   // k_flatten follows every position to its root
+}
+
 cudaError_t launch_border(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s) {
     SweepArgs a{};
+    a.srank = L.rank; a.sworld = L.world;
     a.rows = w.staged_cand; a.rowT = w.T_cand; a.n_rows = &w.ctrl->n_cand;
     a.cols = w.staged_core; a.n_cols = &w.ctrl->n_core; a.aux = w.clabel;
     a.tri = 0; a.ulo = 0; a.uhi = -1;

@@ -93,6 +93,7 @@ struct TcArgs {
     int group;                // column tiles per stage
     int stage_bytes;          // bytes reserved per stage (group tiles + group x BT ints)
     int tile_bytes_max;       // bytes reserved per operand tile
+    int srank, sworld;        // sharding: this rank takes units k * sworld + srank
 };
 
 struct Meta {
@@ -385,7 +386,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         const float cthr = ctrl->thrx;
         for (;;) {
             unsigned u = 0;
-            if (lane == 0) u = atomicAdd(a.ctr, 1u);
+            if (lane == 0) u = atomicAdd(a.ctr, 1u) * (unsigned)a.sworld + (unsigned)a.srank;
             u = __shfl_sync(FULL, u, 0);
             if (u >= sc.units) break;
             int rb, nrow, t0, t1;
@@ -916,6 +917,7 @@ cudaError_t run_tc_both(const TcArgs &a, const Layout &L, cudaStream_t s) {
 
 cudaError_t launch_count_tc(const Work &w, const Layout &L, cudaStream_t s) {
     TcArgs a{};
+    a.srank = L.rank; a.sworld = L.world;
     a.ua = w.ua_all; a.ub = w.ub_all;
     a.n_rows = &w.ctrl->n_all; a.n_cols = &w.ctrl->n_all;
     a.tri = 1;
@@ -927,6 +929,7 @@ cudaError_t launch_count_tc(const Work &w, const Layout &L, cudaStream_t s) {
 cudaError_t launch_union_tc_band(const Work &w, const Layout &L, int band, int blo, int bhi,
                                  cudaStream_t s) {
     TcArgs a{};
+    a.srank = L.rank; a.sworld = L.world;
     a.ua = w.ua_core; a.ub = w.ub_core;
     a.n_rows = &w.ctrl->n_core; a.n_cols = &w.ctrl->n_core; a.aux = w.parent;
     a.tri = 1;
@@ -939,6 +942,7 @@ cudaError_t launch_union_tc_band(const Work &w, const Layout &L, int band, int b
 
 cudaError_t launch_border_tc(const Work &w, const Layout &L, int32_t *labels, cudaStream_t s) {
     TcArgs a{};
+    a.srank = L.rank; a.sworld = L.world;
     a.ua = w.ua_cand; a.ub = w.ub_core;
     a.n_rows = &w.ctrl->n_cand; a.n_cols = &w.ctrl->n_core; a.aux = w.clabel;
     a.tri = 0;

@@ -265,6 +265,52 @@ int dbscan_fit_noalloc(const void *points, int32_t dtype, int64_t n, int32_t d,
                        float eps, int32_t min_pts, int32_t *labels_out,
                        uint8_t *is_core_out, void *stream);
 
+/*
+ * Sharded DBSCAN across `world` processes, one GPU each (rank = this
+ * process's index).  The pages run one GPU; the split follows the row-block
+ * partition of the upper triangle: every rank holds all points and stages
+ * them in one locality order, while the count, union and border sweeps take
+ * only the work units u with u % world == rank.  The caller runs five stages
+ * on the same workspace and, between them, four collectives over all ranks
+ * (NCCL, say):
+ *   stage 0  statistics and the locality order              (points)
+ *            -> broadcast from rank 0 the int32 array DBSCAN_SHARD_ORDER
+ *               (the order's counting sort places points within a bin in
+ *               atomic order, so ranks must share one order)
+ *   stage 1  staging + this rank's share of the count        (points)
+ *            -> all-reduce SUM over the int32 array DBSCAN_SHARD_COUNTS
+ *   stage 2  core flags (is_core_out written) + this rank's share of the
+ *            union-find over core pairs                      (labels_out, is_core_out)
+ *            -> all-gather the int32 array DBSCAN_SHARD_PARENTS of every rank
+ *               into a device array [world, n] (rank order)
+ *   stage 3  merge of all ranks' forests, core labels, this rank's share of
+ *            the border assignment                           (gathered_parents, labels_out)
+ *            -> all-reduce MIN over labels_out (n int32)
+ *   stage 4  finalize                                        (labels_out)
+ * Arguments not used by a stage may be NULL; n, d, dtype, eps, min_pts, rank
+ * and world must be the same at every stage and on every rank (points too).
+ * The workspace (dbscan_workspace_size bytes, required) carries the state
+ * between stages.  Every stage is asynchronous on `stream` and launches its
+ * kernels directly; device-side errors: dbscan_workspace_status.  With
+ * world = 1 and no collectives the stages give dbscan_fit_ex's results.
+ * The tuning switches in force must not change between stages (the fused
+ * small-problem pipeline is never used here).
+ */
+#define DBSCAN_SHARD_COUNTS 0
+#define DBSCAN_SHARD_PARENTS 1
+#define DBSCAN_SHARD_ORDER 2
+int dbscan_fit_shard(int32_t stage, const void *points, int32_t dtype, int64_t n, int32_t d,
+                     float eps, int32_t min_pts, int32_t rank, int32_t world,
+                     const int32_t *gathered_parents, int32_t *labels_out,
+                     uint8_t *is_core_out, void *workspace, size_t workspace_bytes,
+                     void *stream);
+/* Device address and length (ints) of a workspace array the caller combines
+ * across ranks between stages (which: DBSCAN_SHARD_ORDER, DBSCAN_SHARD_COUNTS
+ * or DBSCAN_SHARD_PARENTS); n and d as for the stages.  Pure host
+ * computation. */
+int dbscan_shard_buffer(void *workspace, int64_t n, int32_t d, int32_t which, void **ptr,
+                        int64_t *count);
+
 /* Bytes of workspace dbscan_fit_ex needs for this problem shape; 0 when the
  * shape is invalid or unsupported.  Pure host computation. */
 size_t dbscan_workspace_size(int64_t n, int32_t d, int32_t dtype);

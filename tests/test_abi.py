@@ -155,3 +155,40 @@ def test_options_roundtrip_and_validation(lib, monkeypatch):
         monkeypatch.delenv("DBSCAN_GRAPHS", raising=False)
         monkeypatch.delenv("DBSCAN_FUSED", raising=False)
         binding.dbscan_set_options(reset=True)
+
+
+def test_shard_host_side_checks(lib):
+    # argument errors are found on the host before any device work
+    f = lib.dbscan_fit_shard
+    P = ctypes.c_void_p
+    f.argtypes = [ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P, P, P, ctypes.c_size_t, P]
+    f.restype = ctypes.c_int
+    fake = ctypes.c_void_p(0x1000)
+    INVALID, UNSUP = -1, -2
+    for stage, rank, world in ((-1, 0, 1), (5, 0, 1), (0, 1, 1), (0, -1, 2), (0, 0, 0)):
+        assert f(stage, fake, 0, 10, 3, 1.0, 2, rank, world, None, None, None, fake, 1 << 20, None) == INVALID
+    assert f(0, fake, 0, 10, 3, 1.0, 2, 0, 1, None, None, None, None, 0, None) == INVALID   # no workspace
+    assert f(0, fake, 0, 10, 300, 1.0, 2, 0, 1, None, None, None, fake, 1 << 20, None) == UNSUP
+    assert f(0, fake, 0, 10, 3, -1.0, 2, 0, 1, None, None, None, fake, 1 << 20, None) == INVALID
+    assert f(2, None, 0, 0, 3, 1.0, 2, 0, 2, None, None, None, None, 0, None) == 0   # n == 0: no-op
+    # the combined buffers lie inside the workspace, one int per point each
+    g = lib.dbscan_shard_buffer
+    g.argtypes = [P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, P, P]
+    g.restype = ctypes.c_int
+    size = lib.dbscan_workspace_size
+    size.restype = ctypes.c_size_t
+    size.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
+    base = 1 << 32
+    total = size(50_000, 3, 0)
+    spans = []
+    for which in (0, 1, 2):
+        ptr, cnt = ctypes.c_void_p(), ctypes.c_int64()
+        assert g(ctypes.c_void_p(base), 50_000, 3, which, ctypes.byref(ptr), ctypes.byref(cnt)) == 0
+        assert cnt.value == 50_000 and base <= ptr.value and ptr.value + 4 * cnt.value <= base + total
+        spans.append((ptr.value, ptr.value + 4 * cnt.value))
+    for a in range(3):
+        for b in range(a):
+            assert spans[a][1] <= spans[b][0] or spans[b][1] <= spans[a][0]
+    ptr, cnt = ctypes.c_void_p(), ctypes.c_int64()
+    assert g(ctypes.c_void_p(base), 50_000, 3, 3, ctypes.byref(ptr), ctypes.byref(cnt)) == INVALID
