@@ -140,11 +140,12 @@ enum {
     TC_ALLOW_F16H = DBSCAN_PATH_F16_ACC16
 };
 __host__ __device__ inline unsigned tc_allow_bit(int kind) { return 1u << (kind - 1); }
-// Largest operand row the tensor-core sweep stages: two row tiles and two
-// stages of two column tiles (plus their aux ints) must fit 224 KB of shared
-// memory, 768 x kbytes + 2 KB; 288 bytes is 144 bf16/f16 (d <= 137) or 72
-// tf32 (d <= 67) elements.
-constexpr int TC_MAX_KBYTES = 288;
+// Largest operand row the tensor-core sweep stages.  Up to 288 bytes two row
+// tiles and two stages of two column tiles (plus their aux ints) fit 224 KB of
+// shared memory; wider rows, up to 544 bytes (272 bf16/f16 elements: d = 256
+// with its digits; 136 tf32 elements), take one row tile and stages of one
+// column tile (sweep_tc.cu).
+constexpr int TC_MAX_KBYTES = 544;
 constexpr int TC_F16H_KBYTES = 32;   // the one K = 16 MMA of the F16H path
 
 __host__ __device__ inline bool tc_is_f16(int kind) { return kind == TC_F16 || kind == TC_F16H; }

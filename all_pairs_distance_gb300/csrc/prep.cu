@@ -27,8 +27,9 @@
 // with |c|^2 = sum_k n_k B^k and thrx = sum_k h_k B^k (all digits in [0, B)),
 // every element exactly representable.  The positive terms sum to at most
 // 4 S and the negative ones to at most 2 S + thrx (S = sum_k M_k^2); when both
-// are below 2^24 every partial sum the tensor core forms, in any order, is an
-// exact integer, and w_ij < 0 <=> neighbour.  Every kind accumulates in f32,
+// are at most 2^24 every partial sum the tensor core forms, in any order, is
+// an integer of magnitude at most 2^24, exact in f32, and w_ij < 0 <=>
+// neighbour.  Every kind accumulates in f32,
 // except the opt-in F16H kind, taken only when the whole row fits one K = 16
 // MMA: its f16 accumulator rounds the sum once, which keeps the sign (the
 // smallest nonzero |w| is 1; overflow gives +-inf; an exact zero is stored as
@@ -128,7 +129,9 @@ __global__ void k_setup(Ctrl *ctrl, const int *smin, const int *smax, float *cen
         const double thrx = (double)ctrl->thrx;
         const int nt = tc_nt_for(TC_TF32, thrx);
         int kind = TC_NONE;
-        if (integral && !ctrl->nonfinite && 4.0 * S < 16777216.0 && 2.0 * S + thrx < 16777216.0) {
+        // every partial sum lies in [-(2 S + thrx), 4 S]; integers of magnitude
+        // up to 2^24 are exact in f32 (d = 256 over [0, 255] reaches 4 S = 2^24)
+        if (integral && !ctrl->nonfinite && 4.0 * S <= 16777216.0 && 2.0 * S + thrx <= 16777216.0) {
             // preference: the opt-in F16H (one MMA, half-width accumulator reads),
             // then BF16 (ranges up to 256), F16 (up to 2048; the same MMA rate),
             // TF32 (half the rate; threshold constants of three digits)

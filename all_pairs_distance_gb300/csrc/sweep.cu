@@ -336,16 +336,20 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
 
 // ===========================================================================
 // d > 4: rows and columns from shared memory, 8x8 register accumulators.
+// S = 1 (d > 128, where a row tile and two column stages exceed shared
+// memory): one column stage, loaded and used in turn, and the row values read
+// from the staged row tile in global memory (L2-resident).
 // ===========================================================================
 template <int MODE, int S>
 __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
     constexpr bool AUX = MODE != SWEEP_COUNT;
+    constexpr bool ROWS_GLOBAL = S == 1;
     extern __shared__ __align__(16) float smem[];
     __shared__ unsigned s_unit;
     const int TILE = (D + 1) * BT;
     const int STAGE = TILE + (AUX ? BT : 0);
-    float *rowbuf = smem;                  // D * BT floats: -2 c of the row tile
-    float *stages = smem + D * BT;         // S * STAGE floats
+    float *rowbuf = smem;                                 // D * BT floats: -2 c of the row tile
+    float *stages = smem + (ROWS_GLOBAL ? 0 : D * BT);    // S * STAGE floats
 
     if (a.ctrl->tc_kind != TC_NONE) return;   // the tensor-core sweep handles this data
     const int tid = threadIdx.x;
@@ -363,7 +367,9 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
         int rb, t0, t1;
         if (!decode_unit(u, sc, a.tri, rb, t0, t1)) continue;
 
-        {
+        const float *rowsrc = ROWS_GLOBAL ? a.rows + (size_t)rb * TILE : rowbuf;
+        const float rscale = ROWS_GLOBAL ? -2.f : 1.f;
+        if (!ROWS_GLOBAL) {
             const float *rt = a.rows + (size_t)rb * TILE;
             for (int e = tid; e < D * BT; e += THREADS) rowbuf[e] = -2.f * rt[e];
         }
@@ -380,18 +386,26 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
         for (int m = 0; m < R; ++m) row_init<MODE>(a, rb * BT + slot_of(tr, m), n_rows, acc[m]);
 
         const int nst = t1 - t0;   // one tile per stage
+        if constexpr (S > 1) {
 #pragma unroll
-        for (int s = 0; s < S - 1; ++s) {
-            if (s < nst) issue_stage<AUX>(stages + s * STAGE, a, t0 + s, 1, TILE, 1);
-            cp_async_commit();
+            for (int s = 0; s < S - 1; ++s) {
+                if (s < nst) issue_stage<AUX>(stages + s * STAGE, a, t0 + s, 1, TILE, 1);
+                cp_async_commit();
+            }
         }
         for (int g = 0; g < nst; ++g) {
-            cp_async_wait<S - 2>();
-            __syncthreads();
-            {
+            if constexpr (S > 1) {
+                cp_async_wait<S - 2>();
+                __syncthreads();
                 int gn = g + S - 1;
                 if (gn < nst) issue_stage<AUX>(stages + (gn % S) * STAGE, a, t0 + gn, 1, TILE, 1);
                 cp_async_commit();
+            } else {
+                __syncthreads();   // every thread is done with the previous tile
+                issue_stage<AUX>(stages, a, t0 + g, 1, TILE, 1);
+                cp_async_commit();
+                cp_async_wait<0>();
+                __syncthreads();
             }
             const int tile = t0 + g;
             const float *st = stages + (g % S) * STAGE;
@@ -408,11 +422,12 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
             }
 #pragma unroll 2
             for (int k = 0; k < D; ++k) {
-                float4 rlo = *reinterpret_cast<const float4 *>(rowbuf + k * BT + 4 * tr);
-                float4 rhi = *reinterpret_cast<const float4 *>(rowbuf + k * BT + 64 + 4 * tr);
+                const float4 rlo = *reinterpret_cast<const float4 *>(rowsrc + k * BT + 4 * tr);
+                const float4 rhi = *reinterpret_cast<const float4 *>(rowsrc + k * BT + 64 + 4 * tr);
                 float4 xlo = *reinterpret_cast<const float4 *>(st + k * BT + 4 * tc);
                 float4 xhi = *reinterpret_cast<const float4 *>(st + k * BT + 64 + 4 * tc);
-                float rr[R] = {rlo.x, rlo.y, rlo.z, rlo.w, rhi.x, rhi.y, rhi.z, rhi.w};
+                float rr[R] = {rscale * rlo.x, rscale * rlo.y, rscale * rlo.z, rscale * rlo.w,
+                               rscale * rhi.x, rscale * rhi.y, rscale * rhi.z, rscale * rhi.w};
                 float xx[C] = {xlo.x, xlo.y, xlo.z, xlo.w, xhi.x, xhi.y, xhi.z, xhi.w};
 #pragma unroll
                 for (int m = 0; m < R; ++m)
@@ -589,7 +604,7 @@ template <int MODE, int S>
 static cudaError_t run_gen(const SweepArgs &args, int d, cudaStream_t s) {
     auto kernel = k_sweep_gen<MODE, S>;
     const int aux = MODE != SWEEP_COUNT ? BT : 0;
-    const size_t smem = ((size_t)d * BT + (size_t)S * ((d + 1) * BT + aux)) * sizeof(float);
+    const size_t smem = ((S == 1 ? 0 : (size_t)d * BT) + (size_t)S * ((d + 1) * BT + aux)) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute((const void *)kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -606,7 +621,9 @@ static cudaError_t dispatch(const SweepArgs &args, int d, cudaStream_t s) {
     case 3: return run_small<3, MODE>(args, s);
     case 4: return run_small<4, MODE>(args, s);
     default:
-        return d <= 32 ? run_gen<MODE, 3>(args, d, s) : run_gen<MODE, 2>(args, d, s);
+        // shared memory: a row tile and S column stages of (d + 1) x 128 floats
+        return d <= 32 ? run_gen<MODE, 3>(args, d, s)
+                       : (d <= 128 ? run_gen<MODE, 2>(args, d, s) : run_gen<MODE, 1>(args, d, s));
     }
 }
 

@@ -72,7 +72,10 @@ constexpr int PART_BYTES = 16384;
 constexpr long long WAIT_LIMIT = 8000000000LL;   // clock cycles (about 4 s)
 constexpr int UF_CAP = 1 << 22;
 
-constexpr int F_FIRST = 1, F_TERM = 8;
+// Stage flags: the unit's first stage (its row tiles are loaded with it); the
+// end of a unit (no tiles: with one row buffer the MMA thread frees it here);
+// the end of the sweep.
+constexpr int F_FIRST = 1, F_UEND = 2, F_TERM = 8;
 
 struct TcArgs {
     const uint8_t *ua, *ub;   // row / column operand tiles, packed 128 x kbytes each
@@ -93,6 +96,7 @@ struct TcArgs {
     int group;                // column tiles per stage
     int stage_bytes;          // bytes reserved per stage (group tiles + group x BT ints)
     int tile_bytes_max;       // bytes reserved per operand tile
+    int nabuf;                // row-tile buffers: 2 (double-buffered units), or 1 for wide rows
     int srank, sworld;        // sharding: this rank takes units k * sworld + srank
 };
 
@@ -316,7 +320,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
     // to back, then G x BT ints of aux data
     const size_t abuf_bytes = (size_t)RT * a.tile_bytes_max;
     uint8_t *sA = smem;
-    uint8_t *sStage = smem + 2 * abuf_bytes;
+    const int NA = a.nabuf;
+    uint8_t *sStage = smem + (size_t)NA * abuf_bytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + (size_t)S * a.stage_bytes);
     uint64_t *b_full = bars, *b_empty = bars + TC_MAX_STAGES;
     uint64_t *a_full = bars + 2 * TC_MAX_STAGES, *a_empty = a_full + 2;
@@ -391,7 +396,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
             if (u >= sc.units) break;
             int rb, nrow, t0, t1;
             if (!tc_unit(sc, u, a.tri, lo, hi, rb, nrow, t0, t1)) continue;
-            const int ab = ua & 1;
+            const int ab = NA == 2 ? (ua & 1) : 0;
+            const int a_use = NA == 2 ? (ua >> 1) : ua;   // earlier uses of buffer ab
             bool started = false;   // this unit's row tile has been loaded
             // Stages of up to G consecutive tiles over [ts, te); the unit's row
             // tile is loaded before its first stage, so a unit whose column
@@ -400,7 +406,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                 for (int tf = ts; tf < te; tf += G) {
                     bool first = false;
                     if (!started) {
-                        if (!__all_sync(FULL, mbar_spin(smem_addr(&a_empty[ab]), ((ua >> 1) & 1) ^ 1,
+                        if (!__all_sync(FULL, mbar_spin(smem_addr(&a_empty[ab]), (a_use & 1) ^ 1,
                                                         s_abort, ctrl)))
                             return false;
                         if (lane == B_LANES + (ua % A_LANES)) {
@@ -574,6 +580,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                     }
                 }
             }
+            if (started && ok && NA == 1) {
+                // end of the unit: the MMA thread frees the one row buffer here
+                const int s = k % S;
+                ok = __all_sync(FULL, mbar_spin(smem_addr(&b_empty[s]), ((k / S) & 1) ^ 1, s_abort, ctrl));
+                if (ok && lane == 0) {
+                    Meta m;
+                    m.rb = rb;
+                    m.nrow = nrow;
+                    m.t_first = t0;
+                    m.ntiles = 0;
+                    m.flags = F_UEND;
+                    m.abuf = 0;
+                    meta[s] = m;
+                    mbar_arrive(smem_addr(&b_full[s]));
+                }
+                ++k;
+            }
             if (started) ++ua;
             if (!ok) break;
         }
@@ -587,8 +610,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
         }
         if (!ok && lane == 0) {   // let the copies already issued land before the CTA exits
             for (int j = max(0, k - S); j < k; ++j) mbar_drain(smem_addr(&b_full[j % S]), (j / S) & 1);
-            for (int j = max(0, a_issued - 2); j < a_issued; ++j)
-                mbar_drain(smem_addr(&a_full[j & 1]), (j >> 1) & 1);
+            for (int j = max(0, a_issued - NA); j < a_issued; ++j)
+                mbar_drain(smem_addr(&a_full[j % NA]), (j / NA) & 1);
         }
     } else if (warp == MMA_WARP) {
         if (lane == 0) {
@@ -617,11 +640,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                 const Meta m = meta[s];
                 if (m.flags & F_TERM) break;
                 if (m.flags & F_FIRST) {
-                    // the previous unit's row tiles have been read by every MMA issued so far
-                    if (ua > 0) umma_commit(bar_ae + 8u * ((ua - 1) & 1));
-                    if (!mbar_spin(bar_af + 8u * m.abuf, (ua >> 1) & 1, s_abort, ctrl)) break;
+                    // the previous unit's row tiles have been read by every MMA
+                    // issued so far (one buffer: freed at the unit's end marker)
+                    if (ua > 0 && NA == 2) umma_commit(bar_ae + 8u * ((ua - 1) & 1));
+                    if (!mbar_spin(bar_af + 8u * m.abuf, (NA == 2 ? (ua >> 1) : ua) & 1, s_abort, ctrl)) break;
                     ++ua;
                 }
+                if (m.flags & F_UEND) umma_commit(bar_ae);   // one buffer: free it (no tiles follow)
                 const uint64_t da0 = m.abuf ? dA1 : dA0;
                 // item (i, r): row tile r of the unit against column tiles 2i, 2i + 1;
                 // a pair of consecutive column tiles is one 256-row B operand, and
@@ -840,8 +865,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
 }
 
 // Bytes of shared memory the kernel needs.
-size_t tc_smem_bytes(int tile_bytes, int rows, int stage_bytes, int stages) {
-    return 2 * (size_t)rows * tile_bytes + (size_t)stages * stage_bytes +
+size_t tc_smem_bytes(int tile_bytes, int rows, int nabuf, int stage_bytes, int stages) {
+    return (size_t)nabuf * rows * tile_bytes + (size_t)stages * stage_bytes +
            (2 * TC_MAX_STAGES + 4 + 2 * NACC + 1) * sizeof(uint64_t) + TC_MAX_STAGES * sizeof(Meta) +
            16;
 }
@@ -876,19 +901,29 @@ cudaError_t run_tc(TcArgs a, const Layout &L, cudaStream_t s) {
     // two row blocks need room for four row tiles next to two stages of two
     // column tiles; wide operand rows keep one
     if (rows == 2 && 4 * (size_t)tile + 4 * (size_t)(tile + aux) > budget) rows = 1;
-    auto kernel = rows == 2 ? k_sweep_tc<MODE, KIND, 2> : k_sweep_tc<MODE, KIND, 1>;
-    const size_t abufs = 2 * (size_t)rows * tile;   // two buffers of a unit's row tiles
     // Few, large stages: every stage costs a round of barrier handshakes
     // between the producer, the MMA thread and all epilogue warps, so the
     // group is the largest even number of tiles (<= 32) for which two stages
-    // and the row buffers fit; what is left takes further stages.
+    // and the row buffers fit; what is left takes further stages.  Rows too
+    // wide for two row buffers next to two stages of two tiles (d = 256 on
+    // bf16 or f16: 544-byte rows, 68 KB tiles) take one row buffer, freed at
+    // the end of each unit, and stages of one tile.
+    int nabuf = 2;
+    if (2 * (size_t)rows * tile + 2 * 2 * (size_t)(tile + aux) > budget) {
+        nabuf = 1;
+        rows = 1;
+    }
+    auto kernel = rows == 2 ? k_sweep_tc<MODE, KIND, 2> : k_sweep_tc<MODE, KIND, 1>;
+    const size_t abufs = (size_t)nabuf * rows * tile;   // buffers of a unit's row tiles
     int group = TC_MAX_GROUP;
     while (group > 2 && abufs + 2 * (size_t)group * (tile + aux) > budget) group -= 2;
+    if (nabuf == 1 && abufs + 2 * (size_t)group * (tile + aux) > budget) group = 1;
+    if (abufs + 2 * (size_t)group * (tile + aux) > budget) return cudaErrorInvalidValue;
     const int stage_bytes = group * (tile + aux);
     int stages = (int)((budget - abufs) / stage_bytes);
     if (stages > TC_MAX_STAGES) stages = TC_MAX_STAGES;
     if (stages < 2) stages = 2;
-    size_t smem = tc_smem_bytes(tile, rows, stage_bytes, stages);
+    size_t smem = tc_smem_bytes(tile, rows, nabuf, stage_bytes, stages);
     if (smem < 120 * 1024) smem = 120 * 1024;   // one CTA per SM: it owns all of TMEM
     cudaError_t e = cudaFuncSetAttribute((const void *)kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -897,6 +932,7 @@ cudaError_t run_tc(TcArgs a, const Layout &L, cudaStream_t s) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     a.stages = stages;
+    a.nabuf = nabuf;
     a.group = group;
     a.stage_bytes = stage_bytes;
     a.tile_bytes_max = tile;

@@ -181,6 +181,23 @@ def test_extremes_bf16_d128():
             assert_same(g, e, f"eps={eps} {w}")
 
 
+def test_extremes_bf16_d256():
+    # all-0 and all-255 rows at d = 256: 544-byte operand rows, and the
+    # exactness bound met with equality (4 S = 2^24 after centring); eps up to
+    # 2896 keeps 2 S + thrx within 2^24 (tensor cores), larger eps leaves the
+    # data to the CUDA cores, which must agree as well
+    rng = np.random.default_rng(5)
+    P = (rng.integers(0, 2, size=(600, 256)) * 255).astype(np.float32)
+    P[:150] = rng.integers(250, 256, size=(150, 256))
+    for eps, path in ((80.0, "bf16"), (2896.0, "bf16"), (4080.0, "fp32"), (4079.0, "fp32")):
+        ref = oracle.dbscan(P, eps, 4)
+        info = {}
+        got = gpu_run(P, eps, 4, torch.bfloat16, info=info)
+        assert info["path"] == path, (eps, info)
+        for g, e, w in zip(got, ref, ("cnt", "core", "label")):
+            assert_same(g, e, f"d=256 eps={eps} {w}")
+
+
 def test_dyadic_fractional_coordinates():
     # quarter-integer coordinates are exact in float32 as well; the
     # non-integer branch of the threshold must still give "<= eps^2"
@@ -260,12 +277,17 @@ PATH_CASES = {
     # f16 operands with an f32 accumulator take two K steps
     "d11_blobs": (lambda: synth.blob_set(2_500, 11, 511, 10, 20.0, 250, 38), 60.0, 5,
                   torch.float32, {"tf32", "f16"}),
-    # the widest rows: 144 bf16/f16 elements at d = 128, 72 tf32 elements at d = 64
-    # (a range of 400 is too wide for bf16 and narrow enough for exact tf32 and f16)
+    # wide rows: 144 bf16/f16 or 136 tf32 elements at d = 128, 72 tf32 elements at
+    # d = 64 (a range of 400 is too wide for bf16 and narrow enough for exact tf32
+    # and f16)
     "d128_bf16": (lambda: synth.blob_set(2_500, 128, 255, 8, 6.0, 250, 39), 110.0, 5,
-                  torch.bfloat16, {"bf16", "f16"}),
+                  torch.bfloat16, {"bf16", "f16", "tf32"}),
     "d64_tf32_wide": (lambda: synth.blob_set(2_000, 64, 400, 8, 12.0, 200, 40), 150.0, 5,
                       torch.float32, {"tf32", "f16"}),
+    # the widest rows: 272 bf16/f16 elements at d = 256 (one row buffer and
+    # one-tile stages in the sweeps)
+    "d256_bf16": (lambda: synth.blob_set(2_000, 256, 255, 6, 5.0, 200, 42), 140.0, 5,
+                  torch.bfloat16, {"bf16", "f16"}),
     # a threshold constant of three base-2048 digits (eps^2 >= 2048^2): f16
     # operands hold at most two, tf32 takes three
     "d3_three_digits": (lambda: synth.uniform_ints(1_500, 3, 2047, 41), 2100.0, 40, torch.float32,
@@ -302,6 +324,7 @@ def test_default_path_choice():
                            (synth.uniform_ints(3000, 16, 255, 5), 4.0, "bf16"),
                            (synth.uniform_ints(3000, 12, 511, 6), 4.0, "f16"),
                            (synth.uniform_ints(3000, 128, 255, 7), 4.0, "bf16"),
+                           (synth.uniform_ints(1500, 256, 255, 10), 4.0, "bf16"),
                            (synth.uniform_ints(3000, 64, 400, 8), 4.0, "f16"),
                            (synth.uniform_ints(3000, 3, 2047, 9), 2100.0, "tf32"),
                            (synth.uniform_ints(3000, 2, 3000, 3), 4.0, "fp32"),
