@@ -93,6 +93,7 @@ Layout make_layout(int64_t n, int32_t d) {
     L.off_gbox_all = off;    off += align256(L.gbox_floats * sizeof(float));
     L.off_gbox_core = off;   off += align256(L.gbox_floats * sizeof(float));
     L.off_troot = off;       off += align256((size_t)L.ntiles * sizeof(int));
+    L.off_pivrank = off;     off += align256(512 * sizeof(int));
     L.total = off;
     return L;
 }
@@ -197,6 +198,7 @@ Work carve(void *base, const Layout &L) {
     w.btot = reinterpret_cast<int *>(b + L.off_btot);
     w.rootmin = reinterpret_cast<int *>(b + L.off_rootmin);
     w.troot = reinterpret_cast<int *>(b + L.off_troot);
+    w.pivrank = reinterpret_cast<int *>(b + L.off_pivrank);
     w.box_all = reinterpret_cast<float *>(b + L.off_box_all);
     w.box_core = reinterpret_cast<float *>(b + L.off_box_core);
     w.box_cand = reinterpret_cast<float *>(b + L.off_box_cand);
@@ -257,15 +259,17 @@ static void keep_pool(void) {
 // one kernel per tensor-core kind the call allows (ntc: the allowed paths
 // whose operand rows fit the shape); all but the path chosen on the device
 // return at once.
-//   prep 4 + 5 locality order (+1 operand staging), count 1 + ntc,
+//   prep 4 + 5 locality order (+2 pivot kernels for 3 < d <= 64, +1 operand
+//   staging), count 1 + ntc,
 //   compact 4 (+1 operand staging), union 1 tile-local + 2 CUDA-core waves
 //   + 1 compression + 6 tensor-core bands x ntc + 5 compressions, flatten 2,
 //   border (+1 operand staging) 1 + ntc, finalize 1.
-static int stage_launches(unsigned allow, int stage) {
+static int stage_launches(unsigned allow, int d, int stage) {
     const int ntc = __builtin_popcount(allow);
     const int umma = ntc > 0 ? 1 : 0;
     switch (stage) {
-    case 0: return 9 + umma;
+    // (+2: pivot renumbering and assignment of the order for 3 < d <= 64)
+    case 0: return 9 + umma + (d > 3 && d <= 64 ? 2 : 0);
     case 1: return 1 + ntc;
     case 2: return 4 + umma;
     // tile-local union, two CUDA-core waves and their compression, and per
@@ -282,6 +286,7 @@ struct ProfCall {
     cudaEvent_t ev[DBSCAN_NUM_STAGES + 1];
     int stages;       // number of stages the call ran
     unsigned allow;   // tensor-core kinds launched by the call's sweeps
+    int d;            // dimension (the order's pivot kernels run for 3 < d <= 64)
     int cull;         // 1: culled count, 2: culled union and border (box kernels)
     int fused;        // 1: the fused single-launch pipeline (one kernel)
 };
@@ -296,8 +301,9 @@ struct StageMarks {
     ProfCall call{};
     bool on = false;
     int next = 0;
-    StageMarks(cudaStream_t s, unsigned allow, int cull, int fused) {
+    StageMarks(cudaStream_t s, unsigned allow, int d, int cull, int fused) {
         call.allow = allow;
+        call.d = d;
         call.cull = cull;
         call.fused = fused;
         if (!g_prof.on) return;
@@ -329,7 +335,7 @@ static int run(const void *points, int dtype, int64_t n, int d, float eps, int m
                int32_t *labels, uint8_t *is_core, int32_t *cnt_out, void *ws, const Layout &L,
                cudaStream_t s) {
     Work w = carve(ws, L);
-    StageMarks marks(s, L.allow, L.cull + 2 * L.cull_nbr, L.fused);
+    StageMarks marks(s, L.allow, d, L.cull + 2 * L.cull_nbr, L.fused);
     if (L.fused) {
         // one launch does every stage; its time is reported under "count"
         const size_t zero = L.off_stats + 2 * DBSCAN_MAX_D * sizeof(int);   // Ctrl + min/max
@@ -714,7 +720,7 @@ int dbscan_profile_end(float *stage_ms, int32_t max_stages, int64_t *calls,
             if (c.fused)
                 launches += i == 1 ? 1 : 0;   // the one fused kernel, in the count stage
             else
-                launches += stage_launches(c.allow, i) + ((c.cull & 1) && i == 0 ? 2 : 0) +
+                launches += stage_launches(c.allow, c.d, i) + ((c.cull & 1) && i == 0 ? 2 : 0) +
                             ((c.cull & 2) && i == 2 ? 3 : 0);
         }
         for (int i = 0; i <= c.stages; ++i) cudaEventDestroy(c.ev[i]);

@@ -81,6 +81,7 @@ struct Layout {
     size_t off_box_all, off_box_core, off_box_cand;
     size_t off_gbox_all, off_gbox_core;
     size_t off_troot;     // [ntiles] ints: common root of each core tile's points, or -1
+    size_t off_pivrank;   // [512] ints: renumbered pivots of the locality order
     int64_t nscan_blocks;
     size_t total;
 };
@@ -110,6 +111,7 @@ struct Work {
     float *box_all, *box_core, *box_cand;   // [ntiles][d][min, max] tile bounding boxes
     float *gbox_all, *gbox_core;            // [ntiles / CULL_GROUP][d][min, max] group boxes
     int *troot;           // [ntiles] common root of each core tile's points, or -1 (union)
+    int *pivrank;         // [512] position of each pivot in the locality order's pivot order
 };
 
 Work carve(void *base, const Layout &L);

@@ -92,10 +92,12 @@ __host__ __device__ inline bool use_pivots(int d) { return d > PIVOT_MIN_D && d 
 constexpr int PIVOT_PPT = 4;
 constexpr int PIVOT_THREADS = 256;
 __global__ void __launch_bounds__(PIVOT_THREADS) k_pivot_assign(const void *pts, int dtype, int64_t n,
-                                                                int d, int *pid) {
+                                                                int d, const int *rank, int *pid) {
     constexpr int P = 1 << PIVOT_BITS;
     __shared__ __align__(16) float s_piv[PIVOT_DIMS * P];   // -2 p_jm at m * P + j
     __shared__ __align__(16) float s_pn[P];                  // |p_j|^2 over those coordinates
+    __shared__ int s_rank[P];                                // renumbered pivot ids
+    for (int j = threadIdx.x; j < P; j += blockDim.x) s_rank[j] = rank[j];
     for (int e = threadIdx.x; e < P * PIVOT_DIMS; e += blockDim.x) {
         const int j = e % P, m = e / P;
         const int64_t src = (int64_t)j * n / P;
@@ -155,7 +157,69 @@ __global__ void __launch_bounds__(PIVOT_THREADS) k_pivot_assign(const void *pts,
 #pragma unroll
     for (int q = 0; q < PIVOT_PPT; ++q) {
         const int64_t i = base + (int64_t)q * blockDim.x;
-        if (i < n) pid[i] = bj[q];
+        if (i < n) pid[i] = s_rank[bj[q]];
+    }
+}
+
+// Renumbering of the pivots so that pivots of one cluster are consecutive:
+// in input order consecutive pivot ids belong to different clusters, and a
+// tile that straddles two pivot groups then spans two clusters, whose box the
+// union's tile test cannot cull.  One block: pivots within 2 eps of each other
+// (over the pivot coordinates; a distance over some of the coordinates is at
+// most the full one) are joined by a shared-memory union-find, and pivot j
+// gets rank[j], its position in the order (component, index).  The order only
+// decides which points share a tile, never a result.
+// 1,024 threads: thread t takes pivot j = t % 512 against every second pivot
+// k > j (the half t / 512), its own coordinates in registers.
+__global__ void __launch_bounds__(1024) k_pivot_rank(const void *pts, int dtype, int64_t n, int d,
+                                                     float eps2, int *rank) {
+    constexpr int P = 1 << PIVOT_BITS;
+    __shared__ float s_p[PIVOT_DIMS * P];
+    __shared__ int par[P];
+    const int j = threadIdx.x % P, half = threadIdx.x / P;
+    if (half == 0) {
+        const int64_t src = (int64_t)j * n / P;
+        for (int m = 0; m < PIVOT_DIMS; ++m) s_p[m * P + j] = pivot_coord(pts, dtype, src, m, d);
+        par[j] = j;
+    }
+    __syncthreads();
+    float pj[PIVOT_DIMS];
+#pragma unroll
+    for (int m = 0; m < PIVOT_DIMS; ++m) pj[m] = s_p[m * P + j];
+    volatile int *vp = par;
+    auto find = [&](int x) {
+        for (int it = 0; it < P; ++it) {   // parents only move towards smaller roots
+            const int q = vp[x];
+            if (q == x) break;
+            x = q;
+        }
+        return x;
+    };
+    const float thr = 4.f * eps2;
+    for (int k = j + 1 + half; k < P; k += 2) {
+        float d2 = 0.f;
+#pragma unroll
+        for (int m = 0; m < PIVOT_DIMS; ++m) {
+            const float t = pj[m] - s_p[m * P + k];
+            d2 = fmaf(t, t, d2);
+        }
+        if (!(d2 <= thr)) continue;
+        for (int it = 0; it < 4 * P; ++it) {   // hook the larger root under the smaller
+            int a = find(j), b = find(k);
+            if (a == b) break;
+            if (a < b) { const int t = a; a = b; b = t; }
+            if (atomicCAS(&par[a], a, b) == a) break;
+        }
+    }
+    __syncthreads();
+    const int rj = find(j);
+    __syncthreads();
+    if (half == 0) par[j] = rj;   // every pivot's root (the smallest pivot of its component)
+    __syncthreads();
+    if (half == 0) {
+        int r = 0;
+        for (int k = 0; k < P; ++k) r += (par[k] < rj) || (par[k] == rj && k < j);
+        rank[j] = r;
     }
 }
 
@@ -301,7 +365,9 @@ cudaError_t launch_order(const void *points, int dtype, int64_t n, int d, const 
     const int blocks = (int)((n + 255) / 256);
     if (use_pivots(d)) {
         const int64_t per = (int64_t)PIVOT_THREADS * PIVOT_PPT;
-        k_pivot_assign<<<(unsigned)((n + per - 1) / per), PIVOT_THREADS, 0, s>>>(points, dtype, n, d, w.bin);
+        k_pivot_rank<<<1, 2 << PIVOT_BITS, 0, s>>>(points, dtype, n, d, L.eps2, w.pivrank);
+        k_pivot_assign<<<(unsigned)((n + per - 1) / per), PIVOT_THREADS, 0, s>>>(points, dtype, n, d,
+                                                                                  w.pivrank, w.bin);
     }
     k_order_key<<<blocks, 256, 0, s>>>(points, dtype, n, d, w.ctrl, 30 - L.order_bits, w.bin,
                                        w.hist);
