@@ -55,6 +55,9 @@ def parse():
                     help="skip timing the opt-in f16-accumulator variant")
     ap.add_argument("--no-fused", action="store_true",
                     help="small problems too take the multi-kernel path")
+    ap.add_argument("--force-path", default=None,
+                    choices=["fp32", "tf32", "bf16", "f16", "f16acc16"],
+                    help="allow only this arithmetic path (fp32 = CUDA cores)")
     return ap.parse_args()
 
 
@@ -345,6 +348,8 @@ def run_gb300(args, dist: Dist):
     binding.load()
     if args.no_fused:
         binding.dbscan_set_options(fused=0)
+    if args.force_path:
+        binding.dbscan_set_options(paths=[args.force_path])
     P = synth.generate(args.workload) if args.n is None else synth.scaled(args.workload, args.n)
     dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     x = torch.from_numpy(P).to(dev).to(dtype)
@@ -477,7 +482,7 @@ def run_gb300(args, dist: Dist):
     # The opt-in f16-accumulator variant of the f16 path (DBSCAN_PATH_F16_ACC16),
     # reported in a field of its own: it accumulates in f16, narrower than the
     # float32 the headline uses.
-    if info["path"] == "f16" and not args.no_f16acc:
+    if info["path"] == "f16" and not args.no_f16acc and not args.force_path:
         with binding.options(paths=binding.PATHS_DEFAULT | binding.PATH_BITS["f16acc16"]):
             with torch.cuda.stream(stream):
                 for _ in range(args.warmup):
@@ -508,6 +513,9 @@ def run_gb300(args, dist: Dist):
             raise RuntimeError(f"device status {binding.dbscan_strerror(st)}")
         h_ms = dist.max(sum(a.elapsed_time(b) for a, b in zip(hs, he)) / args.steps)
         h_count = h_stage_ms["count"] / max(h_calls, 1)
+        if h_info["path"] != "f16acc16":   # the opt-in path needs rows of one K = 16 MMA
+            h_ms = None
+    if info["path"] == "f16" and not args.no_f16acc and not args.force_path and h_ms is not None:
         line["f16_accumulator_optin"] = {
             "path": h_info["path"], "dtype": DTYPE_NAMES[h_info["path"]], "ms_per_step": h_ms,
             "value": dist.world * float(n) * n / (h_ms * 1e-3), "unit": UNIT,
