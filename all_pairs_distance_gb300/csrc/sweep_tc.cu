@@ -697,22 +697,36 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
                         b ^= 1u;
                     }
                     issued = issued || m.ntiles > 0;
-                } else
-                for (int i = 0; 2 * i < m.ntiles && ok; ++i, db += dpair) {
-                    const uint32_t idesc = 2 * i + 1 < m.ntiles ? idesc256 : idesc128;
-                    for (int r = 0; r < (RT == 1 ? 1 : m.nrow); ++r) {
-                        if (!(ok = mbar_spin(bar_acce + 8u * b, eph, s_abort, ctrl))) break;
+                } else {
+                    // two row blocks: row tile 0, then row tile 1 (when the unit
+                    // has one), against each pair of column tiles
+                    const uint32_t td0 = tmem, td1 = tmem + (uint32_t)ACC_COLS;
+                    const uint32_t ae0 = bar_acce, ae1 = bar_acce + 8u, af0 = bar_accf, af1 = bar_accf + 8u;
+                    const uint64_t da1 = da0 + (uint64_t)drow;
+                    for (int i = 0; 2 * i < m.ntiles; ++i, db += dpair) {
+                        const uint32_t idesc = 2 * i + 1 < m.ntiles ? idesc256 : idesc128;
+                        if (!(ok = mbar_spin(b ? ae1 : ae0, eph, s_abort, ctrl))) break;
                         tc_fence_after();
-                        const uint64_t da = da0 + (uint64_t)((uint32_t)r * drow);
-                        const uint32_t td = tmem + b * (uint32_t)ACC_COLS;
-                        for (int ks = 0; ks < ksteps; ++ks)
-                            umma<KIND>(td, da + (uint64_t)(16 * ks), db + (uint64_t)(16 * ks), idesc,
-                                       ks > 0 ? 1u : 0u);
-                        issued = true;
-                        umma_commit(bar_accf + 8u * b);
-                        eph ^= b;   // accumulator 0 is next released one phase later
+                        uint32_t td = b ? td1 : td0;
+                        umma<KIND>(td, da0, db, idesc, 0u);
+                        for (int ks = 1; ks < ksteps; ++ks)
+                            umma<KIND>(td, da0 + (uint64_t)(16 * ks), db + (uint64_t)(16 * ks), idesc, 1u);
+                        umma_commit(b ? af1 : af0);
+                        eph ^= b;
                         b ^= 1u;
+                        if (m.nrow > 1) {
+                            if (!(ok = mbar_spin(b ? ae1 : ae0, eph, s_abort, ctrl))) break;
+                            tc_fence_after();
+                            td = b ? td1 : td0;
+                            umma<KIND>(td, da1, db, idesc, 0u);
+                            for (int ks = 1; ks < ksteps; ++ks)
+                                umma<KIND>(td, da1 + (uint64_t)(16 * ks), db + (uint64_t)(16 * ks), idesc, 1u);
+                            umma_commit(b ? af1 : af0);
+                            eph ^= b;
+                            b ^= 1u;
+                        }
                     }
+                    issued = issued || m.ntiles > 0;
                 }
                 if (!ok) break;
                 if (++s == S) {
