@@ -272,10 +272,12 @@ static int stage_launches(unsigned allow, int d, int stage) {
     case 0: return 9 + umma + (d > 3 && d <= 64 ? 2 : 0);
     case 1: return 1 + ntc;
     case 2: return 4 + umma;
-    // tile-local union, two CUDA-core waves and their compression, and per
-    // tensor-core band: a launch per kind, a tile-root snapshot and (after the
-    // first) a compression
-    case 3: return 1 + 2 + 1 + UNION_BANDS * (ntc + 1) + (UNION_BANDS - 1);
+    // tile-local union, then per band on CUDA cores: the sweep, a tile-root
+    // snapshot and (after the first) a compression, and per tensor-core band:
+    // a launch per kind, a tile-root snapshot and (after the first) a
+    // compression
+    case 3: return 1 + UNION_BANDS * 2 + (UNION_BANDS - 1) + UNION_BANDS * (ntc + 1) +
+                   (UNION_BANDS - 1);
     case 4: return 2;
     case 5: return umma + 1 + ntc;
     default: return 1;

@@ -40,13 +40,7 @@ constexpr int UF_CAP = 1 << 22;  // iteration cap of union-find loops
 
 // Counters in Ctrl::unit_ctr.
 constexpr int CTR_COUNT = 0, CTR_UNION0 = 1, CTR_BORDER = 5;
-constexpr int UNION_WAVES = 2;
-// Union waves cover units [edge_w * G, edge_{w+1} * G) for a grid of G CTAs
-// (rows in ascending order, -1 = to the end); the union-find is compressed
-// between waves so that later waves mostly find equal parents in the staged
-// snapshot and never touch global memory.
-static const int kUnionWaveEdges[UNION_WAVES + 1] = {0, 2, -1};
-// Tensor-core union bands: UNION_BANDS and kUnionBandEdges in tc_schedule.h.
+// Union bands (both paths): UNION_BANDS and kUnionBandEdges in tc_schedule.h.
 
 struct SweepArgs {
     const float *rows;     // staged row points
@@ -64,6 +58,11 @@ struct SweepArgs {
     const int *candidx;    // pass 3: original index of each candidate position
     int32_t *labels;       // pass 3: labels (original order)
     int srank, sworld;     // sharding: this rank takes units ubegin + k * sworld + srank
+    const float *rbox, *cbox;   // per-tile bounding boxes of rows / columns (d x (min, max))
+    int cull;              // 1: skip column tiles whose box is eps or more from the row tile's
+    int band, blo, bhi;    // union: only column tiles t with t - rb in [blo, bhi) (-1: no limit)
+    const int *troot;      // union: common root of each tile's points, or -1; tile pairs
+                           // with one common root are skipped
 };
 
 // Position of a thread's m-th row (or column) inside a 128-point tile.  Two
@@ -164,16 +163,19 @@ __device__ __forceinline__ void row_init(const SweepArgs &a, int p, int n_rows, 
 }
 
 // aux_q: the staged parent (UNION) or label (BORDER) of column point q.
+// last (UNION): the staged parent the row was last joined with, which is in
+// the row's set for good, so further neighbours staged with it are skipped.
 template <int MODE>
 __device__ __forceinline__ void on_neighbour(const SweepArgs &a, int p, int q, bool diag,
-                                             int aux_q, int &acc) {
+                                             int aux_q, int &acc, int &last) {
     if (MODE == SWEEP_COUNT) {
         if (diag && q < p) return;        // counted from the other side
         acc += 1;
         if (q != p) atomicAdd(a.cnt + q, 1);
     } else if (MODE == SWEEP_UNION) {
         if (diag && q <= p) return;
-        if (aux_q == acc) return;         // q's parent is an ancestor of p: same set
+        if (aux_q == acc || aux_q == last) return;   // q's parent is in p's set
+        last = aux_q;
         acc = uf_unite(a.parent, acc, aux_q, a.ctrl);
     } else {
         acc = min(acc, aux_q);
@@ -195,19 +197,66 @@ __device__ __forceinline__ void flush_rows(const SweepArgs &a, int rb, int tr, i
     }
 }
 
-// Stage layout: tiles_per_stage point tiles, then (with aux) as many x BT ints.
-template <bool AUX>
-__device__ __forceinline__ void issue_stage(float *dst, const SweepArgs &a, int tfirst,
+// Stage of up to tiles_per_stage tiles given by position, tile_of(j0 + q):
+// the point tiles, then (with aux) as many x BT ints.
+template <bool AUX, typename TileOf>
+__device__ __forceinline__ void issue_tiles(float *dst, const SweepArgs &a, TileOf tile_of, int j0,
                                             int ntiles, int tile_floats, int tiles_per_stage) {
-    const float *src = a.cols + (size_t)tfirst * tile_floats;
-    const int chunks = ntiles * tile_floats / 4;
-    for (int c = threadIdx.x; c < chunks; c += THREADS) cp_async16(dst + 4 * c, src + 4 * c);
-    if (AUX) {
-        const int *asrc = a.aux + (size_t)tfirst * BT;
-        int *adst = reinterpret_cast<int *>(dst + (size_t)tiles_per_stage * tile_floats);
-        const int achunks = ntiles * BT / 4;
-        for (int c = threadIdx.x; c < achunks; c += THREADS) cp_async16(adst + 4 * c, asrc + 4 * c);
+    int *adst = reinterpret_cast<int *>(dst + (size_t)tiles_per_stage * tile_floats);
+    for (int q = 0; q < ntiles; ++q) {
+        const int t = tile_of(j0 + q);
+        const float *src = a.cols + (size_t)t * tile_floats;
+        for (int c = threadIdx.x; c < tile_floats / 4; c += THREADS)
+            cp_async16(dst + (size_t)q * tile_floats + 4 * c, src + 4 * c);
+        if (AUX)
+            for (int c = threadIdx.x; c < BT / 4; c += THREADS)
+                cp_async16(adst + q * BT + 4 * c, a.aux + (size_t)t * BT + 4 * c);
     }
+}
+
+// ---- tile culling on CUDA cores ---------------------------------------------
+// The same exact test as the tensor-core producer's (sweep_tc.cu): for integer
+// data within the exactness bound the box gaps are integers, their squared sum
+// is exact, and a column tile whose box is thrx or more (squared) from the row
+// tile's box holds no neighbour of any of its points.  A unit's column tiles
+// go KEEP_SPAN at a time: every thread tests one, and the kept ones are listed
+// in ascending order in shared memory; only those are copied and evaluated.
+constexpr int KEEP_SPAN = THREADS;
+
+// The union sweep also skips the column tiles whose points all share the row
+// tile's common root (rroot >= 0), a test that holds for any data.
+// Kept tiles of [c0, c1) (c1 - c0 <= KEEP_SPAN) into s_list; returns their
+// number.  Every thread of the block calls it.
+__device__ __forceinline__ int keep_tiles(const SweepArgs &a, int d, int c0, int c1, bool box,
+                                          const float *s_rbox, float thrx, int rroot, int *s_list,
+                                          int *s_wtot) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int t = c0 + tid;
+    bool keep = false;
+    if (t < c1) {
+        keep = !(rroot >= 0 && a.troot[t] == rroot);
+        if (keep && box) {
+            const float *bx = a.cbox + (size_t)t * 2 * d;
+            float g2 = 0.f;
+            for (int k = 0; k < d; ++k) {
+                const float gp =
+                    fmaxf(0.f, fmaxf(bx[2 * k] - s_rbox[2 * k + 1], s_rbox[2 * k] - bx[2 * k + 1]));
+                g2 = fmaf(gp, gp, g2);
+            }
+            keep = g2 < thrx;
+        }
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+    if (lane == 0) s_wtot[wid] = __popc(bal);
+    __syncthreads();
+    int base = 0, total = 0;
+    for (int w = 0; w < THREADS / 32; ++w) {
+        base += w < wid ? s_wtot[w] : 0;
+        total += s_wtot[w];
+    }
+    if (keep) s_list[base + __popc(bal & ((1u << lane) - 1u))] = t;
+    __syncthreads();
+    return total;
 }
 
 // ===========================================================================
@@ -222,6 +271,8 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
     constexpr int STAGE = CT * TILE + (AUX ? CT * BT : 0);
     extern __shared__ __align__(16) float smem[];
     __shared__ unsigned s_unit;
+    __shared__ int s_list[KEEP_SPAN], s_wtot[THREADS / 32];
+    __shared__ float s_rbox[2 * D];
 
     if (a.ctrl->tc_kind != TC_NONE) return;   // the tensor-core sweep handles this data
     const int tid = threadIdx.x;
@@ -229,6 +280,8 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
     const int n_rows = *a.n_rows, n_cols = *a.n_cols;
     if (n_rows <= 0 || n_cols <= 0) return;
     const Sched sc = make_sched(n_rows, n_cols, a.tri, a.ulo, a.uhi);
+    const bool cull = a.cull && a.ctrl->exact && a.rbox && a.cbox;
+    const float thrx = a.ctrl->thrx;
 
     for (;;) {
         if (tid == 0) s_unit = sc.ubegin + atomicAdd(a.ctr, 1u) * (unsigned)a.sworld + (unsigned)a.srank;
@@ -238,6 +291,13 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
         if (u >= sc.uend) break;
         int rb, t0, t1;
         if (!decode_unit(u, sc, a.tri, rb, t0, t1)) continue;
+        if (a.band) {
+            t0 = max(t0, rb + a.blo);
+            if (a.bhi >= 0) t1 = min(t1, rb + a.bhi);
+            if (t0 >= t1) continue;
+        }
+        const int rroot = a.troot ? a.troot[rb] : -1;
+        const bool filt = cull || rroot >= 0;
 
         // rows of this unit: packed (-2c, -2c) and thresholds
         float2 ra[R][D];
@@ -258,15 +318,28 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
             rT[0] = lo.x; rT[1] = lo.y; rT[2] = lo.z; rT[3] = lo.w;
             rT[4] = hi.x; rT[5] = hi.y; rT[6] = hi.z; rT[7] = hi.w;
         }
-        int acc[R];
+        int acc[R], last[R];
 #pragma unroll
-        for (int m = 0; m < R; ++m) row_init<MODE>(a, rb * BT + slot_of(tr, m), n_rows, acc[m]);
+        for (int m = 0; m < R; ++m) {
+            row_init<MODE>(a, rb * BT + slot_of(tr, m), n_rows, acc[m]);
+            last[m] = -1;
+        }
+        if (cull) {
+            for (int e = tid; e < 2 * D; e += THREADS) s_rbox[e] = a.rbox[(size_t)rb * 2 * D + e];
+            __syncthreads();
+        }
 
-        const int nst = (t1 - t0 + CT - 1) / CT;
+      // column tiles in spans: all of [t0, t1) at once, or KEEP_SPAN at a time
+      // listing the kept ones when tiles are skipped
+      for (int c0 = t0; c0 < t1; c0 = filt ? c0 + KEEP_SPAN : t1) {
+        const int c1 = filt ? min(c0 + KEEP_SPAN, t1) : t1;
+        const int nk = filt ? keep_tiles(a, D, c0, c1, cull, s_rbox, thrx, rroot, s_list, s_wtot)
+                            : c1 - c0;
+        auto tile_of = [&](int j) { return filt ? s_list[j] : c0 + j; };
+        const int nst = (nk + CT - 1) / CT;
 #pragma unroll
         for (int s = 0; s < S - 1; ++s) {
-            if (s < nst) issue_stage<AUX>(smem + s * STAGE, a, t0 + s * CT,
-                                          min(CT, t1 - (t0 + s * CT)), TILE, CT);
+            if (s < nst) issue_tiles<AUX>(smem + s * STAGE, a, tile_of, s * CT, min(CT, nk - s * CT), TILE, CT);
             cp_async_commit();
         }
         for (int g = 0; g < nst; ++g) {
@@ -274,15 +347,15 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
             __syncthreads();
             {
                 int gn = g + S - 1;
-                if (gn < nst) issue_stage<AUX>(smem + (gn % S) * STAGE, a, t0 + gn * CT,
-                                               min(CT, t1 - (t0 + gn * CT)), TILE, CT);
+                if (gn < nst)
+                    issue_tiles<AUX>(smem + (gn % S) * STAGE, a, tile_of, gn * CT, min(CT, nk - gn * CT), TILE, CT);
                 cp_async_commit();
             }
             const float *sb = smem + (g % S) * STAGE;
             const int *saux = reinterpret_cast<const int *>(sb + CT * TILE);
-            const int ntile = min(CT, t1 - (t0 + g * CT));
+            const int ntile = min(CT, nk - g * CT);
             for (int q = 0; q < ntile; ++q) {
-                const int tile = t0 + g * CT + q;
+                const int tile = tile_of(g * CT + q);
                 const float *st = sb + q * TILE;
                 float xc[D + 1][C];
 #pragma unroll
@@ -322,7 +395,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
                             if (v < rT[m]) {
                                 const int slot = slot_of(tc, c);
                                 on_neighbour<MODE>(a, p, tile * BT + slot, diag,
-                                                   AUX ? saux[q * BT + slot] : 0, acc[m]);
+                                                   AUX ? saux[q * BT + slot] : 0, acc[m], last[m]);
                             }
                         }
                     }
@@ -330,6 +403,8 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
             }
         }
         cp_async_wait<0>();
+        __syncthreads();   // every thread is done with the stages and the list
+      }
         flush_rows<MODE>(a, rb, tr, n_rows, acc);
     }
 }
@@ -350,6 +425,8 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
     const int STAGE = TILE + (AUX ? BT : 0);
     float *rowbuf = smem;                                 // D * BT floats: -2 c of the row tile
     float *stages = smem + (ROWS_GLOBAL ? 0 : D * BT);    // S * STAGE floats
+    __shared__ int s_list[KEEP_SPAN], s_wtot[THREADS / 32];
+    __shared__ float s_rbox[2 * CULL_MAX_D];
 
     if (a.ctrl->tc_kind != TC_NONE) return;   // the tensor-core sweep handles this data
     const int tid = threadIdx.x;
@@ -357,6 +434,8 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
     const int n_rows = *a.n_rows, n_cols = *a.n_cols;
     if (n_rows <= 0 || n_cols <= 0) return;
     const Sched sc = make_sched(n_rows, n_cols, a.tri, a.ulo, a.uhi);
+    const bool cull = a.cull && a.ctrl->exact && a.rbox && a.cbox && D <= CULL_MAX_D;
+    const float thrx = a.ctrl->thrx;
 
     for (;;) {
         if (tid == 0) s_unit = sc.ubegin + atomicAdd(a.ctr, 1u) * (unsigned)a.sworld + (unsigned)a.srank;
@@ -366,6 +445,13 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
         if (u >= sc.uend) break;
         int rb, t0, t1;
         if (!decode_unit(u, sc, a.tri, rb, t0, t1)) continue;
+        if (a.band) {
+            t0 = max(t0, rb + a.blo);
+            if (a.bhi >= 0) t1 = min(t1, rb + a.bhi);
+            if (t0 >= t1) continue;
+        }
+        const int rroot = a.troot ? a.troot[rb] : -1;
+        const bool filt = cull || rroot >= 0;
 
         const float *rowsrc = ROWS_GLOBAL ? a.rows + (size_t)rb * TILE : rowbuf;
         const float rscale = ROWS_GLOBAL ? -2.f : 1.f;
@@ -381,15 +467,29 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
             rT[0] = lo.x; rT[1] = lo.y; rT[2] = lo.z; rT[3] = lo.w;
             rT[4] = hi.x; rT[5] = hi.y; rT[6] = hi.z; rT[7] = hi.w;
         }
-        int acc[R];
+        int acc[R], last[R];
 #pragma unroll
-        for (int m = 0; m < R; ++m) row_init<MODE>(a, rb * BT + slot_of(tr, m), n_rows, acc[m]);
+        for (int m = 0; m < R; ++m) {
+            row_init<MODE>(a, rb * BT + slot_of(tr, m), n_rows, acc[m]);
+            last[m] = -1;
+        }
+        if (cull) {
+            for (int e = tid; e < 2 * D; e += THREADS) s_rbox[e] = a.rbox[(size_t)rb * 2 * D + e];
+            __syncthreads();
+        }
 
-        const int nst = t1 - t0;   // one tile per stage
+      // column tiles in spans: all of [t0, t1) at once, or KEEP_SPAN at a time
+      // listing the kept ones when tiles are skipped
+      for (int c0 = t0; c0 < t1; c0 = filt ? c0 + KEEP_SPAN : t1) {
+        const int c1 = filt ? min(c0 + KEEP_SPAN, t1) : t1;
+        const int nk = filt ? keep_tiles(a, D, c0, c1, cull, s_rbox, thrx, rroot, s_list, s_wtot)
+                            : c1 - c0;
+        auto tile_of = [&](int j) { return filt ? s_list[j] : c0 + j; };
+        const int nst = nk;   // one tile per stage
         if constexpr (S > 1) {
 #pragma unroll
             for (int s = 0; s < S - 1; ++s) {
-                if (s < nst) issue_stage<AUX>(stages + s * STAGE, a, t0 + s, 1, TILE, 1);
+                if (s < nst) issue_tiles<AUX>(stages + s * STAGE, a, tile_of, s, 1, TILE, 1);
                 cp_async_commit();
             }
         }
@@ -398,16 +498,16 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
                 cp_async_wait<S - 2>();
                 __syncthreads();
                 int gn = g + S - 1;
-                if (gn < nst) issue_stage<AUX>(stages + (gn % S) * STAGE, a, t0 + gn, 1, TILE, 1);
+                if (gn < nst) issue_tiles<AUX>(stages + (gn % S) * STAGE, a, tile_of, gn, 1, TILE, 1);
                 cp_async_commit();
             } else {
                 __syncthreads();   // every thread is done with the previous tile
-                issue_stage<AUX>(stages, a, t0 + g, 1, TILE, 1);
+                issue_tiles<AUX>(stages, a, tile_of, g, 1, TILE, 1);
                 cp_async_commit();
                 cp_async_wait<0>();
                 __syncthreads();
             }
-            const int tile = t0 + g;
+            const int tile = tile_of(g);
             const float *st = stages + (g % S) * STAGE;
             const int *saux = reinterpret_cast<const int *>(st + TILE);
             float v[R][C];
@@ -452,12 +552,14 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
                         if (v[m][c] < rT[m]) {
                             const int slot = slot_of(tc, c);
                             on_neighbour<MODE>(a, p, tile * BT + slot, diag, AUX ? saux[slot] : 0,
-                                               acc[m]);
+                                               acc[m], last[m]);
                         }
                 }
             }
         }
         cp_async_wait<0>();
+        __syncthreads();   // every thread is done with the stages and the list
+      }
         flush_rows<MODE>(a, rb, tr, n_rows, acc);
     }
 }
@@ -540,8 +642,8 @@ __global__ void k_compress(Ctrl *ctrl, int *parent, int tc) {
 // union tile pair whose row and column tiles share one common root holds no
 // pair the union could still join, and the sweep skips it; sets only merge,
 // so a snapshot taken before a band stays safe through it.
-__global__ void k_tile_roots(const Ctrl *ctrl, const int *parent, int *troot) {
-    if (ctrl->tc_kind == TC_NONE) return;
+__global__ void k_tile_roots(const Ctrl *ctrl, const int *parent, int *troot, int tc) {
+    if ((ctrl->tc_kind != TC_NONE) != (tc != 0)) return;
     const int n_core = ctrl->n_core;
     const int nt = (n_core + BT - 1) / BT;
     const int lane = threadIdx.x & 31;
@@ -634,6 +736,7 @@ cudaError_t launch_count(const Work &w, const Layout &L, cudaStream_t s) {
     a.cols = w.staged_all; a.n_cols = &w.ctrl->n_all;
     a.tri = 1; a.ulo = 0; a.uhi = -1;
     a.ctr = &w.ctrl->unit_ctr[CTR_COUNT]; a.ctrl = w.ctrl; a.cnt = w.cnt;
+    a.rbox = w.box_all; a.cbox = w.box_all; a.cull = L.cull;
     cudaError_t e = dispatch<SWEEP_COUNT>(a, L.d, s);
     if (e != cudaSuccess) return e;
     return launch_count_tc(w, L, s);
@@ -645,6 +748,7 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
     a.rows = w.staged_core; a.rowT = w.T_core; a.n_rows = &w.ctrl->n_core;
     a.cols = w.staged_core; a.n_cols = &w.ctrl->n_core; a.aux = w.parent;
     a.tri = 1; a.ctrl = w.ctrl; a.parent = w.parent;
+    a.rbox = w.box_core; a.cbox = w.box_core; a.cull = L.cull_nbr;
     const int grid = persistent_ctas((const void *)k_compress, 256, 0);
     const size_t lsmem = (size_t)(L.d + 1) * BT * sizeof(float) + BT * sizeof(int);
     if (cudaFuncSetAttribute((const void *)k_local_union,
@@ -658,33 +762,39 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
     if (lgrid > L.ntiles) lgrid = L.ntiles;
     if (lgrid < 1) lgrid = 1;
     k_local_union<<<(unsigned)lgrid, BT, lsmem, s>>>(w.ctrl, w.staged_core, w.T_core, L.d, w.parent);
-    // CUDA-core path (its kernels return at once when a tensor-core path was chosen)
-    for (int wv = 0; wv < UNION_WAVES; ++wv) {
-        a.ulo = kUnionWaveEdges[wv];
-        a.uhi = kUnionWaveEdges[wv + 1];
-        a.ctr = &w.ctrl->unit_ctr[CTR_UNION0 + wv];
-        cudaError_t e = dispatch<SWEEP_UNION>(a, L.d, s);
-        if (e != cudaSuccess) return e;
-        if (wv + 1 < UNION_WAVES) {
-            k_compress<<<grid, 256, 0, s>>>(w.ctrl, w.parent, 0);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        }
-    }
-    // Tensor-core path by bands of tile distance from the diagonal, nearest
+    // Both paths go by bands of tile distance from the diagonal, nearest
     // first, compressed between bands: in locality order most neighbour pairs
     // lie near the diagonal, so the far bands find merged roots in their
     // staged parent snapshots and skip their pairs without a global access.
     // Each band also skips the tile pairs whose tiles share one root (a
     // snapshot per band, k_tile_roots; the tile-local union leaves every
-    // parent a root, so the first snapshot needs no compression).
+    // parent a root, so the first snapshot needs no compression).  The
+    // kernels of the path not taken return at once.
     const unsigned rgrid = (unsigned)((L.ntiles + 7) / 8);
+    // CUDA-core path
+    a.ulo = 0; a.uhi = -1;
+    a.band = 1; a.troot = w.troot;
+    for (int bd = 0; bd < UNION_BANDS; ++bd) {
+        cudaError_t e;
+        if (bd > 0) {
+            k_compress<<<grid, 256, 0, s>>>(w.ctrl, w.parent, 0);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+        k_tile_roots<<<rgrid, 256, 0, s>>>(w.ctrl, w.parent, w.troot, 0);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        a.blo = kUnionBandEdges[bd];
+        a.bhi = kUnionBandEdges[bd + 1];
+        a.ctr = &w.ctrl->unit_ctr[CTR_UNION0 + bd];
+        if ((e = dispatch<SWEEP_UNION>(a, L.d, s)) != cudaSuccess) return e;
+    }
+    // tensor-core path
     for (int bd = 0; bd < UNION_BANDS; ++bd) {
         cudaError_t e;
         if (bd > 0) {
             k_compress<<<grid, 256, 0, s>>>(w.ctrl, w.parent, 1);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
-        k_tile_roots<<<rgrid, 256, 0, s>>>(w.ctrl, w.parent, w.troot);
+        k_tile_roots<<<rgrid, 256, 0, s>>>(w.ctrl, w.parent, w.troot, 1);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         e = launch_union_tc_band(w, L, bd, kUnionBandEdges[bd], kUnionBandEdges[bd + 1], s);
         if (e != cudaSuccess) return e;
@@ -722,6 +832,7 @@ cudaError_t launch_border(const Work &w, const Layout &L, int32_t *labels, cudaS
     a.tri = 0; a.ulo = 0; a.uhi = -1;
     a.ctr = &w.ctrl->unit_ctr[CTR_BORDER]; a.ctrl = w.ctrl;
     a.candidx = w.candidx; a.labels = labels;
+    a.rbox = w.box_cand; a.cbox = w.box_core; a.cull = L.cull_nbr;
     cudaError_t e = dispatch<SWEEP_BORDER>(a, L.d, s);
     if (e != cudaSuccess) return e;
     return launch_border_tc(w, L, labels, s);

@@ -407,3 +407,36 @@ def test_row_units_match_oracle(name, rows):
     assert_same(label, label_ref, f"{name} [rows {rows}] labels")
     assert_same(core_c, core_ref, f"{name} [rows {rows}] culled core flags")
     assert_same(label_c, label_ref, f"{name} [rows {rows}] culled labels")
+
+
+SPAN_CASES = {
+    # more than 256 column tiles (the CUDA-core sweeps test the boxes of at most
+    # 256 column tiles at a time): every span boundary of the union and border
+    # sweeps, and of the count sweep when the caller asks for culling
+    "d3_41k": (lambda: synth.scaled("blobs_1m_d3", 41_003, seed=61), 10.0, 8),
+    "d2_40k": (lambda: synth.scaled("blobs_100k_d2", 40_001, seed=62), 20.0, 10),
+    "d8_34k": (lambda: _blobs(34_000, 8, 255, 40, 6.0, 3_400, 63), 14.0, 5),
+    # fractional coordinates: no exact test, so no tile is skipped
+    "d3_fractional_34k": (lambda: synth.scaled("blobs_1m_d3", 34_001, seed=64) * np.float32(0.5),
+                          5.0, 8),
+}
+
+
+@pytest.mark.parametrize("culled", [False, True])
+@pytest.mark.parametrize("name", sorted(SPAN_CASES))
+def test_cuda_core_culling_spans(name, culled):
+    make, eps, min_pts = SPAN_CASES[name]
+    P = make()
+    assert len(P) > 256 * 128
+    cnt_ref, core_ref, label_ref = oracle.dbscan(P, eps, min_pts)
+    with binding.options(paths=["fp32"]):
+        if culled:
+            core, label = gpu_run_culled(P, eps, min_pts)
+        else:
+            info = {}
+            cnt, core, label = gpu_run(P, eps, min_pts, info=info)
+            assert info["path"] == "fp32"
+            assert_same(cnt, cnt_ref, f"{name} counts")
+    assert_same(core, core_ref, f"{name} core flags")
+    assert_same(label, label_ref, f"{name} labels")
+    assert core_ref.sum() > 0 and (label_ref == -1).sum() > 0
