@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-culled", action="store_true")
     ap.add_argument("--no-f16acc", action="store_true",
                     help="skip timing the opt-in f16-accumulator variant")
+    ap.add_argument("--no-ffma", action="store_true",
+                    help="skip timing the same call on CUDA cores only (fp32 FFMA)")
     ap.add_argument("--no-fused", action="store_true",
                     help="small problems too take the multi-kernel path")
     ap.add_argument("--force-path", default=None,
@@ -479,52 +481,74 @@ def run_gb300(args, dist: Dist):
                                   "(identical labels); not an all-pairs evaluation, so no "
                                   "pair-evals/s figure"}
 
-    # The opt-in f16-accumulator variant of the f16 path (DBSCAN_PATH_F16_ACC16),
-    # reported in a field of its own: it accumulates in f16, narrower than the
-    # float32 the headline uses.
-    if info["path"] == "f16" and not args.no_f16acc and not args.force_path:
-        with binding.options(paths=binding.PATHS_DEFAULT | binding.PATH_BITS["f16acc16"]):
+    def timed_variant(paths, step_fn=step):
+        """Mean ms of args.steps calls with only `paths` allowed (warm-up and
+        L2 flushes as for the headline), the stage times of a second pass, and
+        the path the call took."""
+        with binding.options(paths=paths):
             with torch.cuda.stream(stream):
                 for _ in range(args.warmup):
                     flush.zero_()
-                    step()
+                    step_fn()
             torch.cuda.synchronize()
-            hs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-            he = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+            vs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+            ve = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
             dist.barrier()
             with torch.cuda.stream(stream):
                 for k in range(args.steps):
                     flush.zero_()
-                    hs[k].record(stream)
-                    step()
-                    he[k].record(stream)
+                    vs[k].record(stream)
+                    step_fn()
+                    ve[k].record(stream)
             torch.cuda.synchronize()
             dist.barrier()
             binding.dbscan_profile_begin()
             with torch.cuda.stream(stream):
                 for k in range(args.steps):
                     flush.zero_()
-                    step()
+                    step_fn()
             torch.cuda.synchronize()
-            h_stage_ms, h_calls, _ = binding.dbscan_profile_end()
-            h_info = binding.dbscan_workspace_info(ws)
+            v_stage_ms, v_calls, _ = binding.dbscan_profile_end()
+            v_info = binding.dbscan_workspace_info(ws)
         st = binding.dbscan_workspace_status(ws)
         if st != 0:
             raise RuntimeError(f"device status {binding.dbscan_strerror(st)}")
-        h_ms = dist.max(sum(a.elapsed_time(b) for a, b in zip(hs, he)) / args.steps)
-        h_count = h_stage_ms["count"] / max(h_calls, 1)
-        if h_info["path"] != "f16acc16":   # the opt-in path needs rows of one K = 16 MMA
-            h_ms = None
-    if info["path"] == "f16" and not args.no_f16acc and not args.force_path and h_ms is not None:
-        line["f16_accumulator_optin"] = {
-            "path": h_info["path"], "dtype": DTYPE_NAMES[h_info["path"]], "ms_per_step": h_ms,
-            "value": dist.world * float(n) * n / (h_ms * 1e-3), "unit": UNIT,
-            "count_ms": h_count,
-            "count_frac_of_tensor_peak": count_flops(n, d) / (h_count * 1e-3) / 1e12 /
-                                         roofline["peak"],
-            "note": "opt-in DBSCAN_PATH_F16_ACC16: f16 operands and an f16 accumulator (one K = 16 "
-                    "MMA per tile pair); identical results here, but narrower than the float32 "
-                    "accumulation of the headline, whose exactness NVIDIA does not document"}
+        v_ms = dist.max(sum(a.elapsed_time(b) for a, b in zip(vs, ve)) / args.steps)
+        return v_ms, {k: v / max(v_calls, 1) for k, v in v_stage_ms.items()}, v_info
+
+    # The opt-in f16-accumulator variant of the f16 path (DBSCAN_PATH_F16_ACC16),
+    # reported in a field of its own: it accumulates in f16, narrower than the
+    # float32 the headline uses.
+    if info["path"] == "f16" and not args.no_f16acc and not args.force_path:
+        h_ms, h_stages, h_info = timed_variant(binding.PATHS_DEFAULT | binding.PATH_BITS["f16acc16"])
+        if h_info["path"] == "f16acc16":   # the opt-in path needs rows of one K = 16 MMA
+            h_count = h_stages["count"]
+            line["f16_accumulator_optin"] = {
+                "path": h_info["path"], "dtype": DTYPE_NAMES[h_info["path"]], "ms_per_step": h_ms,
+                "value": dist.world * float(n) * n / (h_ms * 1e-3), "unit": UNIT,
+                "count_ms": h_count,
+                "count_frac_of_tensor_peak": count_flops(n, d) / (h_count * 1e-3) / 1e12 /
+                                             roofline["peak"],
+                "note": "opt-in DBSCAN_PATH_F16_ACC16: f16 operands and an f16 accumulator (one K "
+                        "= 16 MMA per tile pair); identical results here, but narrower than the "
+                        "float32 accumulation of the headline, whose exactness NVIDIA does not "
+                        "document"}
+
+    # The same call on CUDA cores only (fp32 FFMA in every sweep), the path the
+    # library takes for data the exact operand encoding cannot hold: its own
+    # time and its count sweep against the FP32 FMA roofline.
+    if info["path"] != "fp32" and not args.no_ffma and not args.force_path:
+        f_ms, f_stages, f_info = timed_variant(["fp32"])
+        f_roof = roofline_fields(f_info, n, d, f_stages["count"], peaks, sms, max_mhz)
+        line["ffma_path"] = {
+            "path": f_info["path"], "dtype": DTYPE_NAMES[f_info["path"]], "ms_per_step": f_ms,
+            "value": dist.world * float(n) * n / (f_ms * 1e-3), "unit": UNIT,
+            "stages_ms": f_stages,
+            "count_pair_evals_per_s": float(n) * n / (f_stages["count"] * 1e-3),
+            "roofline": {k: f_roof[k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                                 "kernel", "peak_source")},
+            "note": "every sweep on CUDA cores (fp32 FFMA, float32 throughout), selected with "
+                    "dbscan_set_options(paths = 0); same results"}
 
     if not args.no_e2e:
         ph = torch.from_numpy(P).to(dtype).pin_memory()
