@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sweep_tc(TcArgs a) {
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const int lo = a.band ? a.blo : 0, hi = a.band ? a.bhi : -1;
-    const TcSched sc = tc_sched(n_rows, n_cols, a.tri, lo, hi, RT);
+    const TcSched sc = tc_sched(n_rows, n_cols, a.tri, lo, hi, RT, tc_chunk(MODE == SWEEP_UNION && a.band, hi, n_cols));
 
     if (warp == PRODUCER_WARP) {
         // The whole warp walks the schedule; the copies of consecutive stages

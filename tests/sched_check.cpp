@@ -19,7 +19,7 @@ static bool run(int mode, int n_rows, int n_cols, int rt) {
     for (int bd = 0; bd < nb; ++bd) {
         const int lo = mode == UNION ? kUnionBandEdges[bd] : 0;
         const int hi = mode == UNION ? kUnionBandEdges[bd + 1] : -1;
-        const TcSched s = tc_sched(n_rows, n_cols, tri, lo, hi, rt);
+        const TcSched s = tc_sched(n_rows, n_cols, tri, lo, hi, rt, tc_chunk(mode == UNION, hi, n_cols));
         for (unsigned u = 0; u < s.units; ++u) {
             int rb, nrow, t0, t1;
             if (!tc_unit(s, u, tri, lo, hi, rb, nrow, t0, t1)) continue;
