@@ -328,19 +328,19 @@ __global__ void __launch_bounds__(FT) k_fused(FusedArgs a) {
     }
     if (!grid_sync(ctrl, nb)) return;
 
-    // ---- union: core-core pairs of the upper triangle, in two rounds ------------
+    // ---- union: core-core pairs of the upper triangle, in two passes ------------
     // In input order every tile pair holds pairs of every cluster, and hooking
     // roots in arbitrary index order grows long parent chains, each step of a
-    // find an L2 round trip.  Round 0 therefore only hooks: for every core-core
+    // find an L2 round trip.  Pass 0 therefore only hooks: for every core-core
     // neighbour pair the larger index's parent takes the smaller index by
     // atomicMin (no finds; parent[x] <= x still holds, and every link is a
     // neighbour pair).  Every core's parent is then compressed to its root.
-    // Round 1 unites the sets of every core-core neighbour pair, staging the
+    // Pass 1 unites the sets of every core-core neighbour pair, staging the
     // column tile's compressed parents in shared memory and skipping each pair
     // whose two sides already had one root (sets only merge, so such a pair
-    // stays joined); after round 0 most pairs are skipped.
+    // stays joined); after pass 0 most pairs are skipped.
     int *s_par = s_aux + FT;
-    for (int round = 0; round < 2; ++round) {
+    for (int pass = 0; pass < 2; ++pass) {
         for (int u = blockIdx.x; u < npairs; u += nb) {
             int rb, cb;
             tri_pair(u, nt, rb, cb);
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(FT) k_fused(FusedArgs a) {
             const int p = rb * FT + tid;
             if (p < n && a.cnt[p] >= a.min_pts) {
                 const float Ti = a.T[p];
-                if (round == 0) {
+                if (pass == 0) {
                     int lo = p;   // the smallest neighbour index of this row so far
                     for (int j = (rb == cb ? tid + 1 : 0); j < FT; ++j) {
                         if (!s_aux[j] || !(pair_value<D>(r, s_row, s_col, d, j) < Ti)) continue;
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(FT) k_fused(FusedArgs a) {
             __syncthreads();
         }
         if (!grid_sync(ctrl, nb)) return;
-        if (round == 0) {   // compress: every core position points at its root
+        if (pass == 0) {   // compress: every core position points at its root
             for (int i = blockIdx.x * FT + tid; i < n; i += nb * FT)
                 if (a.cnt[i] >= a.min_pts) __stcg(a.parent + i, f_find(a.parent, i, ctrl));
             if (!grid_sync(ctrl, nb)) return;

@@ -134,13 +134,13 @@ def test_fused_graph_replay_follows_the_buffers():
     labels = torch.empty(len(sets[0]), dtype=torch.int32, device="cuda")
     core = torch.empty(len(sets[0]), dtype=torch.uint8, device="cuda")
     with torch.cuda.stream(stream), binding.options(graphs=1):
-        for rnd in range(4):
-            P = sets[rnd % 2]
+        for call in range(4):
+            P = sets[call % 2]
             x.copy_(torch.from_numpy(P).to("cuda"))
             binding.dbscan_fit_ex(x, 20.0, 10, labels=labels, is_core=core, workspace=ws,
                                   stream=stream)
             assert binding.dbscan_workspace_status(ws, stream) == 0
             stream.synchronize()
             _, core_ref, label_ref = oracle.dbscan(P, 20.0, 10)
-            assert_same(core.cpu().numpy(), core_ref, f"round {rnd} core flags")
-            assert_same(labels.cpu().numpy(), label_ref, f"round {rnd} labels")
+            assert_same(core.cpu().numpy(), core_ref, f"call {call} core flags")
+            assert_same(labels.cpu().numpy(), label_ref, f"call {call} labels")

@@ -30,17 +30,17 @@ def test_replay_follows_the_buffers(case):
     core = torch.empty(len(sets[0]), dtype=torch.uint8, device="cuda")
     with torch.cuda.stream(stream), binding.options(graphs=1):
         # the same arguments four times (captured once, then replayed), the
-        # input overwritten in place between rounds
-        for rnd in range(4):
-            P = sets[rnd % 2]
+        # input overwritten in place between calls
+        for call in range(4):
+            P = sets[call % 2]
             x.copy_(torch.from_numpy(P).to("cuda").to(dt))
             fit(x, eps, mp, labels=labels, is_core=core, workspace=ws, stream=stream)
             st = binding.dbscan_workspace_status(ws, stream)
             assert st == 0, binding.dbscan_strerror(st)
             stream.synchronize()
             _, core_ref, label_ref = oracle.dbscan(P, eps, mp)
-            assert_same(core.cpu().numpy(), core_ref, f"{case} round {rnd} core flags")
-            assert_same(labels.cpu().numpy(), label_ref, f"{case} round {rnd} labels")
+            assert_same(core.cpu().numpy(), core_ref, f"{case} call {call} core flags")
+            assert_same(labels.cpu().numpy(), label_ref, f"{case} call {call} labels")
 
 
 def test_replay_and_direct_launches_agree():
@@ -71,12 +71,12 @@ def test_graph_cache_evicts_beyond_its_capacity():
     outs = [(torch.empty(len(P), dtype=torch.int32, device="cuda"),
              torch.empty(len(P), dtype=torch.uint8, device="cuda")) for _ in range(20)]
     with torch.cuda.stream(stream), binding.options(graphs=1):
-        for rnd in range(2):
+        for sweep in range(2):
             for lab, core in outs:   # 20 keys (output pointers differ)
                 lab.fill_(-7)
                 binding.dbscan_fit_ex(x, 20.0, 10, labels=lab, is_core=core, workspace=ws,
                                       stream=stream)
             stream.synchronize()
             for lab, core in outs:
-                assert_same(lab.cpu().numpy(), label_ref, f"round {rnd} labels")
-                assert_same(core.cpu().numpy(), core_ref, f"round {rnd} core flags")
+                assert_same(lab.cpu().numpy(), label_ref, f"sweep {sweep} labels")
+                assert_same(core.cpu().numpy(), core_ref, f"sweep {sweep} core flags")
