@@ -584,6 +584,10 @@ __device__ __forceinline__ int sm_find(volatile int *sp, int x) {
     return x;
 }
 
+// DMAX > 0 (d <= DMAX): the thread's own point, scaled by -2, sits in
+// registers, so every FMA reads one shared-memory word instead of two (the
+// products and their order are those of the generic form).
+template <int DMAX>
 __global__ void k_local_union(const Ctrl *ctrl, const float *staged, const float *T, int d,
                               int *parent) {
     extern __shared__ float s_pts[];   // (d + 1) * BT staged floats, then BT parents
@@ -601,6 +605,11 @@ __global__ void k_local_union(const Ctrl *ctrl, const float *staged, const float
         __syncthreads();
         if (i < nv) {
             const float Ti = T[base + i];
+            float ri[DMAX > 0 ? DMAX : 1];
+            if constexpr (DMAX > 0) {
+#pragma unroll
+                for (int k = 0; k < DMAX; ++k) ri[k] = k < d ? -2.f * s_pts[(size_t)k * BT + i] : 0.f;
+            }
             // pairs (i, i + sh mod BT), sh = 1..63, and sh = 64 for i < 64: every
             // unordered pair of the tile once, 63 or 64 per thread
             const int shmax = i < BT / 2 ? BT / 2 : BT / 2 - 1;
@@ -608,8 +617,14 @@ __global__ void k_local_union(const Ctrl *ctrl, const float *staged, const float
                 const int j = (i + sh) & (BT - 1);
                 if (j >= nv) continue;
                 float v = s_pts[(size_t)d * BT + j];
-                for (int k = 0; k < d; ++k)
-                    v = fmaf(-2.f * s_pts[(size_t)k * BT + i], s_pts[(size_t)k * BT + j], v);
+                if constexpr (DMAX > 0) {
+#pragma unroll
+                    for (int k = 0; k < DMAX; ++k)
+                        if (k < d) v = fmaf(ri[k], s_pts[(size_t)k * BT + j], v);
+                } else {
+                    for (int k = 0; k < d; ++k)
+                        v = fmaf(-2.f * s_pts[(size_t)k * BT + i], s_pts[(size_t)k * BT + j], v);
+                }
                 if (!(v < Ti)) continue;
                 int ra = i, rb = j;
                 for (int it = 0; it < 2 * BT; ++it) {
@@ -751,17 +766,19 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
     a.rbox = w.box_core; a.cbox = w.box_core; a.cull = L.cull_nbr;
     const int grid = persistent_ctas((const void *)k_compress, 256, 0);
     const size_t lsmem = (size_t)(L.d + 1) * BT * sizeof(float) + BT * sizeof(int);
-    if (cudaFuncSetAttribute((const void *)k_local_union,
+    auto local = L.d <= 4 ? k_local_union<4>
+                          : (L.d <= 16 ? k_local_union<16> : (L.d <= 64 ? k_local_union<64> : k_local_union<0>));
+    if (cudaFuncSetAttribute((const void *)local,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lsmem) != cudaSuccess)
         return cudaGetLastError();
     int dev = 0, sms = 1, per = 1;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, (const void *)k_local_union, BT, lsmem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, (const void *)local, BT, lsmem);
     int64_t lgrid = (int64_t)sms * (per < 1 ? 1 : per);
     if (lgrid > L.ntiles) lgrid = L.ntiles;
     if (lgrid < 1) lgrid = 1;
-    k_local_union<<<(unsigned)lgrid, BT, lsmem, s>>>(w.ctrl, w.staged_core, w.T_core, L.d, w.parent);
+    local<<<(unsigned)lgrid, BT, lsmem, s>>>(w.ctrl, w.staged_core, w.T_core, L.d, w.parent);
     // Both paths go by bands of tile distance from the diagonal, nearest
     // first, compressed between bands: in locality order most neighbour pairs
     // lie near the diagonal, so the far bands find merged roots in their
