@@ -37,7 +37,7 @@ PATHS_DEFAULT = 1 | 2 | 4
 
 class Options(ctypes.Structure):
     _fields_ = [("paths", ctypes.c_uint32), ("rows", ctypes.c_int32 * 3),
-                ("graphs", ctypes.c_int32), ("fused", ctypes.c_int32)]
+                ("graphs", ctypes.c_int32), ("fused", ctypes.c_int32), ("cull", ctypes.c_int32)]
 
 
 class DbscanError(RuntimeError):
@@ -126,15 +126,17 @@ def dbscan_get_options() -> dict:
     o = Options()
     _check(load().dbscan_get_options(ctypes.byref(o)), "dbscan_get_options")
     return {"paths": int(o.paths), "rows": tuple(int(r) for r in o.rows), "graphs": int(o.graphs),
-            "fused": int(o.fused)}
+            "fused": int(o.fused), "cull": int(o.cull)}
 
 
-def dbscan_set_options(paths=None, rows=None, graphs=None, fused=None, *, reset=False) -> None:
+def dbscan_set_options(paths=None, rows=None, graphs=None, fused=None, cull=None, *,
+                       reset=False) -> None:
     """Change the switches (arguments left None keep their value); ``paths``
     is a bit mask or an iterable of names from PATH_BITS ("fp32" alone, or an
     empty iterable, allows CUDA cores only); ``rows`` one int for every sweep
     or three (count, union, border); ``fused`` 0 keeps small problems on the
-    multi-kernel path; ``reset`` restores the defaults."""
+    multi-kernel path; ``cull`` 0 makes every sweep visit every tile pair;
+    ``reset`` restores the defaults."""
     lib = load()
     if reset:
         _check(lib.dbscan_set_options(None), "dbscan_set_options")
@@ -153,6 +155,7 @@ def dbscan_set_options(paths=None, rows=None, graphs=None, fused=None, *, reset=
         o.rows[i] = int(r[i])
     o.graphs = cur["graphs"] if graphs is None else int(bool(graphs))
     o.fused = cur["fused"] if fused is None else int(bool(fused))
+    o.cull = cur["cull"] if cull is None else int(bool(cull))
     _check(lib.dbscan_set_options(ctypes.byref(o)), "dbscan_set_options")
 
 
@@ -165,7 +168,7 @@ def options(**kw):
         yield
     finally:
         dbscan_set_options(paths=saved["paths"], rows=saved["rows"], graphs=saved["graphs"],
-                           fused=saved["fused"])
+                           fused=saved["fused"], cull=saved["cull"])
 
 
 SHARD_COUNTS, SHARD_PARENTS, SHARD_ORDER = 0, 1, 2

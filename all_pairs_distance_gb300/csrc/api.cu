@@ -129,6 +129,9 @@ static dbscan_options options_from_env() {
     o.fused = 1;
     const char *fu = getenv("DBSCAN_FUSED");
     if (fu && fu[0] == '0') o.fused = 0;
+    o.cull = 1;
+    const char *cu = getenv("DBSCAN_CULL");
+    if (cu && cu[0] == '0') o.cull = 0;
     return o;
 }
 
@@ -162,7 +165,7 @@ static Layout call_layout(int64_t n, int32_t d, float eps, int cull, const dbsca
     L.allow = L.umma_tile_bytes ? allowed_tc(d, L.eps2, o.paths) : 0u;
     for (int m = 0; m < 3; ++m) L.rows[m] = o.rows[m];
     L.fused = o.fused && fused_eligible(n, d);
-    L.cull_nbr = L.box_floats > 0 && L.umma_tile_bytes > 0;
+    L.cull_nbr = L.box_floats > 0 && L.umma_tile_bytes > 0 && o.cull;
     L.cull = cull && L.cull_nbr;
     return L;
 }
@@ -432,8 +435,8 @@ static int run_graph(const void *points, int dtype, int64_t n, int d, float eps,
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     uint32_t eb;
     memcpy(&eb, &eps, sizeof(eb));
-    const GraphKey key(dev, points, dtype, n, d, eb, min_pts, labels, is_core, cnt_out, ws, L.cull,
-                       L.allow, L.rows[0], L.rows[1], L.rows[2], L.fused);
+    const GraphKey key(dev, points, dtype, n, d, eb, min_pts, labels, is_core, cnt_out, ws,
+                       L.cull + 2 * L.cull_nbr, L.allow, L.rows[0], L.rows[1], L.rows[2], L.fused);
     std::lock_guard<std::mutex> lock(g_graph_mu);
     auto it = g_graphs.find(key);
     if (it != g_graphs.end()) {
@@ -669,6 +672,7 @@ int dbscan_set_options(const dbscan_options *opt) {
             if (opt->rows[m] < 0 || opt->rows[m] > 2) return DBSCAN_ERR_INVALID_ARG;
         if (opt->graphs < 0 || opt->graphs > 1) return DBSCAN_ERR_INVALID_ARG;
         if (opt->fused < 0 || opt->fused > 1) return DBSCAN_ERR_INVALID_ARG;
+        if (opt->cull < 0 || opt->cull > 1) return DBSCAN_ERR_INVALID_ARG;
         o = *opt;
     } else {
         o = options_from_env();

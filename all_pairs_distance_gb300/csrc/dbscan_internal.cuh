@@ -52,7 +52,8 @@ struct Ctrl {
     unsigned bar_gen;   // fused pipeline: grid barrier generation
     unsigned bar_count; // fused pipeline: blocks arrived at the current barrier
     int bar_abort;      // fused pipeline: set when a barrier wait timed out
-    int pad1[25];
+    float cull_thr;     // CUDA-core tile test: keep a tile pair whose squared box gap is below
+    int pad1[24];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl must be 256 bytes");
 

@@ -125,6 +125,22 @@ __global__ void k_setup(Ctrl *ctrl, const int *smin, const int *smax, float *cen
             ctrl->thrx = eps2;
         }
         ctrl->exact = (integral && R < 16777215.0) ? 1 : 0;
+        // Box gap bound of the CUDA-core sweeps' tile test.  Exact data: the
+        // gaps are integers and the test is the neighbour test itself (thrx).
+        // Otherwise the sweeps' float test v_ij < T_i can accept a pair whose
+        // exact squared distance exceeds eps^2 by its rounding error: every
+        // partial sum of v_ij and T_i is at most 3 S + eps^2 in magnitude
+        // (S bounds |c|^2, the range R <= 4 S bounds every gap), about 5 d + 2
+        // roundings of relative size 2^-24 reach the test, and the gap sum
+        // adds d + 1 more; 2^-16 (d + 4) (S + eps^2 + 1) covers them all
+        // with a factor above 20, so a skipped tile pair holds no pair the
+        // sweep would have accepted.
+        if (ctrl->exact) {
+            ctrl->cull_thr = ctrl->thrx;
+        } else {
+            const double m = ldexp((double)(d + 4) * (S + (double)eps2 + 1.0), -16);
+            ctrl->cull_thr = __double2float_ru((double)eps2 + m);
+        }
         // tensor-core eligibility (integer data, exact elements, exact sums)
         const double thrx = (double)ctrl->thrx;
         const int nt = tc_nt_for(TC_TF32, thrx);

@@ -215,12 +215,14 @@ __device__ __forceinline__ void issue_tiles(float *dst, const SweepArgs &a, Tile
 }
 
 // ---- tile culling on CUDA cores ---------------------------------------------
-// The same exact test as the tensor-core producer's (sweep_tc.cu): for integer
-// data within the exactness bound the box gaps are integers, their squared sum
-// is exact, and a column tile whose box is thrx or more (squared) from the row
-// tile's box holds no neighbour of any of its points.  A unit's column tiles
-// go KEEP_SPAN at a time: every thread tests one, and the kept ones are listed
-// in ascending order in shared memory; only those are copied and evaluated.
+// A column tile whose box is Ctrl::cull_thr or more (squared) from the row
+// tile's box holds no pair the sweep's test accepts.  For integer data within
+// the exactness bound that is the tensor-core producer's exact test (the gaps
+// are integers, their squared sum exact, and cull_thr = thrx); for other data
+// cull_thr is eps^2 plus a bound on the rounding of the sweep's float test and
+// of the gap sum (prep.cu).  A unit's column tiles go KEEP_SPAN at a time:
+// every thread tests one, and the kept ones are listed in ascending order in
+// shared memory; only those are copied and evaluated.
 constexpr int KEEP_SPAN = THREADS;
 
 // The union sweep also skips the column tiles whose points all share the row
@@ -280,8 +282,8 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
     const int n_rows = *a.n_rows, n_cols = *a.n_cols;
     if (n_rows <= 0 || n_cols <= 0) return;
     const Sched sc = make_sched(n_rows, n_cols, a.tri, a.ulo, a.uhi);
-    const bool cull = a.cull && a.ctrl->exact && a.rbox && a.cbox;
-    const float thrx = a.ctrl->thrx;
+    const bool cull = a.cull && a.rbox && a.cbox;
+    const float thrx = a.ctrl->cull_thr;
 
     for (;;) {
         if (tid == 0) s_unit = sc.ubegin + atomicAdd(a.ctr, 1u) * (unsigned)a.sworld + (unsigned)a.srank;
@@ -434,8 +436,8 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
     const int n_rows = *a.n_rows, n_cols = *a.n_cols;
     if (n_rows <= 0 || n_cols <= 0) return;
     const Sched sc = make_sched(n_rows, n_cols, a.tri, a.ulo, a.uhi);
-    const bool cull = a.cull && a.ctrl->exact && a.rbox && a.cbox && D <= CULL_MAX_D;
-    const float thrx = a.ctrl->thrx;
+    const bool cull = a.cull && a.rbox && a.cbox && D <= CULL_MAX_D;
+    const float thrx = a.ctrl->cull_thr;
 
     for (;;) {
         if (tid == 0) s_unit = sc.ubegin + atomicAdd(a.ctr, 1u) * (unsigned)a.sworld + (unsigned)a.srank;

@@ -97,15 +97,19 @@ typedef enum {
  *           points with 4 < d <= 32 -- run as one fused, cooperative launch
  *           whose grid-wide phases do every stage (CUDA cores, input order);
  *           0: always the multi-kernel path
+ *   cull    1: the union and border sweeps (and dbscan_fit_culled's count)
+ *           skip tile pairs whose bounding boxes prove that they hold no
+ *           pair the sweep would accept; 0: every sweep visits every tile
+ *           pair (for checking that the tile test changes nothing)
  * DBSCAN_PATH_F16_ACC16 is an opt-in: f16 operands with an f16 accumulator
  * (one K = 16 MMA per tile pair, d <= 10).  Its integer sum is rounded to f16
  * once, which keeps the sign the sweep reads -- provided the tensor core forms
  * the K = 16 sum exactly before that rounding.  NVIDIA does not document the
  * internal width of that sum; the library's tests observe it on GB300 only.
  * Defaults: paths = DBSCAN_PATHS_DEFAULT, rows automatic, graphs on, fused
- * on; the environment variables DBSCAN_FORCE_PATH (fp32, tf32, bf16, f16,
- * f16acc16), DBSCAN_TC_ROWS (one digit, or three for count, union, border),
- * DBSCAN_GRAPHS (0 = off) and DBSCAN_FUSED (0 = off) override the defaults,
+ * on, cull on; the environment variables DBSCAN_FORCE_PATH (fp32, tf32, bf16,
+ * f16, f16acc16), DBSCAN_TC_ROWS (one digit, or three for count, union,
+ * border), DBSCAN_GRAPHS, DBSCAN_FUSED and DBSCAN_CULL (0 = off) override the defaults,
  * read once per process at the first call into the library.  Start from
  * dbscan_get_options when changing one switch.
  */
@@ -119,11 +123,12 @@ typedef struct {
     int32_t rows[3];
     int32_t graphs;
     int32_t fused;
+    int32_t cull;
 } dbscan_options;
 
 /* Replace the switches (NULL restores the defaults above, environment
  * included).  DBSCAN_ERR_INVALID_ARG for unknown path bits, a rows entry
- * outside 0..2, or graphs or fused outside 0..1. */
+ * outside 0..2, or graphs, fused or cull outside 0..1. */
 int dbscan_set_options(const dbscan_options *opt);
 /* The switches in force (host pointer). */
 int dbscan_get_options(dbscan_options *opt);
@@ -177,10 +182,13 @@ int dbscan_fit_ex(const void *points, int32_t dtype, int64_t n, int32_t d,
  * neighbour, so for integer data within the exactness bound the result is
  * identical to dbscan_fit_ex.  This is not an all-pairs evaluation (pairs in
  * skipped tiles are never evaluated), which is why it is a separate entry
- * point.  Culling applies on the tensor-core paths for d <= 64 and exact data;
- * otherwise the call runs exactly as dbscan_fit_ex.  (dbscan_fit_ex itself
- * applies the same exact test in its union and border passes, which act only
- * on neighbour pairs; its count pass evaluates every pair.)  The pages evaluate all
+ * point.  Culling applies for d <= 64 with the cull switch on, otherwise the
+ * call runs exactly as dbscan_fit_ex.  For integer data within the exactness
+ * bound the box test is exact; for other data (CUDA-core path) it keeps every
+ * tile pair within eps plus a bound on the float test's rounding, so it never
+ * drops a pair that the unculled sweep would accept.  (dbscan_fit_ex itself
+ * applies the same test in its union and border passes, which act only on
+ * neighbour pairs; its count pass evaluates every pair.)  The pages evaluate all
  * pairs ("Design and optimization of DBSCAN Algorithm based on CUDA", §IV-A);
  * pruning by spatial bounds is not on them.
  */

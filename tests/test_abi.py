@@ -118,15 +118,17 @@ def test_options_roundtrip_and_validation(lib, monkeypatch):
     binding.dbscan_set_options(reset=True)
     try:
         o = binding.dbscan_get_options()
-        assert o == {"paths": binding.PATHS_DEFAULT, "rows": (0, 0, 0), "graphs": 1, "fused": 1} or \
+        assert o == {"paths": binding.PATHS_DEFAULT, "rows": (0, 0, 0), "graphs": 1, "fused": 1,
+                     "cull": 1} or \
             os.environ.get("DBSCAN_FORCE_PATH") or os.environ.get("DBSCAN_TC_ROWS") or \
-            os.environ.get("DBSCAN_GRAPHS") or os.environ.get("DBSCAN_FUSED")
-        binding.dbscan_set_options(paths=["f16"], rows=(1, 2, 1), graphs=0, fused=0)
-        want = {"paths": 4, "rows": (1, 2, 1), "graphs": 0, "fused": 0}
+            os.environ.get("DBSCAN_GRAPHS") or os.environ.get("DBSCAN_FUSED") or \
+            os.environ.get("DBSCAN_CULL")
+        binding.dbscan_set_options(paths=["f16"], rows=(1, 2, 1), graphs=0, fused=0, cull=0)
+        want = {"paths": 4, "rows": (1, 2, 1), "graphs": 0, "fused": 0, "cull": 0}
         assert binding.dbscan_get_options() == want
-        with binding.options(paths=["fp32"], rows=2, fused=1):
+        with binding.options(paths=["fp32"], rows=2, fused=1, cull=1):
             assert binding.dbscan_get_options() == {"paths": 0, "rows": (2, 2, 2), "graphs": 0,
-                                                    "fused": 1}
+                                                    "fused": 1, "cull": 1}
         assert binding.dbscan_get_options() == want
         # out-of-range switches are refused and leave the state alone
         bad = binding.Options()
@@ -138,6 +140,8 @@ def test_options_roundtrip_and_validation(lib, monkeypatch):
         assert lib.dbscan_set_options(ctypes.byref(bad)) == -1
         bad.graphs, bad.fused = 1, 5
         assert lib.dbscan_set_options(ctypes.byref(bad)) == -1
+        bad.fused, bad.cull = 1, 2
+        assert lib.dbscan_set_options(ctypes.byref(bad)) == -1
         assert lib.dbscan_get_options(None) == -1
         assert binding.dbscan_get_options() == want
         # the environment is read once per process and again only on a reset
@@ -145,15 +149,17 @@ def test_options_roundtrip_and_validation(lib, monkeypatch):
         monkeypatch.setenv("DBSCAN_TC_ROWS", "212")
         monkeypatch.setenv("DBSCAN_GRAPHS", "0")
         monkeypatch.setenv("DBSCAN_FUSED", "0")
+        monkeypatch.setenv("DBSCAN_CULL", "0")
         assert binding.dbscan_get_options()["paths"] == 4
         binding.dbscan_set_options(reset=True)
         assert binding.dbscan_get_options() == {"paths": 8, "rows": (2, 1, 2), "graphs": 0,
-                                                "fused": 0}
+                                                "fused": 0, "cull": 0}
     finally:
         monkeypatch.delenv("DBSCAN_FORCE_PATH", raising=False)
         monkeypatch.delenv("DBSCAN_TC_ROWS", raising=False)
         monkeypatch.delenv("DBSCAN_GRAPHS", raising=False)
         monkeypatch.delenv("DBSCAN_FUSED", raising=False)
+        monkeypatch.delenv("DBSCAN_CULL", raising=False)
         binding.dbscan_set_options(reset=True)
 
 

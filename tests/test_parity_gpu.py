@@ -358,7 +358,8 @@ CULL_CASES = {
                    .astype(np.float32), 2047.0, 5, torch.float32),
     "d16_blobs": (lambda: synth.scaled("blobs_200k_d16", 4_001, seed=46), 120.0, 20, torch.float32),
     "d33_no_cull": (lambda: _blobs(2_500, 33, 127, 8, 4.0, 250, 48), 30.0, 5, torch.float32),
-    "fractional_no_cull": (lambda: synth.scaled("blobs_1m_d3", 5_003, seed=47) * np.float32(0.5),
+    # dyadic fractions: the float test is exact, the tile test keeps a margin
+    "fractional_d3": (lambda: synth.scaled("blobs_1m_d3", 5_003, seed=47) * np.float32(0.5),
                            5.0, 8, torch.float32),
 }
 
@@ -416,7 +417,7 @@ SPAN_CASES = {
     "d3_41k": (lambda: synth.scaled("blobs_1m_d3", 41_003, seed=61), 10.0, 8),
     "d2_40k": (lambda: synth.scaled("blobs_100k_d2", 40_001, seed=62), 20.0, 10),
     "d8_34k": (lambda: _blobs(34_000, 8, 255, 40, 6.0, 3_400, 63), 14.0, 5),
-    # fractional coordinates: no exact test, so no tile is skipped
+    # fractional coordinates: the tile test with its rounding margin
     "d3_fractional_34k": (lambda: synth.scaled("blobs_1m_d3", 34_001, seed=64) * np.float32(0.5),
                           5.0, 8),
 }
@@ -440,3 +441,48 @@ def test_cuda_core_culling_spans(name, culled):
     assert_same(core, core_ref, f"{name} core flags")
     assert_same(label, label_ref, f"{name} labels")
     assert core_ref.sum() > 0 and (label_ref == -1).sum() > 0
+
+
+FLOAT_CASES = {
+    # data off the exact path (non-integer, or a range too wide for the
+    # exactness flag), where the tile test keeps every tile pair within eps
+    # plus a bound on the float test's rounding; the coordinates are chosen so
+    # that the float arithmetic itself is exact (multiples of 1/8, or integers
+    # whose sums stay below 2^24), so the sweeps are deterministic and the
+    # oracle decides every pair the same way; more than 256 row tiles
+    "d3_eighths_41k": (lambda: synth.scaled("blobs_1m_d3", 41_003, seed=81) * np.float32(0.125),
+                       1.25, 8),
+    "d2_eighths_34k": (lambda: synth.scaled("blobs_100k_d2", 34_001, seed=82) * np.float32(0.125),
+                       2.5, 10),
+    "d16_eighths_34k": (lambda: synth.scaled("blobs_200k_d16", 34_001, seed=83) * np.float32(0.125),
+                        15.0, 20),
+    # integers over [0, 3070]: range^2 sum >= 2^24 (not flagged exact), sums below 2^24
+    "d2_wide_ints_34k": (lambda: np.rint(synth.scaled("blobs_100k_d2", 34_001, seed=84) *
+                                         np.float32(1.5)).astype(np.float32), 30.0, 10),
+}
+
+
+_FLOAT_REF = {}
+
+
+@pytest.mark.parametrize("culled", [False, True])
+@pytest.mark.parametrize("name", sorted(FLOAT_CASES))
+def test_float_tile_test_matches_oracle(name, culled):
+    make, eps, min_pts = FLOAT_CASES[name]
+    P = make()
+    if name not in _FLOAT_REF:   # one oracle run per case for both entry points
+        _FLOAT_REF[name] = oracle.dbscan(P, eps, min_pts)
+    cnt_ref, core_ref, label_ref = _FLOAT_REF[name]
+    for cull in (0, 1):
+        with binding.options(cull=cull):
+            if culled:
+                core, labels = gpu_run_culled(P, eps, min_pts)
+            else:
+                info = {}
+                cnt, core, labels = gpu_run(P, eps, min_pts, info=info)
+                assert info["path"] == "fp32" and not info["exact"], info
+                assert_same(cnt, cnt_ref, f"{name} cull={cull} counts")
+        assert_same(core, core_ref, f"{name} cull={cull} core flags")
+        assert_same(labels, label_ref, f"{name} cull={cull} labels")
+    assert core_ref.sum() > 0 and (label_ref == -1).sum() > 0
+    assert len(np.unique(label_ref[label_ref >= 0])) > 1
