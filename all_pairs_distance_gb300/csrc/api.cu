@@ -273,16 +273,17 @@ static int stage_launches(unsigned allow, int d, int stage) {
     switch (stage) {
     // (+2: pivot renumbering and assignment of the order for 3 < d <= 64)
     case 0: return 9 + umma + (d > 3 && d <= 64 ? 2 : 0);
-    case 1: return 1 + ntc;
+    // (each CUDA-core sweep: one launch per form of the neighbour test)
+    case 1: return 2 + ntc;
     case 2: return 4 + umma;
-    // tile-local union, then per band on CUDA cores: the sweep, a tile-root
-    // snapshot and (after the first) a compression, and per tensor-core band:
-    // a launch per kind, a tile-root snapshot and (after the first) a
-    // compression
-    case 3: return 1 + UNION_BANDS * 2 + (UNION_BANDS - 1) + UNION_BANDS * (ntc + 1) +
+    // tile-local union, then per band on CUDA cores: the sweep (two forms), a
+    // tile-root snapshot and (after the first) a compression, and per
+    // tensor-core band: a launch per kind, a tile-root snapshot and (after the
+    // first) a compression
+    case 3: return 1 + UNION_BANDS * 3 + (UNION_BANDS - 1) + UNION_BANDS * (ntc + 1) +
                    (UNION_BANDS - 1);
     case 4: return 2;
-    case 5: return umma + 1 + ntc;
+    case 5: return umma + 2 + ntc;
     default: return 1;
     }
 }

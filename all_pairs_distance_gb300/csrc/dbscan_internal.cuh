@@ -7,6 +7,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 #include <stddef.h>
+#include <math.h>
 
 #include "../../include/dbscan.h"
 
@@ -28,6 +29,27 @@ constexpr int CULL_GROUP = 8;
 // negative threshold and never tests as a neighbour either.
 constexpr float PAD_NORM = 1.0e30f;
 constexpr float PAD_THRESH = -1.0e30f;
+
+// Two forms of the CUDA-core neighbour test, with A_ik the row's staged
+// scale of c_ik and s_j the column's norm slot:
+//   expanded (exact data):  v_ij = s_j + sum_k A_ik c_jk,  A = -2 c_i,
+//                           s_j = |c_j|^2, T_i = thrx - |c_i|^2: every sum
+//                           is an exact integer below 2^24, so the test is
+//                           exact and one FMA per coordinate;
+//   direct (other data):    v_ij = s_j + sum_k (c_jk + A_ik)^2,  A = -c_i,
+//                           s_j = 0, T_i = direct_threshold: accurate to a
+//                           few roundings of d^2 itself (the expanded form
+//                           errs by roundings of |c|^2, far above eps^2 when
+//                           the coordinates are large), and symmetric --
+//                           (c_jk - c_ik)^2 is the same number for either
+//                           point as the row, so every pass decides a pair
+//                           the same way whatever the order of the points.
+// A pair is a neighbour iff v_ij < T_i in both; padding has s_j = PAD_NORM
+// and T_i = PAD_THRESH.
+__host__ __device__ inline float direct_threshold(float thrx, bool integral) {
+    // integer data: d^2 <= floor(eps^2) iff d^2 < thrx; otherwise d^2 <= eps^2
+    return integral ? thrx : nextafterf(thrx, INFINITY);
+}
 
 // Device control block at offset 0 of every workspace.
 struct Ctrl {

@@ -35,7 +35,9 @@
 //
 // Arithmetic is that of the CUDA-core sweeps: fp32 FMAs on centred
 // coordinates, v_ij = nrm_j + sum_k (-2 c_ik) c_jk tested against
-// T_i = thrx - nrm_i, exact for integer data while sum_k range_k^2 < 2^24.
+// T_i = thrx - nrm_i, exact for integer data while sum_k range_k^2 < 2^24,
+// and for other data the direct form v_ij = sum_k (c_jk - c_ik)^2 against
+// the common threshold (dbscan_internal.cuh).
 // Every barrier wait is bounded; on timeout the kernel records
 // DBSCAN_ERR_INTERNAL and every block leaves at its next barrier.
 #include "dbscan_internal.cuh"
@@ -139,25 +141,35 @@ __device__ __forceinline__ void tri_pair(int u, int nt, int &rb, int &cb) {
     cb = r + (u - S(r));
 }
 
-// Row thread state: -2 c_i in registers (D > 0) or in shared memory (D = 0).
+// Row thread state: A = -2 c_i (expanded form) or -c_i (direct form) in
+// registers (D > 0) or in shared memory (D = 0).
 template <int D>
 struct RowPoint {
     float a[D > 0 ? D : 1];
 };
 
-// v_ij = nrm_j + sum_k a_k c_jk for column j of the staged column tile s
-// (structure of arrays: (d + 1) x FT floats, the norms last).
+// One term of v_ij: a_k c_jk (expanded) or (c_jk + a_k)^2 (direct).
+__device__ __forceinline__ float pair_term(bool direct, float ak, float ck, float v) {
+    if (direct) {
+        const float q = ck + ak;
+        return fmaf(q, q, v);
+    }
+    return fmaf(ak, ck, v);
+}
+
+// v_ij = slot_j + the sum of the terms for column j of the staged column tile
+// s (structure of arrays: (d + 1) x FT floats, the norm slots last).
 template <int D>
-__device__ __forceinline__ float pair_value(const RowPoint<D> &r, const float *sa, const float *s, int d,
-                                            int j) {
+__device__ __forceinline__ float pair_value(bool direct, const RowPoint<D> &r, const float *sa,
+                                            const float *s, int d, int j) {
     if (D > 0) {
         float v = s[D * FT + j];
 #pragma unroll
-        for (int k = 0; k < D; ++k) v = fmaf(r.a[k], s[k * FT + j], v);
+        for (int k = 0; k < D; ++k) v = pair_term(direct, r.a[k], s[k * FT + j], v);
         return v;
     }
     float v = s[d * FT + j];
-    for (int k = 0; k < d; ++k) v = fmaf(sa[k * FT + threadIdx.x], s[k * FT + j], v);
+    for (int k = 0; k < d; ++k) v = pair_term(direct, sa[k * FT + threadIdx.x], s[k * FT + j], v);
     return v;
 }
 
@@ -173,7 +185,7 @@ __global__ void __launch_bounds__(FT) k_fused(FusedArgs a) {
     int *s_aux = reinterpret_cast<int *>(s_row + (D > 0 ? 0 : (size_t)d * FT));   // 2 x FT ints
     __shared__ float s_centre[DBSCAN_MAX_D];
     __shared__ float s_thrx;
-    __shared__ int s_integral;
+    __shared__ int s_integral, s_direct;
 
     // ---- stats ----------------------------------------------------------------
     {
@@ -237,6 +249,7 @@ __global__ void __launch_bounds__(FT) k_fused(FusedArgs a) {
             thrx = (float)(t + 1.0);
         }
         s_thrx = thrx;
+        s_direct = (integral && R < 16777215.0) ? 0 : 1;
         if (blockIdx.x == 0) {
             ctrl->n_all = n;
             ctrl->range_sq = (float)R;
@@ -250,6 +263,8 @@ __global__ void __launch_bounds__(FT) k_fused(FusedArgs a) {
         }
     }
     __syncthreads();
+    const bool direct = s_direct != 0;             // the form of the test, uniform
+    const float ascale = direct ? -1.f : -2.f;     // the row's scale of c_i
     {
         const float thrx = s_thrx;
         const int npad = nt * FT;
@@ -263,12 +278,18 @@ __global__ void __launch_bounds__(FT) k_fused(FusedArgs a) {
             }
             float nrm = 0.f;
             for (int k = 0; k < d; ++k) {
-                const float c = load_point(a.pts, a.dtype, (size_t)i * d + k) - s_centre[k];
+                // the direct form takes the coordinates as they are (prep.cu)
+                const float c = load_point(a.pts, a.dtype, (size_t)i * d + k) - (direct ? 0.f : s_centre[k]);
                 base[(size_t)k * FT] = c;
                 nrm = fmaf(c, c, nrm);
             }
-            base[(size_t)d * FT] = nrm;
-            a.T[i] = integral ? thrx - nrm : nextafterf(thrx - nrm, INFINITY);
+            if (s_direct) {
+                base[(size_t)d * FT] = 0.f;
+                a.T[i] = direct_threshold(thrx, integral);
+            } else {
+                base[(size_t)d * FT] = nrm;
+                a.T[i] = integral ? thrx - nrm : nextafterf(thrx - nrm, INFINITY);
+            }
         }
         for (int t = blockIdx.x * FT + tid; t < nt; t += nb * FT) a.tcore[t] = 0;
     }
@@ -285,19 +306,19 @@ __global__ void __launch_bounds__(FT) k_fused(FusedArgs a) {
         RowPoint<D> r;
         if (D > 0) {
 #pragma unroll
-            for (int k = 0; k < (D > 0 ? D : 1); ++k) r.a[k] = -2.f * gr[k * FT + tid];
+            for (int k = 0; k < (D > 0 ? D : 1); ++k) r.a[k] = ascale * gr[k * FT + tid];
         } else {
-            for (int k = 0; k < d; ++k) s_row[k * FT + tid] = -2.f * gr[k * FT + tid];
+            for (int k = 0; k < d; ++k) s_row[k * FT + tid] = ascale * gr[k * FT + tid];
         }
         s_aux[tid] = 0;
         __syncthreads();
         const float Ti = a.T[rb * FT + tid];
         int rowc = 0;
         if (rb == cb) {
-            for (int j = 0; j < FT; ++j) rowc += pair_value<D>(r, s_row, s_col, d, j) < Ti;
+            for (int j = 0; j < FT; ++j) rowc += pair_value<D>(direct, r, s_row, s_col, d, j) < Ti;
         } else {
             for (int j = 0; j < FT; ++j) {
-                if (pair_value<D>(r, s_row, s_col, d, j) < Ti) {
+                if (pair_value<D>(direct, r, s_row, s_col, d, j) < Ti) {
                     ++rowc;
                     atomicAdd(&s_aux[j], 1);
                 }
@@ -351,9 +372,9 @@ __global__ void __launch_bounds__(FT) k_fused(FusedArgs a) {
             RowPoint<D> r;
             if (D > 0) {
 #pragma unroll
-                for (int k = 0; k < (D > 0 ? D : 1); ++k) r.a[k] = -2.f * gr[k * FT + tid];
+                for (int k = 0; k < (D > 0 ? D : 1); ++k) r.a[k] = ascale * gr[k * FT + tid];
             } else {
-                for (int k = 0; k < d; ++k) s_row[k * FT + tid] = -2.f * gr[k * FT + tid];
+                for (int k = 0; k < d; ++k) s_row[k * FT + tid] = ascale * gr[k * FT + tid];
             }
             const int q = cb * FT + tid;
             const bool qcore = q < n && a.cnt[q] >= a.min_pts;
@@ -366,7 +387,7 @@ __global__ void __launch_bounds__(FT) k_fused(FusedArgs a) {
                 if (pass == 0) {
                     int lo = p;   // the smallest neighbour index of this row so far
                     for (int j = (rb == cb ? tid + 1 : 0); j < FT; ++j) {
-                        if (!s_aux[j] || !(pair_value<D>(r, s_row, s_col, d, j) < Ti)) continue;
+                        if (!s_aux[j] || !(pair_value<D>(direct, r, s_row, s_col, d, j) < Ti)) continue;
                         const int qj = cb * FT + j;
                         if (qj < p) lo = min(lo, qj);
                         else atomicMin(a.parent + qj, p);
@@ -379,7 +400,7 @@ __global__ void __launch_bounds__(FT) k_fused(FusedArgs a) {
                     for (int j = (rb == cb ? tid + 1 : 0); j < FT; ++j) {
                         const int sj = s_par[j];
                         if (!s_aux[j] || sj == root || sj == j0 || sj == j1 ||
-                            !(pair_value<D>(r, s_row, s_col, d, j) < Ti))
+                            !(pair_value<D>(direct, r, s_row, s_col, d, j) < Ti))
                             continue;
                         j1 = j0;
                         j0 = sj;
@@ -424,9 +445,9 @@ __global__ void __launch_bounds__(FT) k_fused(FusedArgs a) {
             const float *gp = a.staged + (size_t)(p / FT) * (d + 1) * FT + (p % FT);
             if (D > 0) {
 #pragma unroll
-                for (int kk = 0; kk < (D > 0 ? D : 1); ++kk) r.a[kk] = -2.f * gp[kk * FT];
+                for (int kk = 0; kk < (D > 0 ? D : 1); ++kk) r.a[kk] = ascale * gp[kk * FT];
             } else {
-                for (int kk = 0; kk < d; ++kk) s_row[kk * FT + tid] = -2.f * gp[kk * FT];
+                for (int kk = 0; kk < d; ++kk) s_row[kk * FT + tid] = ascale * gp[kk * FT];
             }
         }
         const int q = cb * FT + tid;
@@ -437,7 +458,7 @@ __global__ void __launch_bounds__(FT) k_fused(FusedArgs a) {
             const float Ti = a.T[p];
             int best = 0x7fffffff;
             for (int j = 0; j < FT; ++j)
-                if (s_aux[j] >= 0 && pair_value<D>(r, s_row, s_col, d, j) < Ti) best = min(best, s_aux[j]);
+                if (s_aux[j] >= 0 && pair_value<D>(direct, r, s_row, s_col, d, j) < Ti) best = min(best, s_aux[j]);
             if (best != 0x7fffffff) atomicMin(&a.labels[p], best);
         }
         __syncthreads();

@@ -287,11 +287,17 @@ cudaError_t launch_stage_umma(const Work &w, const Layout &L, int which, cudaStr
 
 // One thread per (padded) position p: the centred coordinates and norm of
 // input point perm[p] into the tiled layout, its row threshold into T[p].
+// Data off the exact path (Ctrl::exact = 0) are tested in the direct form
+// sum_k (c_jk - c_ik)^2 < T on CUDA cores: the norm slot then holds 0 (the
+// sum's start; PAD_NORM for padding) and T[p] the common threshold
+// (dbscan_internal.cuh).
 __global__ void k_stage(const void *pts, int dtype, int64_t n, int d, const Ctrl *ctrl,
                         const float *centre, const int *perm, float *staged, float *T,
                         int64_t npad) {
     extern __shared__ float s_centre[];
-    for (int k = threadIdx.x; k < d; k += blockDim.x) s_centre[k] = centre[k];
+    // the direct form takes the coordinates as they are: the difference of
+    // two nearby floats is exact, while centring rounds each coordinate once
+    for (int k = threadIdx.x; k < d; k += blockDim.x) s_centre[k] = ctrl->exact ? centre[k] : 0.f;
     __syncthreads();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= npad) return;
@@ -310,6 +316,11 @@ __global__ void k_stage(const void *pts, int dtype, int64_t n, int d, const Ctrl
         float c = load_point(pts, dtype, (size_t)src * d + k) - s_centre[k];
         base[(size_t)k * BT] = c;
         nrm = fmaf(c, c, nrm);
+    }
+    if (!ctrl->exact) {
+        base[(size_t)d * BT] = 0.f;
+        T[i] = direct_threshold(ctrl->thrx, ctrl->nonint == 0);
+        return;
     }
     base[(size_t)d * BT] = nrm;
     const float thrx = ctrl->thrx;

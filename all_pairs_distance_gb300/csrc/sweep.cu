@@ -264,9 +264,12 @@ __device__ __forceinline__ int keep_tiles(const SweepArgs &a, int d, int c0, int
 // ===========================================================================
 // d <= 4: rows in registers, packed f32x2 FMAs.
 // ===========================================================================
-template <int D, int MODE>
-__global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
+// DIRECT: the direct form of the test (data off the exact path), else the
+// expanded form (dbscan_internal.cuh); the kernels below pick one per call.
+template <int D, int MODE, bool DIRECT>
+__device__ __forceinline__ void sweep_small(const SweepArgs &a) {
     constexpr bool AUX = MODE != SWEEP_COUNT;
+    constexpr float RSCALE = DIRECT ? -1.f : -2.f;   // the row's staged scale of c_i
     constexpr int TILE = (D + 1) * BT;
     constexpr int CT = 4;   // tiles per stage
     constexpr int S = 3;    // stages
@@ -301,7 +304,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
         const int rroot = a.troot ? a.troot[rb] : -1;
         const bool filt = cull || rroot >= 0;
 
-        // rows of this unit: packed (-2c, -2c) and thresholds
+        // rows of this unit: packed (A, A), A = -2c or -c, and thresholds
         float2 ra[R][D];
         float rT[R];
         {
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
                 float4 hi = *reinterpret_cast<const float4 *>(rt + k * BT + 64 + 4 * tr);
                 float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-                for (int m = 0; m < R; ++m) ra[m][k] = make_float2(-2.f * v[m], -2.f * v[m]);
+                for (int m = 0; m < R; ++m) ra[m][k] = make_float2(RSCALE * v[m], RSCALE * v[m]);
             }
             const float *tt = a.rowT + (size_t)rb * BT;
             float4 lo = *reinterpret_cast<const float4 *>(tt + 4 * tr);
@@ -375,8 +378,15 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
                     for (int p2 = 0; p2 < C / 2; ++p2) {
                         float2 t = make_float2(xc[D][2 * p2], xc[D][2 * p2 + 1]);
 #pragma unroll
-                        for (int k = 0; k < D; ++k)
-                            t = __ffma2_rn(ra[m][k], make_float2(xc[k][2 * p2], xc[k][2 * p2 + 1]), t);
+                        for (int k = 0; k < D; ++k) {
+                            const float2 x = make_float2(xc[k][2 * p2], xc[k][2 * p2 + 1]);
+                            if (DIRECT) {
+                                const float2 q = __fadd2_rn(x, ra[m][k]);
+                                t = __ffma2_rn(q, q, t);
+                            } else {
+                                t = __ffma2_rn(ra[m][k], x, t);
+                            }
+                        }
                         v[p2] = t;
                     }
                     float mn = min3f(min3f(v[0].x, v[0].y, v[1].x), min3f(v[1].y, v[2].x, v[2].y),
@@ -393,7 +403,14 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
                         for (int c = 0; c < C; ++c) {
                             float v = xc[D][c];
 #pragma unroll
-                            for (int k = 0; k < D; ++k) v = fmaf(ra[m][k].x, xc[k][c], v);
+                            for (int k = 0; k < D; ++k) {
+                                if (DIRECT) {
+                                    const float q = xc[k][c] + ra[m][k].x;
+                                    v = fmaf(q, q, v);
+                                } else {
+                                    v = fmaf(ra[m][k].x, xc[k][c], v);
+                                }
+                            }
                             if (v < rT[m]) {
                                 const int slot = slot_of(tc, c);
                                 on_neighbour<MODE>(a, p, tile * BT + slot, diag,
@@ -411,21 +428,31 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
     }
 }
 
+// One kernel per form (both are launched; the one the data did not select
+// returns at once): a kernel holding both bodies spilled registers in the
+// expanded count (1M x 3 FFMA count 73.3 -> 74.2 ms).
+template <int D, int MODE, bool DIRECT>
+__global__ void __launch_bounds__(THREADS, 2) k_sweep_small(SweepArgs a) {
+    if ((a.ctrl->exact == 0) != DIRECT) return;
+    sweep_small<D, MODE, DIRECT>(a);
+}
+
 // ===========================================================================
 // d > 4: rows and columns from shared memory, 8x8 register accumulators.
 // S = 1 (d > 128, where a row tile and two column stages exceed shared
 // memory): one column stage, loaded and used in turn, and the row values read
 // from the staged row tile in global memory (L2-resident).
 // ===========================================================================
-template <int MODE, int S>
-__global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
+template <int MODE, int S, bool DIRECT>
+__device__ __forceinline__ void sweep_gen(const SweepArgs &a, int D) {
     constexpr bool AUX = MODE != SWEEP_COUNT;
+    constexpr float RSCALE = DIRECT ? -1.f : -2.f;   // the row's staged scale of c_i
     constexpr bool ROWS_GLOBAL = S == 1;
     extern __shared__ __align__(16) float smem[];
     __shared__ unsigned s_unit;
     const int TILE = (D + 1) * BT;
     const int STAGE = TILE + (AUX ? BT : 0);
-    float *rowbuf = smem;                                 // D * BT floats: -2 c of the row tile
+    float *rowbuf = smem;                                 // D * BT floats: A of the row tile
     float *stages = smem + (ROWS_GLOBAL ? 0 : D * BT);    // S * STAGE floats
     __shared__ int s_list[KEEP_SPAN], s_wtot[THREADS / 32];
     __shared__ float s_rbox[2 * CULL_MAX_D];
@@ -456,10 +483,10 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
         const bool filt = cull || rroot >= 0;
 
         const float *rowsrc = ROWS_GLOBAL ? a.rows + (size_t)rb * TILE : rowbuf;
-        const float rscale = ROWS_GLOBAL ? -2.f : 1.f;
+        const float rscale = ROWS_GLOBAL ? RSCALE : 1.f;
         if (!ROWS_GLOBAL) {
             const float *rt = a.rows + (size_t)rb * TILE;
-            for (int e = tid; e < D * BT; e += THREADS) rowbuf[e] = -2.f * rt[e];
+            for (int e = tid; e < D * BT; e += THREADS) rowbuf[e] = RSCALE * rt[e];
         }
         float rT[R];
         {
@@ -534,7 +561,14 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
 #pragma unroll
                 for (int m = 0; m < R; ++m)
 #pragma unroll
-                    for (int c = 0; c < C; ++c) v[m][c] = fmaf(rr[m], xx[c], v[m][c]);
+                    for (int c = 0; c < C; ++c) {
+                        if (DIRECT) {
+                            const float q = xx[c] + rr[m];
+                            v[m][c] = fmaf(q, q, v[m][c]);
+                        } else {
+                            v[m][c] = fmaf(rr[m], xx[c], v[m][c]);
+                        }
+                    }
             }
             unsigned hit = 0;
 #pragma unroll
@@ -566,6 +600,12 @@ __global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
     }
 }
 
+template <int MODE, int S, bool DIRECT>
+__global__ void __launch_bounds__(THREADS, 2) k_sweep_gen(SweepArgs a, int D) {
+    if ((a.ctrl->exact == 0) != DIRECT) return;
+    sweep_gen<MODE, S, DIRECT>(a, D);
+}
+
 // ---- tile-local union before the core-core sweep -------------------------------
 // With the points in locality order most core-core neighbour pairs fall inside
 // a diagonal tile.  One CTA per core tile joins the tile's own neighbour pairs
@@ -589,9 +629,10 @@ __device__ __forceinline__ int sm_find(volatile int *sp, int x) {
 // DMAX > 0 (d <= DMAX): the thread's own point, scaled by -2, sits in
 // registers, so every FMA reads one shared-memory word instead of two (the
 // products and their order are those of the generic form).
-template <int DMAX>
-__global__ void k_local_union(const Ctrl *ctrl, const float *staged, const float *T, int d,
-                              int *parent) {
+template <int DMAX, bool DIRECT>
+__device__ __forceinline__ void local_union(const Ctrl *ctrl, const float *staged, const float *T,
+                                            int d, int *parent) {
+    constexpr float RSCALE = DIRECT ? -1.f : -2.f;   // the row's staged scale of c_i
     extern __shared__ float s_pts[];   // (d + 1) * BT staged floats, then BT parents
     volatile int *sp = reinterpret_cast<volatile int *>(s_pts + (size_t)(d + 1) * BT);
     const int n_core = ctrl->n_core;
@@ -610,7 +651,7 @@ __global__ void k_local_union(const Ctrl *ctrl, const float *staged, const float
             float ri[DMAX > 0 ? DMAX : 1];
             if constexpr (DMAX > 0) {
 #pragma unroll
-                for (int k = 0; k < DMAX; ++k) ri[k] = k < d ? -2.f * s_pts[(size_t)k * BT + i] : 0.f;
+                for (int k = 0; k < DMAX; ++k) ri[k] = k < d ? RSCALE * s_pts[(size_t)k * BT + i] : 0.f;
             }
             // pairs (i, i + sh mod BT), sh = 1..63, and sh = 64 for i < 64: every
             // unordered pair of the tile once, 63 or 64 per thread
@@ -622,10 +663,23 @@ __global__ void k_local_union(const Ctrl *ctrl, const float *staged, const float
                 if constexpr (DMAX > 0) {
 #pragma unroll
                     for (int k = 0; k < DMAX; ++k)
-                        if (k < d) v = fmaf(ri[k], s_pts[(size_t)k * BT + j], v);
+                        if (k < d) {
+                            if (DIRECT) {
+                                const float q = s_pts[(size_t)k * BT + j] + ri[k];
+                                v = fmaf(q, q, v);
+                            } else {
+                                v = fmaf(ri[k], s_pts[(size_t)k * BT + j], v);
+                            }
+                        }
                 } else {
-                    for (int k = 0; k < d; ++k)
-                        v = fmaf(-2.f * s_pts[(size_t)k * BT + i], s_pts[(size_t)k * BT + j], v);
+                    for (int k = 0; k < d; ++k) {
+                        if (DIRECT) {
+                            const float q = s_pts[(size_t)k * BT + j] + RSCALE * s_pts[(size_t)k * BT + i];
+                            v = fmaf(q, q, v);
+                        } else {
+                            v = fmaf(RSCALE * s_pts[(size_t)k * BT + i], s_pts[(size_t)k * BT + j], v);
+                        }
+                    }
                 }
                 if (!(v < Ti)) continue;
                 int ra = i, rb = j;
@@ -641,6 +695,13 @@ __global__ void k_local_union(const Ctrl *ctrl, const float *staged, const float
         __syncthreads();
         if (i < nv) parent[base + i] = base + sm_find(sp, i);
     }
+}
+
+template <int DMAX>
+__global__ void k_local_union(const Ctrl *ctrl, const float *staged, const float *T, int d,
+                              int *parent) {
+    if (ctrl->exact) local_union<DMAX, false>(ctrl, staged, T, d, parent);
+    else local_union<DMAX, true>(ctrl, staged, T, d, parent);
 }
 
 // Point every core position straight at its root (between union waves);
@@ -706,9 +767,9 @@ int persistent_ctas(const void *kernel, int threads, size_t smem) {
     return v;
 }
 
-template <int D, int MODE>
-static cudaError_t run_small(const SweepArgs &args, cudaStream_t s) {
-    auto kernel = k_sweep_small<D, MODE>;
+template <int D, int MODE, bool DIRECT>
+static cudaError_t run_small_form(const SweepArgs &args, cudaStream_t s) {
+    auto kernel = k_sweep_small<D, MODE, DIRECT>;
     const int aux = MODE != SWEEP_COUNT ? 4 * BT : 0;
     const size_t smem = (size_t)3 * (4 * (D + 1) * BT + aux) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute((const void *)kernel,
@@ -719,9 +780,9 @@ static cudaError_t run_small(const SweepArgs &args, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int MODE, int S>
-static cudaError_t run_gen(const SweepArgs &args, int d, cudaStream_t s) {
-    auto kernel = k_sweep_gen<MODE, S>;
+template <int MODE, int S, bool DIRECT>
+static cudaError_t run_gen_form(const SweepArgs &args, int d, cudaStream_t s) {
+    auto kernel = k_sweep_gen<MODE, S, DIRECT>;
     const int aux = MODE != SWEEP_COUNT ? BT : 0;
     const size_t smem = ((S == 1 ? 0 : (size_t)d * BT) + (size_t)S * ((d + 1) * BT + aux)) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute((const void *)kernel,
@@ -730,6 +791,18 @@ static cudaError_t run_gen(const SweepArgs &args, int d, cudaStream_t s) {
     const int grid = persistent_ctas((const void *)kernel, THREADS, smem);
     kernel<<<grid, THREADS, smem, s>>>(args, d);
     return cudaGetLastError();
+}
+
+template <int D, int MODE>
+static cudaError_t run_small(const SweepArgs &args, cudaStream_t s) {
+    cudaError_t e = run_small_form<D, MODE, false>(args, s);
+    return e != cudaSuccess ? e : run_small_form<D, MODE, true>(args, s);
+}
+
+template <int MODE, int S>
+static cudaError_t run_gen(const SweepArgs &args, int d, cudaStream_t s) {
+    cudaError_t e = run_gen_form<MODE, S, false>(args, d, s);
+    return e != cudaSuccess ? e : run_gen_form<MODE, S, true>(args, d, s);
 }
 
 template <int MODE>

@@ -486,3 +486,42 @@ def test_float_tile_test_matches_oracle(name, culled):
         assert_same(labels, label_ref, f"{name} cull={cull} labels")
     assert core_ref.sum() > 0 and (label_ref == -1).sum() > 0
     assert len(np.unique(label_ref[label_ref >= 0])) > 1
+
+
+def _jittered(P, scale, seed):
+    # continuous (non-dyadic) float coordinates
+    rng = np.random.default_rng(seed)
+    return (P * np.float32(scale) + rng.random(P.shape, dtype=np.float32) * np.float32(scale))
+
+
+ACCURACY_CASES = {
+    # float data whose spread is large against eps (range ~200 against eps 1,
+    # ~190 against 44): the direct form of the test is accurate to a few
+    # roundings of d^2 itself
+    "d3_41k": (lambda: _jittered(synth.scaled("blobs_1m_d3", 41_003, seed=91), 0.1, 11), 1.0, 8),
+    "d16_34k": (lambda: _jittered(synth.scaled("blobs_200k_d16", 34_001, seed=93), 0.37, 13), 44.4, 20),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ACCURACY_CASES))
+def test_float_data_counts_within_rounding_and_repeatable(name):
+    # on float data a pair can be decided either way only when its squared
+    # distance lies within a relative 1e-5 of eps^2: every count lies between
+    # the oracle's counts at those two radii, and a second call (the points
+    # may land in other tiles) repeats every count, flag and label
+    make, eps, min_pts = ACCURACY_CASES[name]
+    P = make()
+    lo = oracle.counts(P, eps * np.sqrt(1.0 - 1e-5))
+    hi = oracle.counts(P, eps * np.sqrt(1.0 + 1e-5))
+    info = {}
+    first = gpu_run(P, eps, min_pts, info=info)
+    assert info["path"] == "fp32" and not info["exact"], info
+    cnt, core, labels = first
+    bad = np.flatnonzero((cnt < lo) | (cnt > hi))
+    assert bad.size == 0, (f"{bad.size} counts outside the rounding window, first at {bad[:8].tolist()}: "
+                           f"got {cnt[bad[:8]].tolist()} in [{lo[bad[:8]].tolist()}, "
+                           f"{hi[bad[:8]].tolist()}]")
+    assert np.all(core >= (lo >= min_pts)) and np.all(core <= (hi >= min_pts))
+    second = gpu_run(P, eps, min_pts)
+    for g, e, w in zip(second, first, ("counts", "core flags", "labels")):
+        assert_same(g, e, f"{name} repeated call {w}")
