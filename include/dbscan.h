@@ -37,9 +37,13 @@
  * over the data's per-dimension ranges is below 2^24, every product and
  * partial sum the kernels form is an integer below 2^24, which float32 holds
  * exactly, and the results are exact (identical to a double-precision
- * evaluation).  Otherwise pairs within float32 rounding of the eps boundary
- * may be classified either way.  (The opt-in DBSCAN_PATH_F16_ACC16 path is
- * the one exception to float32 accumulation; see dbscan_set_options.)
+ * evaluation).  Other data run on CUDA cores with the test in the direct
+ * form sum_k (x_ik - x_jk)^2, uncentred: accurate to a few float32 roundings
+ * of the squared distance itself and symmetric in i and j, so every pass and
+ * every call decides a pair the same way; only pairs whose squared distance
+ * lies within that rounding (about 1e-6 relative) of eps2 may be classified
+ * either way.  (The opt-in DBSCAN_PATH_F16_ACC16 path is the one exception to
+ * float32 accumulation; see dbscan_set_options.)
  *
  * Memory: every pointer argument is a DEVICE pointer unless the entry point's
  * name ends in _host.  The caller owns all buffers; the library never frees
