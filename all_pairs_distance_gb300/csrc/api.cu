@@ -258,15 +258,11 @@ static void keep_pool(void) {
 }
 
 // ---- stage timing ------------------------------------------------------------
-// Kernels each stage launches.  Every sweep launches its CUDA-core kernel and
-// one kernel per tensor-core kind the call allows (ntc: the allowed paths
-// whose operand rows fit the shape); all but the path chosen on the device
-// return at once.
-//   prep 4 + 5 locality order (+2 pivot kernels for 3 < d <= 64, +1 operand
-//   staging), count 1 + ntc,
-//   compact 4 (+1 operand staging), union 1 tile-local + 2 CUDA-core waves
-//   + 1 compression + 6 tensor-core bands x ntc + 5 compressions, flatten 2,
-//   border (+1 operand staging) 1 + ntc, finalize 1.
+// Kernels each stage launches.  Every sweep launches its two CUDA-core
+// kernels (one per form of the neighbour test) and one kernel per
+// tensor-core kind the call allows (ntc: the allowed paths whose operand rows
+// fit the shape); all but the one the data select on the device return at
+// once.  The per-stage counts are in the switch below.
 static int stage_launches(unsigned allow, int d, int stage) {
     const int ntc = __builtin_popcount(allow);
     const int umma = ntc > 0 ? 1 : 0;

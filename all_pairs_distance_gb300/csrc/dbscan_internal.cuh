@@ -61,7 +61,7 @@ struct Ctrl {
     int exact;          // 1 when the exactness bound holds (set by setup)
     float thrx;         // row threshold constant, see prep.cu
     int n_all;          // number of points
-    unsigned unit_ctr[8];   // work-unit counters: count, union waves 1-4, border
+    unsigned unit_ctr[8];   // CUDA-core work-unit counters: count, union bands 1-3 (slots 1-3), border (5)
     float range_sq;     // sum_k (max_k - min_k)^2
     int tc_kind;        // tensor-core path chosen by setup: a TcKind (TC_NONE = CUDA cores)
     int tc_kpad;        // padded K of the tensor-core operands (elements)

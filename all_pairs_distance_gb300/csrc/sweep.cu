@@ -704,7 +704,7 @@ __global__ void k_local_union(const Ctrl *ctrl, const float *staged, const float
     else local_union<DMAX, true>(ctrl, staged, T, d, parent);
 }
 
-// Point every core position straight at its root (between union waves);
+// Point every core position straight at its root (between union bands);
 // tc = 1 runs only on the tensor-core path, tc = 0 only on the CUDA-core path.
 __global__ void k_compress(Ctrl *ctrl, int *parent, int tc) {
     if ((ctrl->tc_kind != TC_NONE) != (tc != 0)) return;
