@@ -263,8 +263,11 @@ static void keep_pool(void) {
 // tensor-core kind the call allows (ntc: the allowed paths whose operand rows
 // fit the shape); all but the one the data select on the device return at
 // once.  The per-stage counts are in the switch below.
-static int stage_launches(unsigned allow, int d, int stage) {
+int union_band_count(int64_t ntiles);   // sweep.cu
+
+static int stage_launches(unsigned allow, int d, int64_t ntiles, int stage) {
     const int ntc = __builtin_popcount(allow);
+    const int nb = union_band_count(ntiles);
     const int umma = ntc > 0 ? 1 : 0;
     switch (stage) {
     // (+2: pivot renumbering and assignment of the order for 3 < d <= 64)
@@ -276,8 +279,7 @@ static int stage_launches(unsigned allow, int d, int stage) {
     // tile-root snapshot and (after the first) a compression, and per
     // tensor-core band: a launch per kind, a tile-root snapshot and (after the
     // first) a compression
-    case 3: return 1 + UNION_BANDS * 3 + (UNION_BANDS - 1) + UNION_BANDS * (ntc + 1) +
-                   (UNION_BANDS - 1);
+    case 3: return 1 + nb * 3 + (nb - 1) + nb * (ntc + 1) + (nb - 1);
     case 4: return 2;
     case 5: return umma + 2 + ntc;
     default: return 1;
@@ -289,6 +291,7 @@ struct ProfCall {
     int stages;       // number of stages the call ran
     unsigned allow;   // tensor-core kinds launched by the call's sweeps
     int d;            // dimension (the order's pivot kernels run for 3 < d <= 64)
+    int64_t ntiles;   // tiles of the call (the union's band count)
     int cull;         // 1: culled count, 2: culled union and border (box kernels)
     int fused;        // 1: the fused single-launch pipeline (one kernel)
 };
@@ -303,9 +306,10 @@ struct StageMarks {
     ProfCall call{};
     bool on = false;
     int next = 0;
-    StageMarks(cudaStream_t s, unsigned allow, int d, int cull, int fused) {
+    StageMarks(cudaStream_t s, unsigned allow, int d, int64_t ntiles, int cull, int fused) {
         call.allow = allow;
         call.d = d;
+        call.ntiles = ntiles;
         call.cull = cull;
         call.fused = fused;
         if (!g_prof.on) return;
@@ -337,7 +341,7 @@ static int run(const void *points, int dtype, int64_t n, int d, float eps, int m
                int32_t *labels, uint8_t *is_core, int32_t *cnt_out, void *ws, const Layout &L,
                cudaStream_t s) {
     Work w = carve(ws, L);
-    StageMarks marks(s, L.allow, d, L.cull + 2 * L.cull_nbr, L.fused);
+    StageMarks marks(s, L.allow, d, L.ntiles, L.cull + 2 * L.cull_nbr, L.fused);
     if (L.fused) {
         // one launch does every stage; its time is reported under "count"
         const size_t zero = L.off_stats + 2 * DBSCAN_MAX_D * sizeof(int);   // Ctrl + min/max
@@ -723,7 +727,7 @@ int dbscan_profile_end(float *stage_ms, int32_t max_stages, int64_t *calls,
             if (c.fused)
                 launches += i == 1 ? 1 : 0;   // the one fused kernel, in the count stage
             else
-                launches += stage_launches(c.allow, c.d, i) + ((c.cull & 1) && i == 0 ? 2 : 0) +
+                launches += stage_launches(c.allow, c.d, c.ntiles, i) + ((c.cull & 1) && i == 0 ? 2 : 0) +
                             ((c.cull & 2) && i == 2 ? 3 : 0);
         }
         for (int i = 0; i <= c.stages; ++i) cudaEventDestroy(c.ev[i]);

@@ -832,6 +832,24 @@ cudaError_t launch_count(const Work &w, const Layout &L, cudaStream_t s) {
     return launch_count_tc(w, L, s);
 }
 
+// Union bands of a call: the three of tc_schedule.h, or for at most
+// ONE_BAND_MAX_TILES tiles a single band (every tile distance from 1): every
+// band costs a compression, a tile-root snapshot and each sweep's start-up,
+// and with few tiles a band holds too little work to repay them.
+#ifndef ONE_BAND_MAX_TILES
+#define ONE_BAND_MAX_TILES 2048
+#endif
+int union_band_count(int64_t ntiles) { return ntiles <= ONE_BAND_MAX_TILES ? 1 : UNION_BANDS; }
+static void union_band(int64_t ntiles, int bd, int &lo, int &hi) {
+    if (union_band_count(ntiles) == 1) {
+        lo = 1;
+        hi = -1;
+    } else {
+        lo = kUnionBandEdges[bd];
+        hi = kUnionBandEdges[bd + 1];
+    }
+}
+
 cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
     SweepArgs a{};
     a.srank = L.rank; a.sworld = L.world;
@@ -863,10 +881,11 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
     // parent a root, so the first snapshot needs no compression).  The
     // kernels of the path not taken return at once.
     const unsigned rgrid = (unsigned)((L.ntiles + 7) / 8);
+    const int nbands = union_band_count(L.ntiles);
     // CUDA-core path
     a.ulo = 0; a.uhi = -1;
     a.band = 1; a.troot = w.troot;
-    for (int bd = 0; bd < UNION_BANDS; ++bd) {
+    for (int bd = 0; bd < nbands; ++bd) {
         cudaError_t e;
         if (bd > 0) {
             k_compress<<<grid, 256, 0, s>>>(w.ctrl, w.parent, 0);
@@ -874,13 +893,12 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
         }
         k_tile_roots<<<rgrid, 256, 0, s>>>(w.ctrl, w.parent, w.troot, 0);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        a.blo = kUnionBandEdges[bd];
-        a.bhi = kUnionBandEdges[bd + 1];
+        union_band(L.ntiles, bd, a.blo, a.bhi);
         a.ctr = &w.ctrl->unit_ctr[CTR_UNION0 + bd];
         if ((e = dispatch<SWEEP_UNION>(a, L.d, s)) != cudaSuccess) return e;
     }
     // tensor-core path
-    for (int bd = 0; bd < UNION_BANDS; ++bd) {
+    for (int bd = 0; bd < nbands; ++bd) {
         cudaError_t e;
         if (bd > 0) {
             k_compress<<<grid, 256, 0, s>>>(w.ctrl, w.parent, 1);
@@ -888,7 +906,9 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
         }
         k_tile_roots<<<rgrid, 256, 0, s>>>(w.ctrl, w.parent, w.troot, 1);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        e = launch_union_tc_band(w, L, bd, kUnionBandEdges[bd], kUnionBandEdges[bd + 1], s);
+        int lo, hi;
+        union_band(L.ntiles, bd, lo, hi);
+        e = launch_union_tc_band(w, L, bd, lo, hi, s);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -2,12 +2,13 @@
 
 `sched_check.cpp` includes the schedule header the kernel uses
 (`all_pairs_distance_gb300/csrc/tc_schedule.h`), enumerates every unit of the
-count's triangle, the union's distance bands and the border's rectangle, with
-one and with two row blocks per unit, over tile counts that span several
-column chunks (512 tiles; 128 in the union's last band over at most 2,048
-tiles) and ragged tails, and checks that each tile pair the
-sweep must evaluate is evaluated exactly once (the union leaves out the
-diagonal, which the tile-local union covers) and no other pair is.
+count's triangle, the union's distance bands (three, or one for small
+problems) and the border's rectangle, with one and with two row blocks per
+unit, over tile counts that span several column chunks (512 tiles; 128 in the
+union's last band over at most 2,048 tiles) and ragged tails, and checks that
+each tile pair the sweep must evaluate is evaluated exactly once (the union
+leaves out the diagonal, which the tile-local union covers) and no other pair
+is.
 """
 import os
 import shutil
