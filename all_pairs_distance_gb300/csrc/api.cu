@@ -275,11 +275,11 @@ static int stage_launches(unsigned allow, int d, int64_t ntiles, int stage) {
     // (each CUDA-core sweep: one launch per form of the neighbour test)
     case 1: return 2 + ntc;
     case 2: return 4 + umma;
-    // tile-local union, then per band on CUDA cores: the sweep (two forms), a
-    // tile-root snapshot and (after the first) a compression, and per
-    // tensor-core band: a launch per kind, a tile-root snapshot and (after the
-    // first) a compression
-    case 3: return 1 + nb * 3 + (nb - 1) + nb * (ntc + 1) + (nb - 1);
+    // tile-local union, then per band on CUDA cores (three): the sweep (two
+    // forms), a tile-root snapshot and (after the first) a compression, and
+    // per tensor-core band (nb): a launch per kind, a tile-root snapshot and
+    // (after the first) a compression
+    case 3: return 1 + UNION_BANDS * 3 + (UNION_BANDS - 1) + nb * (ntc + 1) + (nb - 1);
     case 4: return 2;
     case 5: return umma + 2 + ntc;
     default: return 1;

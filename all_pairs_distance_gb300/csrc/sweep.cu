@@ -832,10 +832,13 @@ cudaError_t launch_count(const Work &w, const Layout &L, cudaStream_t s) {
     return launch_count_tc(w, L, s);
 }
 
-// Union bands of a call: the three of tc_schedule.h, or for at most
-// ONE_BAND_MAX_TILES tiles a single band (every tile distance from 1): every
-// band costs a compression, a tile-root snapshot and each sweep's start-up,
-// and with few tiles a band holds too little work to repay them.
+// Tensor-core union bands of a call: the three of tc_schedule.h, or for at
+// most ONE_BAND_MAX_TILES tiles a single band (every tile distance from 1):
+// every band costs a compression, a tile-root snapshot and the sweep's
+// start-up, and with few tiles a band holds too little work to repay them
+// (100k x 2 union 0.44 -> 0.38 ms).  The CUDA-core union keeps three bands:
+// its sweeps gain more from the compressions between them (forced onto CUDA
+// cores, 100k x 2 union 1.37 -> 1.80 ms with one band).
 #ifndef ONE_BAND_MAX_TILES
 #define ONE_BAND_MAX_TILES 2048
 #endif
@@ -881,11 +884,10 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
     // parent a root, so the first snapshot needs no compression).  The
     // kernels of the path not taken return at once.
     const unsigned rgrid = (unsigned)((L.ntiles + 7) / 8);
-    const int nbands = union_band_count(L.ntiles);
     // CUDA-core path
     a.ulo = 0; a.uhi = -1;
     a.band = 1; a.troot = w.troot;
-    for (int bd = 0; bd < nbands; ++bd) {
+    for (int bd = 0; bd < UNION_BANDS; ++bd) {
         cudaError_t e;
         if (bd > 0) {
             k_compress<<<grid, 256, 0, s>>>(w.ctrl, w.parent, 0);
@@ -893,11 +895,13 @@ cudaError_t launch_union(const Work &w, const Layout &L, cudaStream_t s) {
         }
         k_tile_roots<<<rgrid, 256, 0, s>>>(w.ctrl, w.parent, w.troot, 0);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        union_band(L.ntiles, bd, a.blo, a.bhi);
+        a.blo = kUnionBandEdges[bd];
+        a.bhi = kUnionBandEdges[bd + 1];
         a.ctr = &w.ctrl->unit_ctr[CTR_UNION0 + bd];
         if ((e = dispatch<SWEEP_UNION>(a, L.d, s)) != cudaSuccess) return e;
     }
     // tensor-core path
+    const int nbands = union_band_count(L.ntiles);
     for (int bd = 0; bd < nbands; ++bd) {
         cudaError_t e;
         if (bd > 0) {
